@@ -1,0 +1,215 @@
+"""Hybrid sliding-window / global GQA attention with a learnable sink, on B300.
+
+The compute lives in ``libhattn.so`` (hand-written sm_103a CUDA behind the C
+ABI of ``include/hattn.h``).  This package is its Python binding:
+
+* ``hattn_prefill``, ``hattn_rope_kv_append``, ``hattn_decode``, ... -- the C
+  entry points under the same names, arguments marshalled with ctypes
+  (tensors become their device pointers); they return the status code.
+* ``prefill``, ``rope_kv_append``, ``decode`` -- conveniences that take torch
+  CUDA tensors, allocate the outputs and the workspace with torch, call the C
+  entry point on torch's current stream and raise on a non-zero status.
+
+There is no fallback: if the library is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhattn.so")
+
+HATTN_OK = 0
+HATTN_ERR_INVALID_ARG = 1
+HATTN_ERR_UNSUPPORTED = 2
+HATTN_ERR_CUDA = 3
+HATTN_ERR_RING_TOO_SMALL = 4
+HATTN_ERR_TIMEOUT = 5
+HATTN_ERR_WORKSPACE = 6
+
+D_QK, D_V, ROPE_DIM = 192, 128, 64
+
+# name -> (restype, argtypes)
+_P, _I, _L, _F, _Z = (ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_float,
+                      ctypes.c_size_t)
+SIGNATURES = {
+    "hattn_version": (_I, []),
+    "hattn_status_string": (ctypes.c_char_p, [_I]),
+    "hattn_prefill_workspace_size": (_Z, [_L, _I, _I]),
+    "hattn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _L, _I, _I, _I, _I, _I, _I, _F, _I, _F,
+                           _P, _Z, _P]),
+    "hattn_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "hattn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "hattn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                          _F, _F, _P, _Z, _P]),
+    "hattn_check_device_status": (_I, [_P]),
+    "hattn_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
+    "hattn_selftest_lost_arrival": (_I, [_P]),
+}
+
+_lib = None
+
+
+class HattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libhattn.so (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libhattn.so not found at {path}; build it with "
+                               "`python -m global_attention_sinks_gqa_b300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr() if x.numel() else None
+    return int(x)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# ---------------------------------------------------------------- C names
+def hattn_version() -> int:
+    return load_library().hattn_version()
+
+
+def status_string(status: int) -> str:
+    return load_library().hattn_status_string(int(status)).decode()
+
+
+hattn_status_string = status_string
+
+
+def hattn_prefill_workspace_size(total_tokens, hkv, dqk=D_QK) -> int:
+    return load_library().hattn_prefill_workspace_size(int(total_tokens), int(hkv), int(dqk))
+
+
+def hattn_prefill(q, k, v, sink, out, lse, batch, cu_seqlens, total_tokens, max_seqlen, hq, hkv,
+                  dqk, dv, rope_dim, rope_base, window, softmax_scale, workspace, workspace_bytes,
+                  stream=None) -> int:
+    return load_library().hattn_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(out), _ptr(lse), int(batch), _ptr(cu_seqlens),
+        int(total_tokens), int(max_seqlen), int(hq), int(hkv), int(dqk), int(dv), int(rope_dim),
+        float(rope_base), int(window), float(softmax_scale), _ptr(workspace), int(workspace_bytes),
+        _stream(stream))
+
+
+def hattn_rope_kv_append(k_new, v_new, start_pos, k_cache, v_cache, B, T, hkv, dqk, dv, cap,
+                         is_ring, rope_dim, rope_base, stream=None) -> int:
+    return load_library().hattn_rope_kv_append(
+        _ptr(k_new), _ptr(v_new), _ptr(start_pos), _ptr(k_cache), _ptr(v_cache), int(B), int(T),
+        int(hkv), int(dqk), int(dv), int(cap), int(is_ring), int(rope_dim), float(rope_base),
+        _stream(stream))
+
+
+def hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window) -> int:
+    return load_library().hattn_decode_workspace_size(int(B), int(T), int(hq), int(hkv), int(dv),
+                                                      int(max_seqlen_k), int(window))
+
+
+def hattn_decode(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv, dqk, dv, cap,
+                 is_ring, window, max_seqlen_k, rope_dim, rope_base, softmax_scale, workspace,
+                 workspace_bytes, stream=None) -> int:
+    return load_library().hattn_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens_k), _ptr(sink), _ptr(out), _ptr(lse),
+        int(B), int(T), int(hq), int(hkv), int(dqk), int(dv), int(cap), int(is_ring), int(window),
+        int(max_seqlen_k), int(rope_dim), float(rope_base), float(softmax_scale), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
+
+
+def hattn_check_device_status(stream=None) -> int:
+    return load_library().hattn_check_device_status(_stream(stream))
+
+
+def hattn_set_wait_limit_ns(limit_ns: int) -> int:
+    return load_library().hattn_set_wait_limit_ns(int(limit_ns))
+
+
+def hattn_selftest_lost_arrival(stream=None) -> int:
+    return load_library().hattn_selftest_lost_arrival(_stream(stream))
+
+
+# ---------------------------------------------------------------- conveniences
+def _check(status: int, what: str):
+    if status != HATTN_OK:
+        raise HattnError(status, what)
+
+
+def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_base: float,
+            softmax_scale: float | None = None, out=None, lse=None, workspace=None,
+            with_lse: bool = True):
+    """One layer's prefill over packed sequences; returns (out, lse)."""
+    total, hq, dqk = q.shape
+    hkv, dv = k.shape[1], v.shape[2]
+    if softmax_scale is None:
+        softmax_scale = dqk ** -0.5
+    if out is None:
+        out = torch.empty((total, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((total, hq), dtype=torch.float32, device=q.device)
+    need = hattn_prefill_workspace_size(total, hkv, dqk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(hattn_prefill(q, k, v, sink, out, lse, cu_seqlens.numel() - 1, cu_seqlens, total,
+                         max_seqlen, hq, hkv, dqk, dv, ROPE_DIM, rope_base, window, softmax_scale,
+                         workspace, workspace.numel()), "hattn_prefill")
+    return out, lse
+
+
+def rope_kv_append(k_new, v_new, start_pos, k_cache, v_cache, *, is_ring: bool, rope_base: float):
+    B, T, hkv, dqk = k_new.shape
+    cap = k_cache.shape[2]
+    _check(hattn_rope_kv_append(k_new, v_new, start_pos, k_cache, v_cache, B, T, hkv, dqk,
+                                v_new.shape[3], cap, 1 if is_ring else 0, ROPE_DIM, rope_base),
+           "hattn_rope_kv_append")
+
+
+def decode(q, k_cache, v_cache, seqlens_k, sink, *, max_seqlen_k: int, window: int,
+           is_ring: bool, rope_base: float, softmax_scale: float | None = None, out=None,
+           lse=None, workspace=None, with_lse: bool = True):
+    """Decode / verify step for T = q.shape[1] tokens per sequence; returns (out, lse)."""
+    B, T, hq, dqk = q.shape
+    hkv, cap = k_cache.shape[1], k_cache.shape[2]
+    dv = v_cache.shape[3]
+    if softmax_scale is None:
+        softmax_scale = dqk ** -0.5
+    if out is None:
+        out = torch.empty((B, T, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((B, T, hq), dtype=torch.float32, device=q.device)
+    need = hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(hattn_decode(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv, dqk, dv,
+                        cap, 1 if is_ring else 0, window, max_seqlen_k, ROPE_DIM, rope_base,
+                        softmax_scale, workspace, workspace.numel() if workspace is not None else 0),
+           "hattn_decode")
+    return out, lse
+
+
+def check_device_status(stream=None):
+    _check(hattn_check_device_status(stream), "device status")

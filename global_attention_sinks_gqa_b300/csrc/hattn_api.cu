@@ -1,0 +1,294 @@
+// hattn_api.cu -- the extern "C" entry points declared in include/hattn.h.
+//
+// Host-side validation (nothing is launched on a bad argument), workspace
+// accounting, the device status word, and dispatch to the kernels.  The
+// library allocates no device memory; the status word is a file-scope
+// __device__ variable.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace hattn {
+
+namespace {
+
+__device__ unsigned int g_status_word;
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+constexpr int kMaxDevices = 64;
+unsigned long long g_wait_limit_ns[kMaxDevices];
+unsigned int* g_status_addr[kMaxDevices];
+std::mutex g_mu;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+// Device address of this device's status word (looked up once per device,
+// with that device current).
+bool device_ctl(DeviceCtl* ctl) {
+  const int dev = current_device();
+  if (dev < 0) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || !p) return false;
+    g_status_addr[dev] = static_cast<unsigned int*>(p);
+  }
+  ctl->status = g_status_addr[dev];
+  ctl->wait_limit_ns = g_wait_limit_ns[dev] ? g_wait_limit_ns[dev] : kDefaultWaitLimitNs;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shapes this build supports (the MiMo-V2-Flash attention layer and its
+// variants): dqk 192, dv 128, RoPE on 64 dims, G = hq/hkv a power of two <= 16.
+hattn_status_t check_heads(int hq, int hkv, int dqk, int dv, int rope_dim) {
+  if (hq <= 0 || hkv <= 0 || dqk <= 0 || dv <= 0 || rope_dim < 0) return HATTN_ERR_INVALID_ARG;
+  if (hq % hkv) return HATTN_ERR_INVALID_ARG;
+  const int G = hq / hkv;
+  if (dqk != kDqk || dv != kDv || rope_dim != kRopeDim) return HATTN_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return HATTN_ERR_UNSUPPORTED;
+  return HATTN_OK;
+}
+
+bool finite_positive(float x) { return isfinite(x) && x > 0.f; }
+
+}  // namespace
+
+void make_rope_freqs(float base, RopeFreqs* f) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < kRopeHalf; ++i) {
+    const double theta = pow(double(base), -2.0 * double(i) / double(kRopeDim));
+    const double turns = theta / two_pi;
+    const float hi = float(turns);
+    f->hi[i] = hi;
+    f->lo[i] = float(turns - double(hi));
+  }
+}
+
+namespace {
+
+__global__ void lost_arrival_kernel(const DeviceCtl ctl) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);  // one arrival expected; none is ever made
+    abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, ctl, reinterpret_cast<volatile int*>(&abort));
+}
+
+}  // namespace
+
+cudaError_t launch_lost_arrival_selftest(const DeviceCtl& ctl, cudaStream_t s) {
+  lost_arrival_kernel<<<1, 32, 0, s>>>(ctl);
+  return cudaGetLastError();
+}
+
+}  // namespace hattn
+
+using namespace hattn;
+
+extern "C" {
+
+int hattn_version(void) { return 100; }
+
+const char* hattn_status_string(hattn_status_t s) {
+  switch (s) {
+    case HATTN_OK: return "HATTN_OK";
+    case HATTN_ERR_INVALID_ARG: return "HATTN_ERR_INVALID_ARG";
+    case HATTN_ERR_UNSUPPORTED: return "HATTN_ERR_UNSUPPORTED";
+    case HATTN_ERR_CUDA: return "HATTN_ERR_CUDA";
+    case HATTN_ERR_RING_TOO_SMALL: return "HATTN_ERR_RING_TOO_SMALL";
+    case HATTN_ERR_TIMEOUT: return "HATTN_ERR_TIMEOUT";
+    case HATTN_ERR_WORKSPACE: return "HATTN_ERR_WORKSPACE";
+  }
+  return "HATTN_ERR_UNKNOWN";
+}
+
+size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk) {
+  if (total_tokens <= 0 || hkv <= 0 || dqk <= 0) return 0;
+  const size_t bytes = size_t(total_tokens) * size_t(hkv) * size_t(dqk) * 2;
+  return (bytes + 255) / 256 * 256;
+}
+
+hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const float* sink,
+                             void* out, float* lse, int batch, const int* cu_seqlens,
+                             long total_tokens, int max_seqlen, int hq, int hkv, int dqk, int dv,
+                             int rope_dim, float rope_base, int window, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
+  if (st != HATTN_OK) return st;
+  if (batch <= 0 || total_tokens < 0 || max_seqlen < 0 || window < 0) return HATTN_ERR_INVALID_ARG;
+  if (total_tokens > 2147483647L || max_seqlen > total_tokens) return HATTN_ERR_INVALID_ARG;
+  if (!finite_positive(rope_base) || !finite_positive(softmax_scale)) return HATTN_ERR_INVALID_ARG;
+  if (total_tokens == 0) return HATTN_OK;
+  if (!q || !k || !v || !sink || !out || !cu_seqlens) return HATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(workspace))
+    return HATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(sink) & 3u || reinterpret_cast<uintptr_t>(lse) & 3u ||
+      reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
+    return HATTN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < hattn_prefill_workspace_size(total_tokens, hkv, dqk))
+    return HATTN_ERR_WORKSPACE;
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrefillArgs a;
+  a.q = q;
+  a.k_rot = workspace;
+  a.v = v;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.cu_seqlens = cu_seqlens;
+  a.batch = batch;
+  a.total = total_tokens;
+  a.max_seqlen = max_seqlen;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.window = window >= max_seqlen ? 0 : window;  // a window covering every key is global
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  make_rope_freqs(rope_base, &a.freqs);
+  a.ctl = ctl;
+  if (launch_rope_keys_packed(k, workspace, cu_seqlens, batch, total_tokens, hkv, a.freqs, ctl, s) !=
+      cudaSuccess)
+    return HATTN_ERR_CUDA;
+  if (max_seqlen == 0) return HATTN_OK;
+  if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;
+  return HATTN_OK;
+}
+
+hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const int* start_pos,
+                                    void* k_cache, void* v_cache, int B, int T, int hkv, int dqk,
+                                    int dv, int cap, int is_ring, int rope_dim, float rope_base,
+                                    void* stream) {
+  hattn_status_t st = check_heads(hkv, hkv, dqk, dv, rope_dim);
+  if (st != HATTN_OK) return st;
+  if (B < 0 || T <= 0 || cap <= 0 || T > cap || (is_ring != 0 && is_ring != 1))
+    return HATTN_ERR_INVALID_ARG;
+  if (!finite_positive(rope_base)) return HATTN_ERR_INVALID_ARG;
+  if (B == 0) return HATTN_OK;
+  if (!k_new || !v_new || !start_pos || !k_cache || !v_cache) return HATTN_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(start_pos) & 3u))
+    return HATTN_ERR_INVALID_ARG;
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  RopeFreqs f;
+  make_rope_freqs(rope_base, &f);
+  if (launch_kv_append(k_new, v_new, start_pos, k_cache, v_cache, B, T, hkv, cap, is_ring, f,
+                       ctl, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return HATTN_ERR_CUDA;
+  return HATTN_OK;
+}
+
+size_t hattn_decode_workspace_size(int B, int T, int hq, int hkv, int dv, int max_seqlen_k,
+                                   int window) {
+  (void)hkv;
+  (void)dv;
+  if (B <= 0 || T <= 0 || hq <= 0 || max_seqlen_k <= 0 || window < 0) return 0;
+  int chunk = 0;
+  const int nsplit = decode_num_splits(max_seqlen_k, T, window, &chunk);
+  return decode_workspace_bytes(B, T, hq, nsplit);
+}
+
+hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int* seqlens_k, const float* sink, void* out, float* lse, int B,
+                            int T, int hq, int hkv, int dqk, int dv, int cap, int is_ring,
+                            int window, int max_seqlen_k, int rope_dim, float rope_base,
+                            float softmax_scale, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
+  if (st != HATTN_OK) return st;
+  if (B < 0 || T <= 0 || cap <= 0 || window < 0 || max_seqlen_k < T ||
+      (is_ring != 0 && is_ring != 1))
+    return HATTN_ERR_INVALID_ARG;
+  if (T > 4 || (hq / hkv) * T > 64) return HATTN_ERR_UNSUPPORTED;
+  if (is_ring && window == 0) return HATTN_ERR_INVALID_ARG;  // a ring only holds a window
+  if (is_ring && cap < window + T - 1) return HATTN_ERR_RING_TOO_SMALL;
+  if (!is_ring && max_seqlen_k > cap) return HATTN_ERR_INVALID_ARG;
+  if (!finite_positive(rope_base) || !finite_positive(softmax_scale)) return HATTN_ERR_INVALID_ARG;
+  if (B == 0) return HATTN_OK;
+  if (!q || !k_cache || !v_cache || !seqlens_k || !sink || !out) return HATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) || (reinterpret_cast<uintptr_t>(sink) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return HATTN_ERR_INVALID_ARG;
+  DecodeArgs a;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.seqlens = seqlens_k;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.T = T;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.cap = cap;
+  a.is_ring = is_ring;
+  a.window = window;
+  a.max_seqlen_k = max_seqlen_k;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  make_rope_freqs(rope_base, &a.freqs);
+  a.nsplit = decode_num_splits(max_seqlen_k, T, window, &a.chunk);
+  const size_t need = decode_workspace_bytes(B, T, hq, a.nsplit);
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
+  if (need) {
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return HATTN_ERR_WORKSPACE;
+    const size_t rows = size_t(B) * hq * T * a.nsplit;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          (rows * kDv * sizeof(float) + 255) / 256 * 256);
+  }
+  if (!device_ctl(&a.ctl)) return HATTN_ERR_CUDA;
+  if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return HATTN_ERR_CUDA;
+  return HATTN_OK;
+}
+
+hattn_status_t hattn_check_device_status(void* stream) {
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HATTN_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, ctl.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HATTN_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(ctl.status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return HATTN_ERR_CUDA;
+  }
+  return static_cast<hattn_status_t>(word);
+}
+
+hattn_status_t hattn_set_wait_limit_ns(unsigned long long limit_ns) {
+  const int dev = current_device();
+  if (dev < 0) return HATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_wait_limit_ns[dev] = limit_ns;
+  return HATTN_OK;
+}
+
+hattn_status_t hattn_selftest_lost_arrival(void* stream) {
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  if (launch_lost_arrival_selftest(ctl, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return HATTN_ERR_CUDA;
+  return HATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// hattn_internal.h -- declarations shared between the C-ABI layer and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hattn.h"
+
+namespace hattn {
+
+constexpr int kDqk = 192;
+constexpr int kDv = 128;
+constexpr int kRopeDim = 64;
+constexpr int kRopeHalf = 32;
+
+// Where kernels report failures, and how long a device-side wait may last.
+struct DeviceCtl {
+  unsigned int* status;          // device address of the status word
+  unsigned long long wait_limit_ns;
+};
+
+// theta_i / (2 pi) for the 32 RoPE frequencies as double-float pairs.
+struct RopeFreqs {
+  float hi[kRopeHalf];
+  float lo[kRopeHalf];
+};
+
+void make_rope_freqs(float base, RopeFreqs* f);
+
+// ---- rope / append (rope_append.cu) --------------------------------------
+cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
+                                    long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
+                                    cudaStream_t s);
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* start_pos,
+                             void* k_cache, void* v_cache, int B, int T, int hkv, int cap,
+                             int is_ring, const RopeFreqs& f, const DeviceCtl& ctl,
+                             cudaStream_t s);
+
+// ---- prefill (prefill_tc.cu) ------------------------------------------------
+struct PrefillArgs {
+  const void* q;
+  const void* k_rot;
+  const void* v;
+  const float* sink;
+  void* out;
+  float* lse;
+  const int* cu_seqlens;
+  int batch;
+  long total;
+  int max_seqlen;
+  int hq, hkv;
+  int window;
+  float scale_log2;  // softmax_scale * log2(e)
+  RopeFreqs freqs;
+  DeviceCtl ctl;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+// ---- decode (decode.cu) -----------------------------------------------------
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int* seqlens;
+  const float* sink;
+  void* out;
+  float* lse;
+  int B, T, hq, hkv, cap, is_ring, window, max_seqlen_k;
+  float scale_log2;
+  RopeFreqs freqs;
+  float* part_o;    // [B, hq, T, nsplit, dv] fp32 (nsplit > 1 only)
+  float* part_lse;  // [B, hq, T, nsplit] fp32, log2 domain
+  int nsplit;
+  int chunk;        // keys per split
+  DeviceCtl ctl;
+};
+int decode_num_splits(int max_seqlen_k, int T, int window, int* chunk);
+size_t decode_workspace_bytes(int B, int T, int hq, int nsplit);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// ---- status ------------------------------------------------------------------
+cudaError_t launch_lost_arrival_selftest(const DeviceCtl& ctl, cudaStream_t s);
+
+}  // namespace hattn

@@ -1,0 +1,141 @@
+// rope_append.cu -- partial RoPE of key rows and the KV-cache append.
+//
+// MiMo-V2-Flash paper review, section 3.1: RoPE is applied to the first 64 of
+// the 192 Q/K dims; section 4: base 10K (SWA layers) / 5M (GA layers).
+// plmsmile notes, MiMo-V2-Flash "local window": an SWA layer's KV cache does
+// not grow with the history (a ring of `cap` slots here, slot = pos % cap);
+// a GA layer's cache grows (slot = pos).
+//
+// Rotated keys are stored mixed-precision: dims 0..63 (the rotated ones) as
+// IEEE fp16, dims 64..191 unchanged as bf16.  fp16 keeps 11 significant bits
+// of the rotated values where bf16 keeps 8, which holds the logit error of
+// the bf16/fp16 tensor-core path to a few 1e-4 (rotation changes the values,
+// so unlike the untouched dims they are no longer exact bf16 numbers).  A
+// rotated value beyond the fp16 range is recorded as HATTN_ERR_INVALID_ARG.
+//
+// Both kernels give one warp one 192-element key row: lane l < 24 holds the
+// 16-byte chunk of dims 8l..8l+7, so the rotated pair (i, i + 32) of a lane
+// l < 4 sits in lane l + 4 and one shuffle brings the partner over.  Loads
+// and stores are 128-bit and coalesced along the row.
+#include "common.cuh"
+
+namespace hattn {
+
+namespace {
+
+__device__ __forceinline__ uint4 rope_chunk(uint4 x, uint4 partner, int lane, int pos,
+                                            const RopeFreqs& f, bool* overflow) {
+  if (lane >= 8) return x;
+  const bool first = lane < 4;  // dims i (first half) vs i + 32 (second half)
+  const int i0 = 8 * (lane & 3);
+  uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+  uint32_t ps[4] = {partner.x, partner.y, partner.z, partner.w};
+  uint32_t ys[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float2 a = unpack_bf16x2(xs[w]);
+    const float2 b = unpack_bf16x2(ps[w]);
+    const float2 cs0 = rope_cos_sin(pos, f.hi[i0 + 2 * w], f.lo[i0 + 2 * w]);
+    const float2 cs1 = rope_cos_sin(pos, f.hi[i0 + 2 * w + 1], f.lo[i0 + 2 * w + 1]);
+    float y0, y1;
+    if (first) {  // y[i] = x[i] c - x[i+32] s
+      y0 = a.x * cs0.x - b.x * cs0.y;
+      y1 = a.y * cs1.x - b.y * cs1.y;
+    } else {      // y[i+32] = x[i+32] c + x[i] s
+      y0 = a.x * cs0.x + b.x * cs0.y;
+      y1 = a.y * cs1.x + b.y * cs1.y;
+    }
+    if (fabsf(y0) > kF16Max || fabsf(y1) > kF16Max) *overflow = true;
+    ys[w] = pack_f16x2(y0, y1);
+  }
+  return make_uint4(ys[0], ys[1], ys[2], ys[3]);
+}
+
+// Rotate the key row at `src` (position pos) into `dst`.  Whole warp calls.
+// Returns true (on the lane concerned) if a rotated value left the fp16 range.
+__device__ __forceinline__ bool rope_key_row(const uint4* src, uint4* dst, int pos, int lane,
+                                             const RopeFreqs& f) {
+  uint4 x = make_uint4(0, 0, 0, 0);
+  if (lane < 24) x = __ldg(src + lane);
+  uint4 p;
+  p.x = __shfl_xor_sync(0xffffffffu, x.x, 4);
+  p.y = __shfl_xor_sync(0xffffffffu, x.y, 4);
+  p.z = __shfl_xor_sync(0xffffffffu, x.z, 4);
+  p.w = __shfl_xor_sync(0xffffffffu, x.w, 4);
+  bool overflow = false;
+  const uint4 y = rope_chunk(x, p, lane, pos, f, &overflow);
+  if (lane < 24) dst[lane] = y;
+  return overflow;
+}
+
+constexpr int kRowsPerBlock = 8;  // one warp per row
+
+__global__ void __launch_bounds__(256) rope_keys_packed_kernel(
+    const uint4* __restrict__ k, uint4* __restrict__ k_rot, const int* __restrict__ cu_seqlens,
+    int batch, long total, int hkv, const RopeFreqs f, const DeviceCtl ctl) {
+  const int lane = threadIdx.x & 31;
+  const long row = long(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
+  if (row >= total * hkv) return;
+  const long n = row / hkv;
+  // sequence holding packed token n: largest b with cu[b] <= n
+  int lo = 0, hi = batch;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu_seqlens + mid) <= n) lo = mid; else hi = mid - 1;
+  }
+  const int pos = int(n - __ldg(cu_seqlens + lo));
+  if (rope_key_row(k + row * 24, k_rot + row * 24, pos, lane, f))
+    record_status(ctl, HATTN_ERR_INVALID_ARG);
+}
+
+__global__ void __launch_bounds__(256) kv_append_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+    const int* __restrict__ start_pos, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+    int B, int T, int hkv, int cap, int is_ring, const RopeFreqs f, const DeviceCtl ctl) {
+  const int lane = threadIdx.x & 31;
+  const long row = long(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);  // (b, t, g)
+  if (row >= long(B) * T * hkv) return;
+  const int g = int(row % hkv);
+  const int t = int((row / hkv) % T);
+  const int b = int(row / (long(hkv) * T));
+  const int pos = __ldg(start_pos + b) + t;
+  if (pos < 0 || (!is_ring && pos >= cap)) {
+    if (lane == 0) record_status(ctl, HATTN_ERR_INVALID_ARG);
+    return;  // whole warp leaves together: no shuffle is pending
+  }
+  const long slot = is_ring ? (pos % cap) : pos;
+  const long crow = (long(b) * hkv + g) * cap + slot;
+  if (rope_key_row(k_new + row * 24, k_cache + crow * 24, pos, lane, f))
+    record_status(ctl, HATTN_ERR_INVALID_ARG);
+  if (lane < 16) v_cache[crow * 16 + lane] = __ldg(v_new + row * 16 + lane);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
+                                    long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
+                                    cudaStream_t s) {
+  const long rows = total * hkv;
+  if (rows == 0) return cudaSuccess;
+  const long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  rope_keys_packed_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
+      static_cast<const uint4*>(k), static_cast<uint4*>(k_rot), cu_seqlens, batch, total, hkv, f,
+      ctl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* start_pos,
+                             void* k_cache, void* v_cache, int B, int T, int hkv, int cap,
+                             int is_ring, const RopeFreqs& f, const DeviceCtl& ctl,
+                             cudaStream_t s) {
+  const long rows = long(B) * T * hkv;
+  if (rows == 0) return cudaSuccess;
+  const long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  kv_append_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), start_pos,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), B, T, hkv, cap, is_ring, f,
+      ctl);
+  return cudaGetLastError();
+}
+
+}  // namespace hattn

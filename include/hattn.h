@@ -1,0 +1,200 @@
+/*
+ * hattn.h -- C ABI of the hybrid sliding-window / global sink-attention
+ * library (libhattn.so, NVIDIA B300, sm_103a).
+ *
+ * What the library computes (one attention layer's forward pass):
+ *
+ *   MiMo-V2-Flash Technical Report paper review (xllm-io), section 3.1
+ *   "overall structure": causal GQA attention, 64 query heads over 8 KV heads
+ *   in sliding-window (SWA) layers and over 4 KV heads in global (GA)
+ *   layers, Q/K head dim 192, V head dim 128, RoPE on the first 64 dims,
+ *   window W = 128, SWA and GA layers interleaved 5:1.
+ *   Same page, section 4: RoPE base 10K for SWA layers, 5M for GA layers.
+ *   Same page, section 3.2, and the plmsmile notes on the MiMo series,
+ *   MiMo-V2-Flash "Learnable Attention Sink": each query head h has a
+ *   learnable logit s_h whose exp(s_h) joins the softmax denominator:
+ *
+ *     out[p,h] = sum_{j in J(p)} exp(z_pj - m) v_j / Z,
+ *     Z = sum_{j in J(p)} exp(z_pj - m) + exp(s_h - m),
+ *     lse[p,h] = m + ln Z   (natural log; the sink is included),
+ *     z_pj = scale * <RoPE(q_p, p), RoPE(k_j, j)>,
+ *     J(p) = { j : j <= p and (window == 0 or p - j < window) }.
+ *
+ *   plmsmile notes, MiMo-V2-Flash "local window": SWA layers keep a KV cache
+ *   that does not grow with the history (here a ring buffer); GA layers keep
+ *   a growing cache.  Same notes, MTP: drafted tokens are verified by the
+ *   main model in one parallel pass (here: 1 to 4 query tokens per sequence).
+ *
+ * Readings (the pages leave these open): the window holds W keys including
+ * the query itself; the sink is a raw logit, one fp32 per query head; query
+ * head h reads KV head h / (hq / hkv); RoPE turns the pairs (i, i + 32),
+ * i < 32, by pos * base^(-i / 32) ("rotate-half").
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *     and contiguous, 16-byte aligned.  bf16 is IEEE bfloat16 (uint16 bits).
+ *   - `stream` is a cudaStream_t (passed as void*); NULL = legacy default
+ *     stream.  Calls are asynchronous on that stream; the library does not
+ *     synchronise except in hattn_check_device_status().
+ *   - The library allocates no device memory.  Scratch space is a caller
+ *     buffer ("workspace") whose size the *_workspace_size() functions give.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     non-HATTN_OK status means nothing was launched (except HATTN_ERR_CUDA,
+ *     reported when a launch itself fails).  Nothing throws across the ABI.
+ *   - Supported shapes: dqk = 192, dv = 128, rope_dim = 64, hq % hkv == 0 and
+ *     G = hq / hkv in {1, 2, 4, 8, 16}.  Others return HATTN_ERR_UNSUPPORTED.
+ *   - Kernels never trap.  Device-side failures (a bounded wait that ran out)
+ *     are recorded in a device status word read by
+ *     hattn_check_device_status().
+ */
+#ifndef HATTN_H_
+#define HATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HATTN_OK = 0,
+  HATTN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misalignment */
+  HATTN_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shape set */
+  HATTN_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed */
+  HATTN_ERR_RING_TOO_SMALL = 4,/* ring cache cap < window + T - 1 */
+  HATTN_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out */
+  HATTN_ERR_WORKSPACE = 6      /* workspace missing or smaller than required */
+} hattn_status_t;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int hattn_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* hattn_status_string(hattn_status_t status);
+
+/*
+ * Bytes of workspace hattn_prefill() needs: the rotated keys,
+ * total_tokens * hkv * dqk 16-bit values, rounded up to 256 bytes.
+ */
+size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk);
+
+/*
+ * Prefill: one attention layer over packed variable-length sequences (a
+ * hybrid block is five window layers and one global layer, called in turn).
+ *
+ *   q          bf16 [total_tokens, hq, dqk]   un-rotated queries
+ *   k          bf16 [total_tokens, hkv, dqk]  un-rotated keys
+ *   v          bf16 [total_tokens, hkv, dv]
+ *   sink       fp32 [hq]                      sink logits s_h
+ *   out        bf16 [total_tokens, hq, dv]    written
+ *   lse        fp32 [total_tokens, hq]        written (may be NULL)
+ *   batch      number of sequences (>= 1)
+ *   cu_seqlens int32 [batch + 1] DEVICE; cu_seqlens[0] = 0, non-decreasing,
+ *              cu_seqlens[batch] = total_tokens.  RoPE positions restart at 0
+ *              in every sequence.
+ *   max_seqlen an upper bound of every sequence length (sizes the grid)
+ *   window     > 0: sliding window of `window` keys including the query;
+ *              0: global causal attention
+ *   rope_base  RoPE base (1e4 for SWA layers, 5e6 for GA layers)
+ *   softmax_scale  logit scale (1/sqrt(192) for this model)
+ *   workspace  DEVICE scratch of >= hattn_prefill_workspace_size() bytes,
+ *              overwritten with the rotated keys (dims 0..63 fp16, 64..191
+ *              bf16); out and lse must not overlap q, k, v or it.
+ * Queries and keys are rotated before the tensor-core products; the rotated
+ * dims are carried as fp16 (see hattn_rope_kv_append), so |RoPE(x)| must stay
+ * below 65504 on dims 0..63 (recorded as HATTN_ERR_INVALID_ARG otherwise).
+ */
+hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const float* sink,
+                             void* out, float* lse, int batch, const int* cu_seqlens,
+                             long total_tokens, int max_seqlen, int hq, int hkv, int dqk, int dv,
+                             int rope_dim, float rope_base, int window, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Rotate new keys and write them and their values into the KV cache.
+ *
+ *   k_new     bf16 [B, T, hkv, dqk]   un-rotated keys of the T new tokens
+ *   v_new     bf16 [B, T, hkv, dv]
+ *   start_pos int32 [B] DEVICE: position of token 0 of sequence b (>= 0)
+ *   k_cache   [B, hkv, cap, dqk] rotated keys, updated in place: dims 0..63
+ *             (the rotated ones) as IEEE fp16, dims 64..191 as bf16.  fp16
+ *             keeps 11 significant bits of the rotated values (bf16 keeps 8),
+ *             which holds the log-sum-exp error near 3e-4; a rotated value
+ *             beyond +-65504 is recorded as HATTN_ERR_INVALID_ARG in the
+ *             device status.
+ *   v_cache   bf16 [B, hkv, cap, dv]  updated in place
+ *   is_ring   1: slot = pos % cap (fixed-size SWA cache);
+ *             0: slot = pos (growing GA cache); a position >= cap is skipped
+ *             and recorded as HATTN_ERR_INVALID_ARG in the device status.
+ *   T         1..cap tokens per sequence
+ */
+hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const int* start_pos,
+                                    void* k_cache, void* v_cache, int B, int T, int hkv, int dqk,
+                                    int dv, int cap, int is_ring, int rope_dim, float rope_base,
+                                    void* stream);
+
+/*
+ * Bytes of workspace hattn_decode() needs for a batch whose longest
+ * sequence holds max_seqlen_k tokens (0 when one pass per KV head suffices).
+ */
+size_t hattn_decode_workspace_size(int B, int T, int hq, int hkv, int dv, int max_seqlen_k,
+                                   int window);
+
+/*
+ * Decode / MTP-verify step: the last T tokens of
+ * every sequence (positions seqlens_k[b] - T + t) attend over the cache,
+ * which must already hold them (call hattn_rope_kv_append() first).
+ *
+ *   q          bf16 [B, T, hq, dqk]    un-rotated queries
+ *   k_cache    [B, hkv, cap, dqk] rotated keys as written by
+ *              hattn_rope_kv_append() (dims 0..63 fp16, 64..191 bf16)
+ *   v_cache    bf16 [B, hkv, cap, dv]
+ *   seqlens_k  int32 [B] DEVICE: tokens of sequence b including the T new
+ *              ones; T <= seqlens_k[b] <= max_seqlen_k, and for a linear
+ *              cache seqlens_k[b] <= cap.
+ *   sink       fp32 [hq]
+ *   out        bf16 [B, T, hq, dv]     written
+ *   lse        fp32 [B, T, hq]         written (may be NULL)
+ *   T          1..4 query tokens per sequence
+ *   is_ring    1: key j lives in slot j % cap and cap >= window + T - 1 is
+ *              required (else HATTN_ERR_RING_TOO_SMALL); needs window > 0.
+ *              0: key j lives in slot j.
+ *   workspace  DEVICE scratch of >= hattn_decode_workspace_size() bytes
+ *              (may be NULL when that size is 0).
+ */
+hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int* seqlens_k, const float* sink, void* out, float* lse, int B,
+                            int T, int hq, int hkv, int dqk, int dv, int cap, int is_ring,
+                            int window, int max_seqlen_k, int rope_dim, float rope_base,
+                            float softmax_scale, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * Synchronise `stream`, then report (and clear) the device status word:
+ * HATTN_OK, HATTN_ERR_TIMEOUT (a bounded wait inside a kernel ran out) or
+ * HATTN_ERR_INVALID_ARG (a device-side index check skipped an access), or
+ * HATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+hattn_status_t hattn_check_device_status(void* stream);
+
+/*
+ * Set how long (nanoseconds) any single device-side wait may last before the
+ * kernel gives up with HATTN_ERR_TIMEOUT (default 2e9 = 2 s; 0 restores the
+ * default).  Applies to launches made after the call on the current device.
+ */
+hattn_status_t hattn_set_wait_limit_ns(unsigned long long limit_ns);
+
+/*
+ * Self-test of the failure path: launches one CTA that waits on an mbarrier
+ * nothing ever arrives at, bounded by the current wait limit.  The kernel
+ * returns normally; hattn_check_device_status() then reports
+ * HATTN_ERR_TIMEOUT.  Nothing faults, traps or hangs.
+ */
+hattn_status_t hattn_selftest_lost_arrival(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HATTN_H_ */

@@ -90,21 +90,17 @@ static void rope_apply(const double* x, double* y, int dim, int rope_dim, const 
 }
 
 /*
- * One attention row: query vector qr (already rotated), keys kr[j] (rotated),
- * values vr[j], n keys.  sink_on selects whether exp(sink) joins the
- * denominator.  Writes out[dv] and *lse.  With no key and no sink the row is
- * empty: out = 0 and lse = -inf.
+ * Finish one attention row from its logits z[0..n) (keys in position order):
+ * m = max(z, sink), Z = sum exp(z - m) (+ exp(sink - m)),
+ * out = sum exp(z_j - m) v_j / Z, lse = m + ln Z.  v_j is the bf16 value row
+ * of key j, widened exactly.  sink_on selects whether exp(sink) joins the
+ * denominator.  With no key and no sink the row is empty: out = 0, lse = -inf.
  */
-static void attend_row(const double* qr, const double* const* kr, const double* const* vr, long n,
-                       int dqk, int dv, double scale, double sink, int sink_on, double* z,
-                       double* out, double* lse) {
+static void softmax_row(const double* z, long n, const uint16_t* const* v_rows, int dv, double sink,
+                        int sink_on, double* out, double* lse) {
     double m = -INFINITY;
-    for (long j = 0; j < n; ++j) {
-        double acc = 0.0;
-        for (int d = 0; d < dqk; ++d) acc += qr[d] * kr[j][d];
-        z[j] = scale * acc;
+    for (long j = 0; j < n; ++j)
         if (z[j] > m) m = z[j];
-    }
     if (sink_on && sink > m) m = sink;
     for (int e = 0; e < dv; ++e) out[e] = 0.0;
     if (m == -INFINITY) {
@@ -115,11 +111,17 @@ static void attend_row(const double* qr, const double* const* kr, const double* 
     for (long j = 0; j < n; ++j) {
         double w = exp(z[j] - m);
         Z += w;
-        for (int e = 0; e < dv; ++e) out[e] += w * vr[j][e];
+        for (int e = 0; e < dv; ++e) out[e] += w * bf16_to_double(v_rows[j][e]);
     }
     if (sink_on) Z += exp(sink - m);
     for (int e = 0; e < dv; ++e) out[e] /= Z;
     *lse = m + log(Z);
+}
+
+static double dot(const double* a, const double* b, int n) {
+    double acc = 0.0;
+    for (int d = 0; d < n; ++d) acc += a[d] * b[d];
+    return acc;
 }
 
 static int omp_threads_used(int nthreads) {
@@ -194,20 +196,19 @@ int hattn_oracle_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v
     if (!th) return ORACLE_NO_MEM;
     int bad = 0;
     int nt = omp_threads_used(nthreads);
+    long maxkeys = (window > 0 && window < maxlen) ? window : maxlen;
 #pragma omp parallel num_threads(nt)
     {
         int half = rope_dim / 2 + 1;
         double* qd = (double*)malloc(sizeof(double) * (size_t)dqk);
-        double* qr = (double*)malloc(sizeof(double) * (size_t)dqk);
+        double* qr = (double*)malloc(sizeof(double) * (size_t)dqk * (size_t)G);
         double* c = (double*)malloc(sizeof(double) * (size_t)half);
         double* s = (double*)malloc(sizeof(double) * (size_t)half);
         double* kd = (double*)malloc(sizeof(double) * (size_t)dqk);
-        double* kbuf = (double*)malloc(sizeof(double) * (size_t)maxlen * (size_t)dqk);
-        double* vbuf = (double*)malloc(sizeof(double) * (size_t)maxlen * (size_t)dv);
-        const double** kr = (const double**)malloc(sizeof(double*) * (size_t)(maxlen + 1));
-        const double** vr = (const double**)malloc(sizeof(double*) * (size_t)(maxlen + 1));
-        double* z = (double*)malloc(sizeof(double) * (size_t)(maxlen + 1));
-        if (!qd || !qr || !c || !s || !kd || !kbuf || !vbuf || !kr || !vr || !z) {
+        double* kr = (double*)malloc(sizeof(double) * (size_t)dqk);
+        double* z = (double*)malloc(sizeof(double) * (size_t)(maxkeys + 1) * (size_t)G);
+        const uint16_t** vr = (const uint16_t**)malloc(sizeof(uint16_t*) * (size_t)(maxkeys + 1));
+        if (!qd || !qr || !c || !s || !kd || !kr || !z || !vr) {
 #pragma omp atomic write
             bad = ORACLE_NO_MEM;
         } else {
@@ -225,31 +226,32 @@ int hattn_oracle_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v
                 long lo = (window > 0 && p - window + 1 > 0) ? p - window + 1 : 0;
                 long nk = p - lo + 1;
                 for (int g = 0; g < hkv; ++g) {
-                    /* the visible keys of this KV head, rotated at their own positions */
-                    for (long j = lo; j <= p; ++j) {
-                        const uint16_t* ks = k + ((base_tok + j) * hkv + g) * (long)dqk;
-                        const uint16_t* vs = v + ((base_tok + j) * hkv + g) * (long)dv;
-                        for (int d = 0; d < dqk; ++d) kd[d] = bf16_to_double(ks[d]);
-                        rope_angles(j, rope_dim, th, c, s);
-                        rope_apply(kd, kbuf + (j - lo) * dqk, dqk, rope_dim, c, s);
-                        for (int e = 0; e < dv; ++e) vbuf[(j - lo) * dv + e] = bf16_to_double(vs[e]);
-                        kr[j - lo] = kbuf + (j - lo) * dqk;
-                        vr[j - lo] = vbuf + (j - lo) * dv;
-                    }
+                    /* the G query heads of this KV head, rotated at position p */
                     rope_angles(p, rope_dim, th, c, s);
                     for (int hh = 0; hh < G; ++hh) {
-                        int h = g * G + hh;
-                        const uint16_t* qs = q + (n * hq + h) * (long)dqk;
+                        const uint16_t* qs = q + (n * hq + g * G + hh) * (long)dqk;
                         for (int d = 0; d < dqk; ++d) qd[d] = bf16_to_double(qs[d]);
-                        rope_apply(qd, qr, dqk, rope_dim, c, s);
-                        attend_row(qr, kr, vr, nk, dqk, dv, scale, sink[h], 1, z,
-                                   out + (r * hq + h) * (long)dv, lse + r * hq + h);
+                        rope_apply(qd, qr + (long)hh * dqk, dqk, rope_dim, c, s);
+                    }
+                    /* logits against every visible key, rotated at its own position */
+                    for (long j = lo; j <= p; ++j) {
+                        const uint16_t* ks = k + ((base_tok + j) * hkv + g) * (long)dqk;
+                        for (int d = 0; d < dqk; ++d) kd[d] = bf16_to_double(ks[d]);
+                        rope_angles(j, rope_dim, th, c, s);
+                        rope_apply(kd, kr, dqk, rope_dim, c, s);
+                        for (int hh = 0; hh < G; ++hh)
+                            z[(long)hh * nk + (j - lo)] = scale * dot(qr + (long)hh * dqk, kr, dqk);
+                        vr[j - lo] = v + ((base_tok + j) * hkv + g) * (long)dv;
+                    }
+                    for (int hh = 0; hh < G; ++hh) {
+                        int h = g * G + hh;
+                        softmax_row(z + (long)hh * nk, nk, vr, dv, sink[h], 1,
+                                    out + (r * hq + h) * (long)dv, lse + r * hq + h);
                     }
                 }
             }
         }
-        free(qd); free(qr); free(c); free(s); free(kd); free(kbuf); free(vbuf);
-        free((void*)kr); free((void*)vr); free(z);
+        free(qd); free(qr); free(c); free(s); free(kd); free(kr); free(z); free((void*)vr);
     }
     free(th);
     return bad;
@@ -286,58 +288,57 @@ int hattn_oracle_decode(const uint16_t* q, const uint16_t* k_hist, const uint16_
     int bad = 0;
     int nt = omp_threads_used(nthreads);
     long nrows = (long)B * T;
+    long maxkeys = (window > 0 && window < Lmax) ? window : Lmax;
 #pragma omp parallel num_threads(nt)
     {
         int half = rope_dim / 2 + 1;
         double* qd = (double*)malloc(sizeof(double) * (size_t)dqk);
-        double* qr = (double*)malloc(sizeof(double) * (size_t)dqk);
+        double* qr = (double*)malloc(sizeof(double) * (size_t)dqk * (size_t)G);
         double* c = (double*)malloc(sizeof(double) * (size_t)half);
         double* s = (double*)malloc(sizeof(double) * (size_t)half);
         double* kd = (double*)malloc(sizeof(double) * (size_t)dqk);
-        double* kbuf = (double*)malloc(sizeof(double) * (size_t)Lmax * (size_t)dqk);
-        double* vbuf = (double*)malloc(sizeof(double) * (size_t)Lmax * (size_t)dv);
-        const double** kr = (const double**)malloc(sizeof(double*) * (size_t)(Lmax + 1));
-        const double** vr = (const double**)malloc(sizeof(double*) * (size_t)(Lmax + 1));
-        double* z = (double*)malloc(sizeof(double) * (size_t)(Lmax + 1));
-        if (!qd || !qr || !c || !s || !kd || !kbuf || !vbuf || !kr || !vr || !z) {
+        double* kr = (double*)malloc(sizeof(double) * (size_t)dqk);
+        double* z = (double*)malloc(sizeof(double) * (size_t)(maxkeys + 1) * (size_t)G);
+        const uint16_t** vr = (const uint16_t**)malloc(sizeof(uint16_t*) * (size_t)(maxkeys + 1));
+        if (!qd || !qr || !c || !s || !kd || !kr || !z || !vr) {
 #pragma omp atomic write
             bad = ORACLE_NO_MEM;
         } else {
 #pragma omp for schedule(dynamic, 1)
             for (long r = 0; r < nrows; ++r) {
-                int b = (int)(r / T), t = (int)(r % T);
+                int b = (int)(r / T);
                 long L = seqlens[b];
-                long p = L - T + t;
+                long p = L - T + (r % T);
                 long lo = (window > 0 && p - window + 1 > 0) ? p - window + 1 : 0;
                 if (lo < key_lo) lo = key_lo;
                 long hi = p; /* inclusive */
                 if (key_hi >= 0 && hi > key_hi - 1) hi = key_hi - 1;
                 long nk = hi >= lo ? hi - lo + 1 : 0;
                 for (int g = 0; g < hkv; ++g) {
-                    for (long j = lo; j <= hi; ++j) {
-                        const uint16_t* ks = k_hist + (((long)b * Lmax + j) * hkv + g) * (long)dqk;
-                        const uint16_t* vs = v_hist + (((long)b * Lmax + j) * hkv + g) * (long)dv;
-                        for (int d = 0; d < dqk; ++d) kd[d] = bf16_to_double(ks[d]);
-                        rope_angles(j, rope_dim, th, c, s);
-                        rope_apply(kd, kbuf + (j - lo) * dqk, dqk, rope_dim, c, s);
-                        for (int e = 0; e < dv; ++e) vbuf[(j - lo) * dv + e] = bf16_to_double(vs[e]);
-                        kr[j - lo] = kbuf + (j - lo) * dqk;
-                        vr[j - lo] = vbuf + (j - lo) * dv;
-                    }
                     rope_angles(p, rope_dim, th, c, s);
                     for (int hh = 0; hh < G; ++hh) {
-                        int h = g * G + hh;
-                        const uint16_t* qs = q + ((r * hq) + h) * (long)dqk;
+                        const uint16_t* qs = q + ((r * hq) + g * G + hh) * (long)dqk;
                         for (int d = 0; d < dqk; ++d) qd[d] = bf16_to_double(qs[d]);
-                        rope_apply(qd, qr, dqk, rope_dim, c, s);
-                        attend_row(qr, kr, vr, nk, dqk, dv, scale, sink[h], sink_on, z,
-                                   out + (r * hq + h) * (long)dv, lse + r * hq + h);
+                        rope_apply(qd, qr + (long)hh * dqk, dqk, rope_dim, c, s);
+                    }
+                    for (long j = lo; j <= hi; ++j) {
+                        const uint16_t* ks = k_hist + (((long)b * Lmax + j) * hkv + g) * (long)dqk;
+                        for (int d = 0; d < dqk; ++d) kd[d] = bf16_to_double(ks[d]);
+                        rope_angles(j, rope_dim, th, c, s);
+                        rope_apply(kd, kr, dqk, rope_dim, c, s);
+                        for (int hh = 0; hh < G; ++hh)
+                            z[(long)hh * nk + (j - lo)] = scale * dot(qr + (long)hh * dqk, kr, dqk);
+                        vr[j - lo] = v_hist + (((long)b * Lmax + j) * hkv + g) * (long)dv;
+                    }
+                    for (int hh = 0; hh < G; ++hh) {
+                        int h = g * G + hh;
+                        softmax_row(z + (long)hh * nk, nk, vr, dv, sink[h], sink_on,
+                                    out + (r * hq + h) * (long)dv, lse + r * hq + h);
                     }
                 }
             }
         }
-        free(qd); free(qr); free(c); free(s); free(kd); free(kbuf); free(vbuf);
-        free((void*)kr); free((void*)vr); free(z);
+        free(qd); free(qr); free(c); free(s); free(kd); free(kr); free(z); free((void*)vr);
     }
     free(th);
     return bad;

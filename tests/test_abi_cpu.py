@@ -1,0 +1,133 @@
+"""The C-ABI library loads, exports every entry point include/hattn.h
+declares, and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import global_attention_sinks_gqa_b300 as ha
+from global_attention_sinks_gqa_b300 import build as hbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hbuild.build()
+    return ha.load_library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "hattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hattn_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert "hattn_prefill" in names and "hattn_decode" in names
+    assert "hattn_rope_kv_append" in names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in ha.SIGNATURES, n
+
+
+def test_version_and_status_strings(lib):
+    assert ha.hattn_version() >= 100
+    for code, name in [(0, "HATTN_OK"), (1, "HATTN_ERR_INVALID_ARG"),
+                       (2, "HATTN_ERR_UNSUPPORTED"), (4, "HATTN_ERR_RING_TOO_SMALL"),
+                       (5, "HATTN_ERR_TIMEOUT"), (6, "HATTN_ERR_WORKSPACE")]:
+        assert ha.status_string(code) == name
+
+
+def test_workspace_sizes(lib):
+    assert ha.hattn_prefill_workspace_size(32768, 8, 192) == 32768 * 8 * 192 * 2
+    assert ha.hattn_prefill_workspace_size(3, 1, 192) == 1280  # 1152 rounded to 256
+    # a ring window fits one chunk: no workspace
+    assert ha.hattn_decode_workspace_size(64, 4, 64, 8, 128, 65536, 128) == 0
+    n = ha.hattn_decode_workspace_size(64, 4, 64, 4, 128, 65536, 0)
+    rows = 64 * 64 * 4 * 32  # 32 chunks of 2048 keys
+    assert n == rows * 128 * 4 + rows * 4
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null "device pointer" never dereferenced
+
+
+def _prefill(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, sink=FAKE, out=FAKE, lse=FAKE, batch=1,
+                cu_seqlens=FAKE, total_tokens=512, max_seqlen=512, hq=8, hkv=1, dqk=192, dv=128,
+                rope_dim=64, rope_base=1e4, window=128, softmax_scale=0.07, workspace=FAKE,
+                workspace_bytes=512 * 192 * 2, stream=0)
+    args.update(kw)
+    return ha.hattn_prefill(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hkv=3), ha.HATTN_ERR_INVALID_ARG),
+    (dict(dqk=128), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(dv=64), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(rope_dim=32), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(hq=64, hkv=2), ha.HATTN_ERR_UNSUPPORTED),      # G = 32
+    (dict(q=None), ha.HATTN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), ha.HATTN_ERR_INVALID_ARG),        # misaligned
+    (dict(window=-1), ha.HATTN_ERR_INVALID_ARG),
+    (dict(softmax_scale=0.0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(rope_base=float("nan")), ha.HATTN_ERR_INVALID_ARG),
+    (dict(max_seqlen=513), ha.HATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=100), ha.HATTN_ERR_WORKSPACE),
+    (dict(workspace=None), ha.HATTN_ERR_WORKSPACE),
+    (dict(batch=0), ha.HATTN_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_bad_arguments(lib, kw, code):
+    assert _prefill(**kw) == code
+
+
+def _decode(**kw):
+    args = dict(q=FAKE, k_cache=FAKE, v_cache=FAKE, seqlens_k=FAKE, sink=FAKE, out=FAKE,
+                lse=FAKE, B=64, T=4, hq=64, hkv=8, dqk=192, dv=128, cap=131, is_ring=1,
+                window=128, max_seqlen_k=65536, rope_dim=64, rope_base=1e4, softmax_scale=0.07,
+                workspace=None, workspace_bytes=0, stream=0)
+    args.update(kw)
+    return ha.hattn_decode(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cap=130), ha.HATTN_ERR_RING_TOO_SMALL),          # needs W + T - 1 = 131
+    (dict(cap=127, T=1), ha.HATTN_ERR_RING_TOO_SMALL),
+    (dict(T=5), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(T=0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(is_ring=1, window=0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(is_ring=0, window=0, hkv=4, cap=1000, max_seqlen_k=2000), ha.HATTN_ERR_INVALID_ARG),
+    (dict(is_ring=0, window=0, hkv=4, cap=65536), ha.HATTN_ERR_WORKSPACE),
+    (dict(hq=64, hkv=2), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(max_seqlen_k=3), ha.HATTN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 4), ha.HATTN_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert _decode(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(T=200, cap=131), ha.HATTN_ERR_INVALID_ARG),
+    (dict(is_ring=2), ha.HATTN_ERR_INVALID_ARG),
+    (dict(dqk=64), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(k_cache=None), ha.HATTN_ERR_INVALID_ARG),
+])
+def test_append_rejects_bad_arguments(lib, kw, code):
+    args = dict(k_new=FAKE, v_new=FAKE, start_pos=FAKE, k_cache=FAKE, v_cache=FAKE, B=64, T=4,
+                hkv=8, dqk=192, dv=128, cap=131, is_ring=1, rope_dim=64, rope_base=1e4, stream=0)
+    args.update(kw)
+    assert ha.hattn_rope_kv_append(**args) == code
+
+
+def test_oracle_is_not_reachable_from_the_product():
+    """The product package never imports the oracle."""
+    pkg = os.path.join(ROOT, "global_attention_sinks_gqa_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, f
+                assert "hattn_oracle" not in txt, f

@@ -1,0 +1,281 @@
+"""CUDA path vs the fp64 oracle, element by element, on the same seeded inputs.
+
+Small cases are compared in full; the full-size workloads are compared on
+sampled rows (rows are independent, so a sampled row is exact).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import global_attention_sinks_gqa_b300 as ha
+import oracle
+import synth
+from gpu_util import compare, fill_cache, gpu_prefill, oracle_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ prefill
+def test_prefill_tiny_swa_config():
+    """batch 1, seq 512, 8 query heads / 1 KV head, W = 128, base 1e4, seed 0."""
+    cfg = synth.CONFIGS["tiny_swa"]
+    c = synth.prefill_case(cfg["seqlens"], cfg["hq"], cfg["hkv"], window=cfg["window"],
+                           rope_base=cfg["rope_base"], seed=cfg["seed"])
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, "tiny swa")
+
+
+RAGGED = [1, 127, 128, 129, 255, 1000, 3, 16, 17]
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("window,base", [(128, 1e4), (0, 5e6)])
+def test_prefill_ragged_varlen(G, window, base):
+    c = synth.prefill_case(RAGGED, 2 * G, 2, window=window, rope_base=base, seed=100 + G)
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"ragged G={G} W={window}")
+
+
+@pytest.mark.parametrize("window", [1, 2, 7, 16, 100, 200, 255, 256, 257, 300, 1000])
+def test_prefill_window_widths(window):
+    c = synth.prefill_case([700, 301], 16, 2, window=window, rope_base=1e4, seed=200 + window)
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"W={window}")
+
+
+def test_prefill_window_covering_sequence_is_global():
+    c = synth.prefill_case([600], 8, 1, window=600, rope_base=1e4, seed=300)
+    out_w, lse_w = gpu_prefill(c)
+    c.window = 0
+    out_g, lse_g = gpu_prefill(c)
+    assert torch.equal(out_w, out_g) and torch.equal(lse_w, lse_g)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out_w, lse_w, o_ref, l_ref, "W=S")
+
+
+@pytest.mark.parametrize("window,base,sink_mean,sink_std", [
+    (128, 1e4, 6.0, 2.0),    # SWA: sink weight comparable to the window's mass
+    (0, 5e6, 8.0, 2.0),      # GA: sinks near the row log-sum-exp (~7-8 at S ~ 1500)
+    (0, 5e6, 12.0, 0.5),     # sink dominates
+    (64, 1e4, -30.0, 1.0),   # sink negligible
+])
+def test_prefill_sink_stress(window, base, sink_mean, sink_std):
+    c = synth.prefill_case([1500, 77], 16, 1, window=window, rope_base=base, seed=400,
+                           sink_mean=sink_mean, sink_std=sink_std)
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"sink N({sink_mean},{sink_std})")
+    # the sink is visible: dropping it would move the output by far more than the tolerance
+    o0, _ = oracle.prefill(c.q, c.k, c.v, torch.full((16,), -math.inf),
+                           c.cu_seqlens.tolist(), window=window, rope_base=base, scale=c.scale)
+    if sink_mean > 0:
+        assert np.abs(o0 - o_ref).max() > 0.1
+
+
+def test_prefill_repeatable_and_independent_of_lse_pointer():
+    c = synth.prefill_case([1000, 500], 64, 8, window=128, rope_base=1e4, seed=500)
+    out1, lse1 = gpu_prefill(c)
+    out2, lse2 = gpu_prefill(c)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    dev = torch.device("cuda")
+    out3, lse3 = ha.prefill(c.q.to(dev), c.k.to(dev), c.v.to(dev), c.sink.to(dev),
+                            c.cu_seqlens.to(dev), max_seqlen=1000, window=128, rope_base=1e4,
+                            softmax_scale=c.scale, with_lse=False)
+    torch.cuda.synchronize()
+    assert lse3 is None and torch.equal(out3, out1)
+
+
+def _sample_rows(S, n_mid, seed):
+    rs = np.random.RandomState(seed)
+    mid = rs.choice(np.arange(64, S - 64), size=n_mid, replace=False)
+    return np.unique(np.concatenate([np.arange(64), mid, np.arange(S - 64, S)]))
+
+
+@pytest.mark.parametrize("name,n_mid", [("swa_prefill_32k", 512), ("ga_prefill_32k", 96)])
+def test_prefill_full_size_sampled(name, n_mid):
+    """The bench workloads at full size (seq 32768, 64 query heads), sampled rows."""
+    cfg = synth.CONFIGS[name]
+    dev = torch.device("cuda")
+    c = synth.prefill_case(cfg["seqlens"], cfg["hq"], cfg["hkv"], window=cfg["window"],
+                           rope_base=cfg["rope_base"], seed=cfg["seed"], device=dev)
+    out, lse = ha.prefill(c.q, c.k, c.v, c.sink, c.cu_seqlens, max_seqlen=c.max_seqlen,
+                          window=c.window, rope_base=c.rope_base, softmax_scale=c.scale)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    S = c.total
+    rows = _sample_rows(S, n_mid, cfg["seed"])
+    if cfg["window"] == 0:  # a global row needs every earlier key: keep the oracle's work small
+        rows = np.unique(np.concatenate([np.arange(8), rows[rows >= S - 8],
+                                         _sample_rows(S, n_mid, 9)[64:64 + n_mid]]))
+    cpu = synth.PrefillCase(c.q.cpu(), c.k.cpu(), c.v.cpu(), c.sink.cpu(), c.cu_seqlens.cpu(),
+                            c.seqlens, c.hq, c.hkv, c.window, c.rope_base, c.scale)
+    o_ref, l_ref = oracle_prefill(cpu, rows=rows)
+    idx = torch.tensor(rows, device=dev)
+    compare(out[idx], lse[idx], o_ref, l_ref, name)
+
+
+# ------------------------------------------------------------------ append / decode
+def test_append_writes_rotated_keys_into_slots():
+    B, T, hkv, cap = 3, 4, 2, 131
+    g = torch.Generator().manual_seed(600)
+    k_new = torch.randn((B, T, hkv, 192), generator=g).to(torch.bfloat16)
+    v_new = torch.randn((B, T, hkv, 128), generator=g).to(torch.bfloat16)
+    start = [0, 129, 5000]  # ring wrap-around at 131 for the second and third
+    dev = torch.device("cuda")
+    for is_ring, base in [(True, 1e4), (False, 5e6)]:
+        capx = cap if is_ring else 6000
+        kc = torch.full((B, hkv, capx, 192), 7.0, dtype=torch.bfloat16, device=dev)
+        vc = torch.full((B, hkv, capx, 128), 7.0, dtype=torch.bfloat16, device=dev)
+        sp = torch.tensor(start, dtype=torch.int32, device=dev)
+        ha.rope_kv_append(k_new.to(dev), v_new.to(dev), sp, kc, vc, is_ring=is_ring,
+                          rope_base=base)
+        torch.cuda.synchronize()
+        ha.check_device_status()
+        kc_h, vc_h = kc.cpu(), vc.cpu()
+        written = torch.zeros((B, capx), dtype=torch.bool)
+        for b in range(B):
+            for t in range(T):
+                pos = start[b] + t
+                slot = pos % cap if is_ring else pos
+                written[b, slot] = True
+                for h in range(hkv):
+                    ref = oracle.rope(k_new[b, t, h][None], [pos], rope_base=base)[0]
+                    row = kc_h[b, h, slot]
+                    rot = row[:64].view(torch.int16).view(torch.float16).double().numpy()
+                    # fp16 keeps 11 significant bits: half-ulp rounding + fp32 work
+                    assert np.all(np.abs(rot - ref[:64]) <= np.abs(ref[:64]) * 2.0 ** -11 + 1e-6)
+                    assert torch.equal(row[64:], k_new[b, t, h, 64:])
+                    assert torch.equal(vc_h[b, h, slot], v_new[b, t, h])
+        untouched = ~written
+        assert (kc_h.permute(0, 2, 1, 3)[untouched] == 7.0).all()
+        assert (vc_h.permute(0, 2, 1, 3)[untouched] == 7.0).all()
+
+
+def _decode_compare(d, cap, is_ring, what):
+    dev = torch.device("cuda")
+    kc, vc = fill_cache(d, cap, is_ring)
+    sl = torch.tensor(d.seqlens, dtype=torch.int32, device=dev)
+    out, lse = ha.decode(d.q.to(dev), kc, vc, sl, d.sink.to(dev), max_seqlen_k=max(d.seqlens),
+                         window=d.window, is_ring=is_ring, rope_base=d.rope_base,
+                         softmax_scale=d.scale)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    o_ref, l_ref = oracle.decode(d.q, d.k_hist, d.v_hist, d.seqlens, d.sink, window=d.window,
+                                 rope_base=d.rope_base, scale=d.scale)
+    return compare(out, lse, o_ref, l_ref, what)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("G", [1, 8, 16])
+def test_decode_swa_ring(T, G):
+    lens = [T, T + 1, 100, 130, 131, 132, 500, 1000]
+    d = synth.decode_case(lens, T, G * 2, 2, window=128, rope_base=1e4, seed=700 + T + G)
+    _decode_compare(d, 128 + T - 1, True, f"swa ring T={T} G={G}")
+
+
+@pytest.mark.parametrize("T", [1, 4])
+@pytest.mark.parametrize("G", [4, 16])
+def test_decode_ga_linear_multi_chunk(T, G):
+    lens = [T, 64, 1023, 1024, 1025, 2048, 2049, 5000]  # 1 to 3 chunks of 2048
+    d = synth.decode_case(lens, T, G * 2, 2, window=0, rope_base=5e6, seed=800 + T + G)
+    _decode_compare(d, max(lens) + 3, False, f"ga T={T} G={G}")
+
+
+def test_decode_sink_stress():
+    lens = [3000, 17, 4096]
+    d = synth.decode_case(lens, 4, 64, 4, window=0, rope_base=5e6, seed=900, sink_mean=9.0,
+                          sink_std=1.5)
+    _decode_compare(d, 4100, False, "ga decode sink stress")
+    d = synth.decode_case([400, 5], 4, 64, 8, window=128, rope_base=1e4, seed=901,
+                          sink_mean=5.0, sink_std=1.0)
+    _decode_compare(d, 131, True, "swa decode sink stress")
+
+
+def test_decode_equals_prefill_last_rows():
+    """The decode path on a cache equals the prefill path's last T rows."""
+    L, T = 1500, 4
+    for window, base, hkv, cap, ring in [(128, 1e4, 8, 131, True), (0, 5e6, 4, 2000, False)]:
+        c = synth.prefill_case([L], 64, hkv, window=window, rope_base=base, seed=950)
+        out_p, lse_p = gpu_prefill(c)
+        d = synth.DecodeCase(c.q[L - T:][None], c.k[None], c.v[None], c.sink, [L], 64, hkv,
+                             window, base, c.scale)
+        dev = torch.device("cuda")
+        kc, vc = fill_cache(d, cap, ring)
+        out_d, lse_d = ha.decode(d.q.to(dev), kc, vc,
+                                 torch.tensor([L], dtype=torch.int32, device=dev),
+                                 c.sink.to(dev), max_seqlen_k=L, window=window, is_ring=ring,
+                                 rope_base=base, softmax_scale=c.scale)
+        torch.cuda.synchronize()
+        diff = (out_d[0].float() - out_p[L - T:].float()).abs().max().item()
+        assert diff <= 2e-2
+        assert (lse_d[0] - lse_p[L - T:]).abs().max().item() <= 1e-3
+
+
+def test_decode_full_size_config():
+    """batch 64, 4 query tokens per sequence: SWA over a 131-slot ring (8 KV
+    heads) and GA over lengths uniform in [8K, 64K] (4 KV heads).  The T new
+    tokens go through the append kernel first, as in the bench step."""
+    cfg = synth.CONFIGS["decode_b64_t4"]
+    B, T = cfg["B"], cfg["T"]
+    lens = synth.random_lengths(B, cfg["lens"][0], cfg["lens"][1], cfg["seed"])
+    dev = torch.device("cuda")
+    sample = sorted({int(np.argmax(lens)), int(np.argmin(lens)), 0, 17, 40})
+    for layer, cap, ring in [("swa", 131, True), ("ga", 65536, False)]:
+        p = cfg[layer]
+        d = synth.decode_case(lens, T, p["hq"], p["hkv"], window=p["window"],
+                              rope_base=p["rope_base"], seed=cfg["seed"], device=dev,
+                              lmax=cfg["lens"][1])
+        kc, vc = fill_cache(d, cap, ring, upto=[L - T for L in lens])
+        idx = torch.arange(T, device=dev)
+        k_new = torch.stack([d.k_hist[b, L - T + idx] for b, L in enumerate(lens)])
+        v_new = torch.stack([d.v_hist[b, L - T + idx] for b, L in enumerate(lens)])
+        sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+        ha.rope_kv_append(k_new, v_new, sl - T, kc, vc, is_ring=ring, rope_base=p["rope_base"])
+        out, lse = ha.decode(d.q, kc, vc, sl, d.sink, max_seqlen_k=cfg["lens"][1],
+                             window=p["window"], is_ring=ring, rope_base=p["rope_base"],
+                             softmax_scale=d.scale)
+        torch.cuda.synchronize()
+        ha.check_device_status()
+        for b in sample:
+            L = lens[b]
+            o_ref, l_ref = oracle.decode(d.q[b:b + 1].cpu(), d.k_hist[b:b + 1, :L].cpu(),
+                                         d.v_hist[b:b + 1, :L].cpu(), [L], d.sink.cpu(),
+                                         window=p["window"], rope_base=p["rope_base"],
+                                         scale=d.scale)
+            compare(out[b:b + 1], lse[b:b + 1], o_ref, l_ref, f"{layer} b={b} L={L}")
+        del d, kc, vc
+        torch.cuda.empty_cache()
+
+
+def test_hybrid_block_256k_sampled():
+    """One hybrid block at seq 262144: 5 SWA layers (64q/8kv, W=128, base 1e4)
+    and 1 GA layer (64q/4kv, base 5e6), fresh inputs per layer, sampled rows."""
+    cfg = synth.CONFIGS["hybrid_block_256k"]
+    S = cfg["seqlens"][0]
+    dev = torch.device("cuda")
+    layers = [("swa", i) for i in range(cfg["n_swa"])] + [("ga", cfg["n_swa"])]
+    for kind, li in layers:
+        p = cfg[kind]
+        c = synth.prefill_case([S], p["hq"], p["hkv"], window=p["window"],
+                               rope_base=p["rope_base"], seed=cfg["seed"] * 100 + li, device=dev)
+        out, lse = ha.prefill(c.q, c.k, c.v, c.sink, c.cu_seqlens, max_seqlen=S,
+                              window=c.window, rope_base=c.rope_base, softmax_scale=c.scale)
+        torch.cuda.synchronize()
+        ha.check_device_status()
+        if kind == "swa":
+            rows = _sample_rows(S, 64, li)
+        else:
+            rows = np.array([0, 1, 130, 4097, 131071, S - 1])
+        cpu = synth.PrefillCase(c.q.cpu(), c.k.cpu(), c.v.cpu(), c.sink.cpu(),
+                                c.cu_seqlens.cpu(), c.seqlens, c.hq, c.hkv, c.window,
+                                c.rope_base, c.scale)
+        o_ref, l_ref = oracle_prefill(cpu, rows=rows)
+        idx = torch.tensor(rows, device=dev)
+        compare(out[idx], lse[idx], o_ref, l_ref, f"hybrid layer {li} ({kind})")
+        del c, out, lse, cpu
+        torch.cuda.empty_cache()
