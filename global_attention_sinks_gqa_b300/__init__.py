@@ -46,6 +46,8 @@ SIGNATURES = {
     "hattn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "hattn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                           _F, _F, _P, _Z, _P]),
+    "hattn_decode_static_scratch": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                         _I, _I, _I, _I, _F, _F, _P]),
     "hattn_check_device_status": (_I, [_P]),
     "hattn_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
     "hattn_selftest_lost_arrival": (_I, [_P]),
@@ -139,6 +141,18 @@ def hattn_decode(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv, 
         int(B), int(T), int(hq), int(hkv), int(dqk), int(dv), int(cap), int(is_ring), int(window),
         int(max_seqlen_k), int(rope_dim), float(rope_base), float(softmax_scale), _ptr(workspace),
         int(workspace_bytes), _stream(stream))
+
+
+def hattn_decode_static_scratch(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv,
+                                dqk, dv, cap, is_ring, window, max_seqlen_k, rope_dim, rope_base,
+                                softmax_scale, stream=None) -> int:
+    """hattn_decode() without a caller workspace, for callers that cannot
+    allocate device memory: the library's fixed scratch array is used instead
+    (see include/hattn.h for its size and sharing rules)."""
+    return load_library().hattn_decode_static_scratch(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens_k), _ptr(sink), _ptr(out), _ptr(lse),
+        int(B), int(T), int(hq), int(hkv), int(dqk), int(dv), int(cap), int(is_ring), int(window),
+        int(max_seqlen_k), int(rope_dim), float(rope_base), float(softmax_scale), _stream(stream))
 
 
 def hattn_check_device_status(stream=None) -> int:

@@ -171,6 +171,46 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
                             void* stream);
 
 /*
+ * Size of the fixed device array hattn_decode_static_scratch() uses as its
+ * scratch (32 MiB): enough for B * hq * T * chunks <= 65,000 partial rows of
+ * 516 bytes, chunks = ceil(keys / 2048) -- e.g. batch 8 x 64 heads x 4 tokens
+ * over up to 32K keys (32,768 rows).  A window layer whose window fits in one
+ * chunk needs no scratch at all.
+ */
+#define HATTN_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * hattn_decode() for callers that cannot allocate device memory.  The paper
+ * has no counterpart to this entry point; it exists for callers that cannot
+ * call cudaMalloc -- code running inside a host framework that owns all
+ * device memory through its own pool and forbids side allocations, or a
+ * serving loop whose memory budget is fixed at start-up -- and so cannot
+ * provide hattn_decode()'s workspace.
+ *
+ * Same arguments and results as hattn_decode() minus the workspace; the
+ * scratch is a fixed array of HATTN_DECODE_STATIC_SCRATCH_BYTES inside the
+ * library, held on every GPU that loads the library until the process exits.
+ *   - Allocates nothing: no cudaMalloc / cudaFree, no allocating library call.
+ *   - A step whose scratch need (hattn_decode_workspace_size()) exceeds that
+ *     size returns HATTN_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.  A failed lookup returns HATTN_ERR_CUDA.
+ *   - Every call shares the one array per device and it keeps the last
+ *     call's contents.  Nothing in it needs to start at zero: every partial
+ *     result is written before it is read.  Calls that overlap on the GPU
+ *     (on different streams, or from several host threads) race on it and
+ *     must be serialised by the caller.
+ */
+hattn_status_t hattn_decode_static_scratch(const void* q, const void* k_cache,
+                                           const void* v_cache, const int* seqlens_k,
+                                           const float* sink, void* out, float* lse, int B,
+                                           int T, int hq, int hkv, int dqk, int dv, int cap,
+                                           int is_ring, int window, int max_seqlen_k,
+                                           int rope_dim, float rope_base, float softmax_scale,
+                                           void* stream);
+
+/*
  * Synchronise `stream`, then report (and clear) the device status word:
  * HATTN_OK, HATTN_ERR_TIMEOUT (a bounded wait inside a kernel ran out) or
  * HATTN_ERR_INVALID_ARG (a device-side index check skipped an access), or
