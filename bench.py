@@ -282,11 +282,13 @@ def run_cuda(args, rank, world):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
+        torch.cuda.nvtx.range_push("timed")
         start.record(stream)
         for s in range(args.steps):
             launches += step(ev[s])
         stop.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     barrier(world)
     total_ms = start.elapsed_time(stop)
     ms = max_over_ranks(total_ms, world) / args.steps
@@ -481,6 +483,57 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def run_profile_case(args):
+    """One call of one part of the step at a chosen size, for an ncu capture:
+    a warm-up call, then the profiled call inside the NVTX range "profile"."""
+    import global_attention_sinks_gqa_b300 as ha
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = args.profile_case
+    if name in ("swa_prefill", "ga_prefill"):
+        c = synth.CONFIGS[name + "_32k"]
+        S = args.seq or c["seqlens"][0]
+        pc = synth.prefill_case([S], c["hq"], c["hkv"], window=c["window"],
+                                rope_base=c["rope_base"], seed=c["seed"], device=dev)
+        ws = torch.empty(ha.hattn_prefill_workspace_size(S, pc.hkv, D_QK), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            return ha.prefill(pc.q, pc.k, pc.v, pc.sink, pc.cu_seqlens, max_seqlen=S,
+                              window=pc.window, rope_base=pc.rope_base,
+                              softmax_scale=pc.scale, workspace=ws)
+        work = f"{name} seq {S}"
+    elif name in ("decode_swa", "decode_ga"):
+        dc = synth.CONFIGS["decode_b64_t4"]
+        kind = name.split("_")[1]
+        p = dc[kind]
+        B = args.batch or dc["B"]
+        T = dc["T"]
+        lens = synth.random_lengths(B, dc["lens"][0], dc["lens"][1], dc["seed"])
+        cap = 131 if kind == "swa" else dc["lens"][1]
+        kc = torch.randn((B, p["hkv"], cap, D_QK), device=dev).to(torch.bfloat16)
+        vc = torch.randn((B, p["hkv"], cap, D_V), device=dev).to(torch.bfloat16)
+        q = torch.randn((B, T, p["hq"], D_QK), device=dev).to(torch.bfloat16)
+        sink = torch.randn(p["hq"], device=dev)
+        sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+
+        def call():
+            return ha.decode(q, kc, vc, sl, sink, max_seqlen_k=dc["lens"][1],
+                             window=p["window"], is_ring=kind == "swa",
+                             rope_base=p["rope_base"])
+        work = f"{name} batch {B} x {T}"
+    else:
+        raise SystemExit(f"unknown profile case {name}")
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("profile")
+    call()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    ha.check_device_status()
+    print(json.dumps({"profile_case": work, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,7 +542,14 @@ def main():
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--cpu-baseline", type=int, default=1)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--profile-case", default=None,
+                    help="swa_prefill | ga_prefill | decode_swa | decode_ga: one call, for ncu")
+    ap.add_argument("--seq", type=int, default=0, help="prefill length for --profile-case")
+    ap.add_argument("--batch", type=int, default=0, help="decode batch for --profile-case")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
