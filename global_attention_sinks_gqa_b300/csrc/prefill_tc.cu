@@ -11,25 +11,32 @@
 // 128 dims bf16, so QK^T runs as 4 fp16 k-steps plus 8 bf16 k-steps into one
 // fp32 accumulator.
 //
-// Work decomposition (ours): one CTA tile is 128 query rows = TQ = 128/G
-// consecutive tokens x the G query heads that share one KV head, so every
-// K/V tile fetched from memory serves all G heads (GQA reuse through the M
-// dimension of the MMA).  The keys a tile needs are walked in blocks of BN
-// rows starting at the window's first key: a sliding-window tile touches only
-// the band [t0 - W + 1, t0 + TQ - 1]; a global tile walks up to its diagonal.
+// Work decomposition (ours).  A tile is 128 query rows = TQ = 128/G
+// consecutive tokens x the G query heads that share one KV head, so every K/V
+// byte fetched serves all G heads (GQA reuse through the M dimension of the
+// MMA).  A unit is two such tiles, A and B (2*TQ consecutive tokens), that
+// walk the same key blocks of BN keys: a sliding-window unit walks only the
+// band [t0 - W + 1, t0 + 2*TQ - 1], a global unit every block up to its
+// diagonal.  The two tiles ping-pong: while the tensor core multiplies one,
+// the other's softmax runs.
 //
-// CTA roles (192 threads, persistent over tiles):
-//   warp 0      TMA producer: Q tile (3 boxes of 64 dims), K/V blocks
-//               (2-stage ring), all 128-byte swizzled.
-//   warp 1      TMEM allocator and single-thread MMA issuer:
-//               S_j = Q K_j^T  (M=128, N=BN, K=192; A, B from smem)
-//               O  += P_j V_j  (M=128, N=128, K=BN; P from TMEM, V from smem)
-//   warps 2-5   one thread per query row (TMEM lane): RoPE of the Q tile,
-//               masked online softmax in base 2 with the running max started
-//               at the sink logit, P written back to TMEM as bf16 over the
-//               consumed S columns, lazy O rescaling (only when the max grows
-//               by more than 2^8), and the epilogue O / (l + 2^(s - m)).
-// TMEM: S/P double buffer at columns 0 and 128, O at columns 256..383.
+// CTA roles (384 threads, persistent over units):
+//   warp 0      TMA producer: Q tiles (3 boxes of 64 dims each) and a ring of
+//               NSLOT slots, each one [BN keys][64 dims] box of K or V, filled
+//               in the order K_0, V_0, K_1, V_1, ... (128-byte swizzle).
+//   warp 1      TMEM allocator and single-thread MMA issuer, per key block j:
+//                 O_A += P_A,j V_j ; S_A = Q_A K_{j+1}^T ;
+//                 O_B += P_B,j V_j ; S_B = Q_B K_{j+1}^T
+//               (S: M=128, N=BN, K=192 from shared memory; PV: P from TMEM,
+//               V from shared memory).  The tensor core runs them in issue
+//               order, so S_t may be rewritten right behind the PV reading P_t.
+//   warps 2-3   idle (they complete warpgroup 0 for the register split)
+//   warps 4-7   tile A, one thread per query row (TMEM lane): RoPE of the Q
+//   warps 8-11  tile B  tile, masked online softmax in base 2 with the running
+//               max started at the sink logit, P written back to TMEM as bf16
+//               over the consumed S columns, lazy O rescaling (only when the
+//               max grows by more than 2^8), and the epilogue O / (l + 2^(s-m)).
+// TMEM: S_A 0.., S_B 128.., O_A 256..383, O_B 384..511.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -42,86 +49,201 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past 256x growth
+constexpr int kThreads = 384;
+// Register split (setmaxnreg): warpgroup 0 (producer, MMA issuer, two idle
+// warps) drops to kRegsLow, the two softmax warpgroups rise to kRegsHigh.  The
+// sum must not exceed what the launch allocated (kThreads x kRegsLaunch), or
+// the increase would wait forever; the host checks the kernel's register
+// count against kRegsLaunch before every launch.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsLow = 104;
+constexpr int kRegsHigh = 200;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split");
 
-template <int G, int BN, int QS>
+template <int G, int BN>
 struct Cfg {
-  static constexpr int TQ = 128 / G;                 // tokens per tile
-  static constexpr int kQBytes = 128 * 384;           // 3 boxes [128 rows][64 dims]
-  static constexpr int kKBox = BN * 128;              // one 64-dim box of a K/V block
-  static constexpr int kKBytes = 3 * kKBox;
-  static constexpr int kVBytes = 2 * kKBox;
+  static constexpr int TQ = 128 / G;                // tokens per tile
+  static constexpr int UT = 2 * TQ;                 // tokens per unit (tiles A and B)
+  static constexpr int kQBox = 128 * 128;           // [128 rows][64 dims] bf16
+  static constexpr int kQBytes = 3 * kQBox;
+  static constexpr int kSlot = BN * 128;            // [BN keys][64 dims] bf16
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + QS * kQBytes;
-  static constexpr int kOffV = kOffK + 2 * kKBytes;
-  static constexpr int kOffBar = kOffV + 2 * kVBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
-  static constexpr uint32_t kSCol0 = 0, kSCol1 = 128, kOCol = 256, kTmemCols = 512;
+  static constexpr int kOffRing = 2 * kQBytes;
+  static constexpr int kBarBytes = 1024;
+  static constexpr int kMaxSmem = 232448;
+  static constexpr int NSLOT = (kMaxSmem - 1024 - kBarBytes - kOffRing) / kSlot;
+  static constexpr int kOffBar = kOffRing + NSLOT * kSlot;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "BN");
-  static_assert(kKBox % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kSlot % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+  static_assert(NSLOT >= 8, "ring must hold a K and a V block with room to prefetch");
+  static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
 
+__host__ __device__ constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t o_col(int t) { return t ? 384u : 256u; }
+
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int NSLOT>
 struct Bars {
   uint64_t q_full[2], q_ready[2], q_empty[2];
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done, o_free, drain;
+  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
+  uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-struct TileInfo {
-  int b, g, t0, L, kstart, nblk, tok0;
+struct UnitInfo {
+  int b, g, t0, L, tok0, kstart, nblk;
 };
 
-template <int G, int BN, bool GLOBAL>
-__device__ __forceinline__ bool tile_info(int t_lin, const PrefillArgs& a, int nqt, TileInfo& ti) {
-  constexpr int TQ = 128 / G;
-  const int per_qt = a.batch * a.hkv;
-  const int q_ord = t_lin / per_qt;
-  const int rem = t_lin - q_ord * per_qt;
-  // global tiles: longest (latest) first for balance; window tiles: in order
-  const int qt = GLOBAL ? (nqt - 1 - q_ord) : q_ord;
-  ti.b = rem / a.hkv;
-  ti.g = rem - ti.b * a.hkv;
-  ti.tok0 = __ldg(a.cu_seqlens + ti.b);
-  ti.L = __ldg(a.cu_seqlens + ti.b + 1) - ti.tok0;
-  ti.t0 = qt * TQ;
-  if (ti.t0 >= ti.L) return false;
-  const int qlast = min(ti.t0 + TQ, ti.L) - 1;
-  ti.kstart = GLOBAL ? 0 : max(0, ti.t0 - a.window + 1);
-  ti.nblk = (qlast + 1 - ti.kstart + BN - 1) / BN;
+// Unit u of the persistent loop.  Global units run latest (longest) first so
+// the tail of the schedule is short; window units run in order.
+template <int G, int BN, bool WIN>
+__device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, int nut, UnitInfo& ui) {
+  constexpr int UT = 256 / G;
+  const int per = a.batch * a.hkv;
+  const int q_ord = u / per;
+  const int rem = u - q_ord * per;
+  const int qt = WIN ? q_ord : (nut - 1 - q_ord);
+  ui.b = rem / a.hkv;
+  ui.g = rem - ui.b * a.hkv;
+  ui.tok0 = __ldg(a.cu_seqlens + ui.b);
+  ui.L = __ldg(a.cu_seqlens + ui.b + 1) - ui.tok0;
+  ui.t0 = qt * UT;
+  if (ui.t0 >= ui.L) return false;
+  const int qend = min(ui.t0 + UT, ui.L);  // one past the last valid query
+  ui.kstart = WIN ? max(0, ui.t0 - a.window + 1) : 0;
+  ui.nblk = (qend - ui.kstart + BN - 1) / BN;
   return true;
 }
 
-template <int G, int BN, int QS, bool GLOBAL>
-__global__ void __launch_bounds__(192, 1)
+// One block of the online softmax for one query row.  s holds the row's BN raw
+// logits; masked columns become -inf.  Writes P (bf16) into the S columns and
+// updates the running max m, the exact sum l (for lse) and the sum lr of the
+// bf16-rounded weights PV uses (for out; equal to l on unmasked blocks).
+template <int BN, bool MASKED>
+__device__ __forceinline__ void softmax_block(uint32_t (&s)[BN], int c_lo, int c_hi,
+                                              float scale_log2, uint32_t t_s, uint32_t t_o,
+                                              bool may_rescale, float& m, float& l, float& lr) {
+  if (MASKED) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c)
+      if (c > c_hi || c < c_lo) s[c] = __float_as_uint(-INFINITY);
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c + 1 < BN; c += 2)
+    mx = fmax3f(mx, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+  const float m_new = fmaxf(m, mx * scale_log2);
+  const bool resc = m_new > m + kRescaleThreshold;
+  float alpha = 1.f;
+  if (resc) {
+    alpha = fast_exp2(m - m_new);  // 0 when m was -inf
+    m = m_new;
+    l *= alpha;
+    lr *= alpha;
+  }
+  const float msub = (m == -INFINITY) ? 0.f : m;
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+  const uint64_t nm2 = f2_pack(-msub, -msub);
+  uint64_t acc = f2_pack(0.f, 0.f), acc_r = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < BN; c += 16) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const float2 x = f2_unpack(
+          f2_fma(f2_pack(__uint_as_float(s[c + e]), __uint_as_float(s[c + e + 1])), sc2, nm2));
+      const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+      const uint32_t u = pack_bf16x2(p0, p1);
+      pk[e >> 1] = u;
+      acc = f2_add(acc, f2_pack(p0, p1));
+      if (MASKED)
+        acc_r = f2_add(acc_r, f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)));
+    }
+    tmem_st8(t_s + (c >> 1), pk);  // P (bf16 pairs) over consumed S columns
+  }
+  const float2 sum = f2_unpack(acc);
+  l += sum.x + sum.y;
+  if (MASKED) {
+    const float2 sr = f2_unpack(acc_r);
+    lr += sr.x + sr.y;
+  } else {
+    lr += sum.x + sum.y;
+  }
+  if (may_rescale && __any_sync(0xffffffffu, resc)) {
+    // O holds the earlier blocks scaled by 2^-m_old; the PV that wrote them is
+    // complete (the S block just waited for was committed after it), and the
+    // PV of this block waits for p_full, which follows this rescale.
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t v[32];
+      tmem_ld32_nowait(t_o + c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        tmem_reg_fence(v[e]);
+        v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+      }
+      tmem_st32(t_o + c, v);
+    }
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void load_s_row(uint32_t t_s, uint32_t (&s)[BN]) {
+  int c = 0;
+#pragma unroll
+  for (; c + 32 <= BN; c += 32) tmem_ld32_nowait(t_s + c, s + c);
+#pragma unroll
+  for (; c < BN; c += 16) tmem_ld16_nowait(t_s + c, s + c);
+  tmem_ld_wait();
+#pragma unroll
+  for (int e = 0; e < BN; ++e) tmem_reg_fence(s[e]);
+}
+
+template <int G, int BN, bool WIN>
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapV, const PrefillArgs a) {
-  using C = Cfg<G, BN, QS>;
+  using C = Cfg<G, BN>;
   constexpr int TQ = C::TQ;
+  constexpr int NSLOT = C::NSLOT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
+  Bars<NSLOT>* bars = reinterpret_cast<Bars<NSLOT>*>(smem + C::kOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nqt = (a.max_seqlen + TQ - 1) / TQ;
-  const int ntiles = nqt * a.batch * a.hkv;
+  const int nut = (a.max_seqlen + C::UT - 1) / C::UT;
+  const int nunits = nut * a.batch * a.hkv;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->q_full[i], 1);
-      mbar_init(&bars->q_ready[i], 128);
-      mbar_init(&bars->q_empty[i], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->q_ready[t], 128);
+      mbar_init(&bars->q_empty[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->pv_done[t], 1);
+      mbar_init(&bars->o_free[t], 128);
+    }
+    for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
     }
-    mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -139,141 +261,222 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  uint8_t* ring = smem + C::kOffRing;
 
-  if (warp == 0) {
+  if (warp < 4) {
+    reg_dealloc<kRegsLow>();  // one instruction for all of warpgroup 0
+    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t q_fills[2] = {0, 0}, kv_fills[2] = {0, 0};
-      int tc = 0, it = 0;
+      uint32_t pos = 0;            // ring positions filled so far
+      uint32_t qfills[2] = {0, 0};
       bool ok = true;
-      for (int t_lin = blockIdx.x; t_lin < ntiles && ok; t_lin += gridDim.x) {
-        TileInfo ti;
-        if (!tile_info<G, BN, GLOBAL>(t_lin, a, nqt, ti)) continue;
-        const int qs = tc % QS;
-        const uint32_t qph = uint32_t(tc / QS) & 1u;
-        if (!mbar_wait(&bars->q_empty[qs], qph ^ 1u, a.ctl, abort)) break;
-        mbar_arrive_expect_tx(&bars->q_full[qs], C::kQBytes);
-        uint8_t* qdst = smem + C::kOffQ + qs * C::kQBytes;
-        for (int i = 0; i < 3; ++i)
-          tma_load_3d(qdst + i * 16384, &mapQ, &bars->q_full[qs], 64 * i, ti.g * G,
-                      ti.tok0 + ti.t0);
-        ++q_fills[qs];
-        for (int j = 0; j < ti.nblk; ++j, ++it) {
-          const int s = it & 1;
-          const uint32_t ph = uint32_t(it >> 1) & 1u;
-          if (!mbar_wait(&bars->kv_empty[s], ph ^ 1u, a.ctl, abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->kv_full[s], C::kKBytes + C::kVBytes);
-          const int krow = ti.tok0 + ti.kstart + j * BN;
-          uint8_t* kdst = smem + C::kOffK + s * C::kKBytes;
-          uint8_t* vdst = smem + C::kOffV + s * C::kVBytes;
+      auto load_box = [&](const CUtensorMap* map, int dim0, int g, int row) -> bool {
+        const uint32_t slot = pos % NSLOT;
+        const uint32_t ph = (pos / NSLOT) & 1u;
+        if (!mbar_wait(&bars->kv_empty[slot], ph ^ 1u, a.ctl, abort)) return false;
+        mbar_arrive_expect_tx(&bars->kv_full[slot], C::kSlot);
+        tma_load_3d(ring + slot * C::kSlot, map, &bars->kv_full[slot], dim0, g, row);
+        ++pos;
+        return true;
+      };
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        UnitInfo ui;
+        if (!unit_info<G, BN, WIN>(u, a, nut, ui)) continue;
+        const int row0 = ui.tok0 + ui.kstart;
+        // K_0 first (its slots free up while the previous unit finishes), then
+        // the two Q tiles, then V_0, K_1, V_1, ...
+        for (int i = 0; i < 3 && ok; ++i) ok = load_box(&mapK, 64 * i, ui.g, row0);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!mbar_wait(&bars->q_empty[t], (qfills[t] & 1u) ^ 1u, a.ctl, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->q_full[t], C::kQBytes);
+          uint8_t* qdst = smem + C::kOffQ + t * C::kQBytes;
           for (int i = 0; i < 3; ++i)
-            tma_load_3d(kdst + i * C::kKBox, &mapK, &bars->kv_full[s], 64 * i, ti.g, krow);
-          for (int i = 0; i < 2; ++i)
-            tma_load_3d(vdst + i * C::kKBox, &mapV, &bars->kv_full[s], 64 * i, ti.g, krow);
-          ++kv_fills[s];
+            tma_load_3d(qdst + i * C::kQBox, &mapQ, &bars->q_full[t], 64 * i, ui.g * G,
+                        ui.tok0 + ui.t0 + t * TQ);
+          ++qfills[t];
         }
-        ++tc;
+        for (int j = 0; j < ui.nblk && ok; ++j) {
+          for (int i = 0; i < 2 && ok; ++i) ok = load_box(&mapV, 64 * i, ui.g, row0 + j * BN);
+          if (j + 1 < ui.nblk)
+            for (int i = 0; i < 3 && ok; ++i)
+              ok = load_box(&mapK, 64 * i, ui.g, row0 + (j + 1) * BN);
+        }
       }
       // never leave with copies in flight into this CTA's shared memory
-      for (int i = 0; i < 2; ++i) {
-        if (q_fills[i]) mbar_wait_drain(&bars->q_full[i], (q_fills[i] - 1) & 1u, a.ctl);
-        if (kv_fills[i]) mbar_wait_drain(&bars->kv_full[i], (kv_fills[i] - 1) & 1u, a.ctl);
+      for (int t = 0; t < 2; ++t)
+        if (qfills[t]) mbar_wait_drain(&bars->q_full[t], (qfills[t] - 1) & 1u, a.ctl);
+      for (uint32_t sl = 0; sl < uint32_t(NSLOT); ++sl) {
+        const uint32_t fills = pos > sl ? (pos - sl + NSLOT - 1) / NSLOT : 0;
+        if (fills) mbar_wait_drain(&bars->kv_full[sl], (fills - 1) & 1u, a.ctl);
       }
     }
-  } else if (warp == 1) {
+    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_rot = make_idesc_f16(128, BN, 0, 0);   // dims 0..63
       constexpr uint32_t idesc_s = make_idesc_bf16(128, BN, 0, 0);    // dims 64..191
       constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, 0, 1);
-      const uint32_t sbase = smem_u32(smem);
-      int tc = 0, it = 0;
-      long pv_issued = 0;  // PVs issued so far; PV k completes o_done phase k
+      constexpr uint32_t idesc_o64 = make_idesc_bf16(128, 64, 0, 1);
+      const uint32_t qbase = smem_u32(smem + C::kOffQ);
+      const uint32_t rbase = smem_u32(ring);
+      uint32_t pos = 0;   // ring positions consumed (same sequence as the producer)
+      uint32_t blk = 0;   // key blocks completed by both tiles so far
+      uint32_t uc = 0;    // units started
       bool ok = true;
-      auto issue_pv = [&](int itj, bool first_of_tile) -> bool {
-        const int s = itj & 1;
-        const uint32_t ph = uint32_t(itj >> 1) & 1u;
-        if (!mbar_wait(&bars->p_full[s], ph, a.ctl, abort)) return false;
-        if (first_of_tile && tc > 0) {
-          if (!mbar_wait(&bars->o_free, uint32_t(tc - 1) & 1u, a.ctl, abort)) return false;
+      auto wait_slots = [&](uint32_t p0, int n) -> bool {
+        for (int i = 0; i < n; ++i) {
+          const uint32_t p = p0 + i;
+          if (!mbar_wait(&bars->kv_full[p % NSLOT], (p / NSLOT) & 1u, a.ctl, abort)) return false;
         }
-        tc_fence_after();
-        const uint32_t p_tmem = tmem + (s ? C::kSCol1 : C::kSCol0);
-        const uint32_t v_base = sbase + C::kOffV + s * C::kVBytes;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bdesc = make_sdesc_sw128(v_base + kk * 2048, C::kKBox, 1024);
-          umma_ts(tmem + C::kOCol, p_tmem + kk * 8, bdesc, idesc_o,
-                  (first_of_tile && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(&bars->o_done);
-        umma_commit(&bars->kv_empty[s]);
-        ++pv_issued;
         return true;
       };
-      for (int t_lin = blockIdx.x; t_lin < ntiles && ok; t_lin += gridDim.x) {
-        TileInfo ti;
-        if (!tile_info<G, BN, GLOBAL>(t_lin, a, nqt, ti)) continue;
-        const int qs = tc % QS;
-        const uint32_t qph = uint32_t(tc / QS) & 1u;
-        if (!mbar_wait(&bars->q_ready[qs], qph, a.ctl, abort)) break;
-        const uint32_t q_base = sbase + C::kOffQ + qs * C::kQBytes;
-        for (int j = 0; j < ti.nblk && ok; ++j) {
-          const int itj = it + j;
-          const int s = itj & 1;
-          const uint32_t ph = uint32_t(itj >> 1) & 1u;
-          if (!mbar_wait(&bars->kv_full[s], ph, a.ctl, abort)) { ok = false; break; }
-          // S buffer s last held P_{itj-2}; make sure the PV reading it is done
-          // (waiting on the latest PV issued, never on an older phase).
-          if (pv_issued > 0 && pv_issued - 1 >= itj - 2) {
-            if (!mbar_wait(&bars->o_done, uint32_t(pv_issued - 1) & 1u, a.ctl, abort)) {
+      auto release_slots = [&](uint32_t p0, int n) {
+        for (int i = 0; i < n; ++i) umma_commit(&bars->kv_empty[(p0 + i) % NSLOT]);
+      };
+      auto issue_qk = [&](int t, uint32_t kpos) {
+        const uint32_t qb = qbase + t * C::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk) {
+          const uint32_t kslot = (kpos + (kk >> 2)) % NSLOT;
+          const uint64_t adesc = make_sdesc_sw128(qb + (kk >> 2) * C::kQBox + (kk & 3) * 32, 16, 1024);
+          const uint64_t bdesc = make_sdesc_sw128(rbase + kslot * C::kSlot + (kk & 3) * 32, 16, 1024);
+          umma_ss(tmem + s_col(t), adesc, bdesc, kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vpos, bool acc) {
+        const uint32_t s0 = vpos % NSLOT, s1 = (vpos + 1) % NSLOT;
+        const uint32_t v0 = rbase + s0 * C::kSlot, v1 = rbase + s1 * C::kSlot;
+        const uint32_t p_tmem = tmem + s_col(t);
+        if (s1 == s0 + 1) {  // the two 64-dim halves of V are adjacent: one N=128 MMA per k-step
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_ts(tmem + o_col(t), p_tmem + kk * 8, make_sdesc_sw128(v0 + kk * 2048, C::kSlot, 1024),
+                    idesc_o, (acc || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            umma_ts(tmem + o_col(t), p_tmem + kk * 8, make_sdesc_sw128(v0 + kk * 2048, C::kSlot, 1024),
+                    idesc_o64, (acc || kk > 0) ? 1u : 0u);
+            umma_ts(tmem + o_col(t) + 64, p_tmem + kk * 8,
+                    make_sdesc_sw128(v1 + kk * 2048, C::kSlot, 1024), idesc_o64,
+                    (acc || kk > 0) ? 1u : 0u);
+          }
+        }
+      };
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        UnitInfo ui;
+        if (!unit_info<G, BN, WIN>(u, a, nut, ui)) continue;
+        const uint32_t k0 = pos;
+        pos += 3;
+        if (!wait_slots(k0, 3)) break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!mbar_wait(&bars->q_ready[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk(t, k0);
+          umma_commit(&bars->s_full[t]);
+          if (ui.nblk == 1) umma_commit(&bars->q_empty[t]);
+        }
+        if (!ok) break;
+        release_slots(k0, 3);
+        for (int j = 0; j < ui.nblk && ok; ++j, ++blk) {
+          const uint32_t vp = pos;
+          pos += 2;
+          const bool more = j + 1 < ui.nblk;
+          const uint32_t kn = pos;
+          if (more) pos += 3;
+          if (!wait_slots(vp, 2)) { ok = false; break; }
+          for (int t = 0; t < 2; ++t) {
+            if (!mbar_wait(&bars->p_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
+            if (j == 0 && uc > 0 &&
+                !mbar_wait(&bars->o_free[t], (uc - 1) & 1u, a.ctl, abort)) {
               ok = false;
               break;
             }
+            tc_fence_after();
+            issue_pv(t, vp, j > 0);
+            umma_commit(&bars->pv_done[t]);
+            if (t == 1) release_slots(vp, 2);
+            if (more) {
+              if (t == 0 && !wait_slots(kn, 3)) { ok = false; break; }
+              issue_qk(t, kn);
+              umma_commit(&bars->s_full[t]);
+              if (j + 2 == ui.nblk) umma_commit(&bars->q_empty[t]);
+              if (t == 1) release_slots(kn, 3);
+            }
           }
-          tc_fence_after();
-          const uint32_t k_base = sbase + C::kOffK + s * C::kKBytes;
-          const uint32_t d_tmem = tmem + (s ? C::kSCol1 : C::kSCol0);
-#pragma unroll
-          for (int kk = 0; kk < 12; ++kk) {
-            const uint64_t adesc =
-                make_sdesc_sw128(q_base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            const uint64_t bdesc =
-                make_sdesc_sw128(k_base + (kk >> 2) * C::kKBox + (kk & 3) * 32, 16, 1024);
-            umma_ss(d_tmem, adesc, bdesc, kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&bars->s_full[s]);
-          if (j == ti.nblk - 1) umma_commit(&bars->q_empty[qs]);
-          if (j >= 1 && !issue_pv(itj - 1, j == 1)) { ok = false; break; }
         }
-        if (!ok) break;
-        if (!issue_pv(it + ti.nblk - 1, ti.nblk == 1)) break;
-        it += ti.nblk;
-        ++tc;
+        ++uc;
       }
       // every MMA issued must be complete before TMEM is released
       umma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, a.ctl);
     }
+    }  // warps 2 and 3: idle
   } else {
     // ------------------------------------------------------------ softmax rows
+    reg_alloc<kRegsHigh>();
+    const int t = (warp - 4) >> 2;             // tile: warps 4-7 -> A, 8-11 -> B
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;            // query row of the tile
     const int hl = r % G;
     const int tl = r / G;
     const uint32_t lane_addr = uint32_t(quad * 32) << 16;
-    int tc = 0, it = 0;
-    for (int t_lin = blockIdx.x; t_lin < ntiles; t_lin += gridDim.x) {
-      TileInfo ti;
-      if (!tile_info<G, BN, GLOBAL>(t_lin, a, nqt, ti)) continue;
-      const int qs = tc % QS;
-      const uint32_t qph = uint32_t(tc / QS) & 1u;
-      if (!warp_wait(&bars->q_full[qs], qph, a.ctl, abort)) break;
-      const int qpos = ti.t0 + tl;
+    const uint32_t t_s = tmem + lane_addr + s_col(t);
+    const uint32_t t_o = tmem + lane_addr + o_col(t);
+    uint32_t blk = 0, uc = 0;
+    // the previous unit's row, finished after the next unit's Q is rotated
+    bool have_prev = false;
+    float pm = 0.f, pl = 0.f, plr = 0.f, psink = 0.f;
+    bool pvalid = false;
+    long porow = 0;
+    uint32_t pblk = 0;
+
+    auto epilogue = [&]() -> bool {
+      if (!warp_wait(&bars->pv_done[t], (pblk - 1) & 1u, a.ctl, abort)) return false;
+      tc_fence_after();
+      const float msub = (pm == -INFINITY) ? 0.f : pm;
+      const float sink_w = exp2f(psink - msub);
+      const float l_tot = pl + sink_w;
+      const float inv = 1.f / (plr + sink_w);
+      uint4* optr = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + porow * 256);
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t v[32];
+        tmem_ld32_nowait(t_o + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) tmem_reg_fence(v[e]);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+        if (pvalid) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            optr[(c >> 3) + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      if (pvalid && a.lse != nullptr) a.lse[porow] = (msub + log2f(l_tot)) * kLn2;
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[t]);
+      return true;
+    };
+
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      UnitInfo ui;
+      if (!unit_info<G, BN, WIN>(u, a, nut, ui)) continue;
+      if (!warp_wait(&bars->q_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
+      const int qmin = ui.t0 + t * TQ;           // first token of this tile
+      const int qpos = qmin + tl;
       // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
       // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
       {
-        uint8_t* qrow = smem + C::kOffQ + qs * C::kQBytes + r * 128;
+        uint8_t* qrow = smem + C::kOffQ + t * C::kQBytes + r * 128;
         uint4 ch[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) ch[c] = *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
@@ -299,125 +502,52 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
         fence_proxy_async_smem();
-        mbar_arrive(&bars->q_ready[qs]);
+        mbar_arrive(&bars->q_ready[t]);
       }
-      const int h = ti.g * G + hl;
+      if (have_prev && !epilogue()) { ok = false; break; }
+      const int h = ui.g * G + hl;
       const float sink_l2 = __ldg(a.sink + h) * kLog2e;
       float m = sink_l2;  // running max (log2 units), started at the sink logit
-      float l = 0.f;      // running sum of exp2(x - m) over visible keys (for lse)
-      float lr = 0.f;     // the same sum of the bf16-rounded weights PV uses (for out)
-      bool ok = true;
-      for (int j = 0; j < ti.nblk; ++j) {
-        const int itj = it + j;
-        const int s = itj & 1;
-        const uint32_t ph = uint32_t(itj >> 1) & 1u;
-        if (!warp_wait(&bars->s_full[s], ph, a.ctl, abort)) { ok = false; break; }
+      float l = 0.f, lr = 0.f;
+      const int qmax = qmin + TQ - 1;
+      for (int j = 0; j < ui.nblk; ++j, ++blk) {
+        if (!warp_wait(&bars->s_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t t_s = tmem + lane_addr + (s ? C::kSCol1 : C::kSCol0);
-        const int kb = ti.kstart + j * BN;  // position of column 0
-        // visible columns: kpos <= qpos and (global or qpos - kpos < W)
-        const int c_hi = qpos - kb;                                     // inclusive
-        const int c_lo = GLOBAL ? 0 : (qpos - a.window + 1 - kb);       // inclusive
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BN; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(t_s + c, v);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = c + e;
-            if (col <= c_hi && col >= c_lo) mx = fmaxf(mx, __uint_as_float(v[e]));
-          }
-        }
-        const float m_blk = mx * a.scale_log2;
-        const float m_new = fmaxf(m, m_blk);
-        const bool resc = (m == -INFINITY) ? (m_new != -INFINITY)
-                                           : (m_new > m + kRescaleThreshold);
-        const float m_use = resc ? m_new : m;
-        const float alpha = resc ? exp2f(m - m_new) : 1.f;
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O holds sum over earlier blocks scaled by 2^-m: rescale it once the
-          // previous PV has landed.
-          if (!warp_wait(&bars->o_done, uint32_t(itj - 1) & 1u, a.ctl, abort)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t t_o = tmem + lane_addr + C::kOCol;
-#pragma unroll
-          for (int c = 0; c < 128; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(t_o + c, v);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st16(t_o + c, v);
-          }
-          tmem_st_wait();
-        }
-        l *= alpha;
-        lr *= alpha;
-        m = m_use;
-        const float msub = (m == -INFINITY) ? 0.f : m;
-#pragma unroll
-        for (int c = 0; c < BN; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(t_s + c, v);
-          uint32_t pk[8];
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const int col = c + e;
-            float p0 = 0.f, p1 = 0.f;
-            if (col <= c_hi && col >= c_lo)
-              p0 = fast_exp2(fmaf(__uint_as_float(v[e]), a.scale_log2, -msub));
-            if (col + 1 <= c_hi && col + 1 >= c_lo)
-              p1 = fast_exp2(fmaf(__uint_as_float(v[e + 1]), a.scale_log2, -msub));
-            // out is normalised by the sum of the same bf16-rounded weights the
-            // PV product uses; lse uses the exact sum
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-            const float2 pr = unpack_bf16x2(pk[e >> 1]);
-            l += p0 + p1;
-            lr += pr.x + pr.y;
-          }
-          tmem_st8(t_s + (c >> 1), pk);  // P (bf16 pairs) over consumed S columns
+        const int kb = ui.kstart + j * BN;  // position of column 0
+        uint32_t s[BN];
+        load_s_row<BN>(t_s, s);
+        // the block needs a mask if any row of the tile loses a column to the
+        // causal edge or (sliding window) to the window's far edge
+        const bool masked = (kb + BN - 1 > qmin) || (WIN && kb < qmax - a.window + 1);
+        if (masked) {
+          const int c_hi = qpos - kb;
+          const int c_lo = WIN ? qpos - a.window + 1 - kb : -1;
+          softmax_block<BN, true>(s, c_lo, c_hi, a.scale_log2, t_s, t_o, j > 0, m, l, lr);
+        } else {
+          softmax_block<BN, false>(s, 0, BN, a.scale_log2, t_s, t_o, j > 0, m, l, lr);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[s]);
+        mbar_arrive(&bars->p_full[t]);
       }
       if (!ok) break;
-      // --------------------------------------------------------- epilogue
-      if (!warp_wait(&bars->o_done, uint32_t(it + ti.nblk - 1) & 1u, a.ctl, abort)) break;
-      tc_fence_after();
-      const float msub = (m == -INFINITY) ? 0.f : m;
-      const float sink_w = exp2f(sink_l2 - msub);
-      const float l_tot = l + sink_w;
-      const float inv = 1.f / (lr + sink_w);
-      const bool valid = qpos < ti.L;
-      const long orow = long(ti.tok0 + qpos) * a.hq + h;
-      uint4* optr = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + orow * 256);
-      const uint32_t t_o = tmem + lane_addr + C::kOCol;
-#pragma unroll
-      for (int c = 0; c < 128; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(t_o + c, v);
-        uint32_t pk[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
-        if (valid) {
-          optr[(c >> 3) + 0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          optr[(c >> 3) + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
-      }
-      if (valid && a.lse != nullptr) a.lse[orow] = (msub + log2f(l_tot)) * kLn2;
-      tc_fence_before();
-      mbar_arrive(&bars->o_free);
-      it += ti.nblk;
-      ++tc;
+      have_prev = true;
+      pm = m;
+      pl = l;
+      plr = lr;
+      psink = sink_l2;
+      pvalid = qpos < ui.L;
+      porow = long(ui.tok0 + qpos) * a.hq + h;
+      pblk = blk;
+      ++uc;
     }
+    if (ok && have_prev) epilogue();
   }
 
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem, Cfg<G, BN>::kTmemCols);
   }
 }
 
@@ -460,35 +590,42 @@ int num_sms() {
   return n;
 }
 
-template <int G, int BN, int QS, bool GLOBAL>
+template <int G, int BN, bool WIN>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
-  using C = Cfg<G, BN, QS>;
+  using C = Cfg<G, BN>;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, a.q, a.total, a.hq, kDqk, G, C::TQ) ||
       !make_map(&mk, a.k_rot, a.total, a.hkv, kDqk, 1, BN) ||
       !make_map(&mv, a.v, a.total, a.hkv, kDv, 1, BN))
     return cudaErrorInvalidValue;
-  auto kern = prefill_kernel<G, BN, QS, GLOBAL>;
+  auto kern = prefill_kernel<G, BN, WIN>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    // The register split inside the kernel needs the launch to allocate
+    // kRegsLaunch registers per thread; anything less would stall it.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long nqt = (a.max_seqlen + C::TQ - 1) / C::TQ;
-  const long ntiles = nqt * a.batch * a.hkv;
-  if (ntiles == 0) return cudaSuccess;
-  const int grid = int(ntiles < num_sms() ? ntiles : num_sms());
-  kern<<<grid, 192, C::kSmemBytes, s>>>(mq, mk, mv, a);
+  const long nut = (a.max_seqlen + C::UT - 1) / C::UT;
+  const long nunits = nut * a.batch * a.hkv;
+  if (nunits == 0) return cudaSuccess;
+  const int grid = int(nunits < num_sms() ? nunits : num_sms());
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
+// Key block: 80 when a window unit's band (W - 1 + 2*TQ keys) fits two
+// blocks of 80, else 128.
 template <int G>
 cudaError_t launch_g(const PrefillArgs& a, cudaStream_t s) {
-  if (a.window == 0) return launch_t<G, 128, 1, true>(a, s);
-  if (a.window <= 256) return launch_t<G, 80, 2, false>(a, s);
-  return launch_t<G, 128, 1, false>(a, s);
+  if (a.window == 0) return launch_t<G, 128, false>(a, s);
+  if (a.window - 1 + 256 / G <= 160) return launch_t<G, 80, true>(a, s);
+  return launch_t<G, 128, true>(a, s);
 }
 
 }  // namespace
