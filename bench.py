@@ -206,7 +206,8 @@ class Workload:
         v_new = synth.randn_bf16((B, T, hkv, D_V), g, dev)
         sink = synth.randn_f32((hq,), g, dev)
         sl = torch.tensor(self.lens, dtype=torch.int32, device=dev)
-        ws_n = ha.hattn_decode_workspace_size(B, T, hq, hkv, D_V, self.lmax, p["window"])
+        ws_n = ha.hattn_decode_workspace_size(B, T, hq, hkv, D_V, self.lmax, p["window"], cap,
+                                              1 if ring else 0)
         ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
         return dict(q=q, k_new=k_new, v_new=v_new, sink=sink, kc=kc, vc=vc, seqlens=sl,
                     start=sl - T, ws=ws, ws_n=ws_n,

@@ -43,7 +43,7 @@ SIGNATURES = {
     "hattn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _L, _I, _I, _I, _I, _I, _I, _F, _I, _F,
                            _P, _Z, _P]),
     "hattn_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
-    "hattn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "hattn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "hattn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                           _F, _F, _P, _Z, _P]),
     "hattn_decode_static_scratch": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -128,9 +128,10 @@ def hattn_rope_kv_append(k_new, v_new, start_pos, k_cache, v_cache, B, T, hkv, d
         _stream(stream))
 
 
-def hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window) -> int:
+def hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window, cap, is_ring) -> int:
     return load_library().hattn_decode_workspace_size(int(B), int(T), int(hq), int(hkv), int(dv),
-                                                      int(max_seqlen_k), int(window))
+                                                      int(max_seqlen_k), int(window), int(cap),
+                                                      int(is_ring))
 
 
 def hattn_decode(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv, dqk, dv, cap,
@@ -215,7 +216,8 @@ def decode(q, k_cache, v_cache, seqlens_k, sink, *, max_seqlen_k: int, window: i
         out = torch.empty((B, T, hq, dv), dtype=torch.bfloat16, device=q.device)
     if lse is None and with_lse:
         lse = torch.empty((B, T, hq), dtype=torch.float32, device=q.device)
-    need = hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window)
+    need = hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window, cap,
+                                       1 if is_ring else 0)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(hattn_decode(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv, dqk, dv,

@@ -1,23 +1,43 @@
-// decode.cu -- decode / MTP-verify attention over a KV cache, split over keys.
+// decode.cu -- decode / MTP-verify attention over a KV cache, split over keys,
+// on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // Method: plmsmile notes on the MiMo series, MiMo-V2-Flash MTP: drafted
 // tokens are verified by one parallel pass of the main model, so each
 // sequence brings T = 1..4 query tokens (positions L-T .. L-1) that attend
 // causally over the cache; "local window": an SWA layer's cache is a fixed
 // ring (slot = pos % cap), a GA layer's cache grows (slot = pos).  The sink
-// (paper review, section 3.2) joins the denominator once, in the merge.
+// (paper review, section 3.2) joins the denominator once, when a row is
+// finished.
 //
-// Decomposition (ours): one CTA per (sequence, KV head, key chunk).  Its
-// G*T query rows (all query heads of the KV head, all T tokens) share every
-// K/V byte it loads.  Keys stream through shared memory in blocks of 64 with
-// 16-byte cp.async copies (double buffered, XOR-swizzled 16-byte chunks so
-// ldmatrix reads are conflict free); QK^T and PV run on mma.sync m16n8k16
-// (fp32 accumulate; the 64 rotated dims as fp16, the rest as bf16, matching
-// the cache written by the append) with an online softmax in base 2.  Each of the
-// four warps owns 16 rows and a slice of every key block; warps sharing rows
-// merge by log-sum-exp at the end.  With one chunk the CTA finishes the rows
-// itself (sink included); otherwise it writes (O / l, m + log2 l) and a merge
-// kernel combines the chunks and the sink with one warp per output row.
+// Decomposition (ours).  A work item is (sequence, KV head, chunk of cache
+// slots); its G*T query rows (all query heads of the KV head, all T tokens)
+// share every K/V byte it loads.  A linear cache splits the visible positions
+// into chunks of `chunk` keys; a ring's slots are split the same way (the key
+// position of slot s is the one position of the last `cap` that is congruent
+// to s).  The kernel is persistent: one CTA per SM walks the items
+// round-robin.  The G*T <= 64 rows sit in a 128-row tile whose other rows are
+// zero, so QK^T and PV are plain M=128 tensor-core products; the step is
+// bound by streaming the cache, not by the multiply.
+//
+// CTA roles (192 threads):
+//   warp 0      TMA producer: per item the Q tile (3 boxes [G*T rows][64 dims])
+//               into one of two buffers, and blocks of 64 cache slots (K: 3
+//               boxes, V: 2 boxes of [64 slots][64 dims], 128-byte swizzle)
+//               into a 3-stage ring, running ahead across item boundaries.
+//   warp 1      TMEM allocator and single-thread MMA issuer:
+//                 S_j = Q K_j^T (M=128, N=64, K=192) into one of two S buffers,
+//                 O  += P_j V_j (M=128, N=128, K=64, P from TMEM),
+//               in the order QK_0, QK_1, PV_0, QK_2, PV_1, ... (the tensor core
+//               runs them in issue order, so S may be rewritten right behind
+//               the PV reading the P stored over it).
+//   warps 2-5   one thread per tile row (TMEM lane); warps whose 32 rows are
+//               all padding only keep the barriers: RoPE of the Q rows in
+//               shared memory, masked online softmax in base 2, P written back
+//               to TMEM as bf16, lazy O rescaling, and the epilogue.  A
+//               single-chunk item finishes its rows (sink included); otherwise
+//               it writes (O / l, m + log2 l) and a merge kernel combines the
+//               chunks and the sink with one warp per output row.
+// TMEM: S_0 columns 0..63, S_1 64..127, O 128..255.
 #include <math.h>
 
 #include "common.cuh"
@@ -28,406 +48,504 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kBK = 64;                // keys per block
-constexpr int kThreads = 128;
-constexpr int kKRow = 384;             // bytes per key row (192 bf16)
-constexpr int kVRow = 256;             // bytes per value row (128 bf16)
-constexpr int kStageBytes = kBK * (kKRow + kVRow);
-constexpr int kSmemBytes = 2 * kStageBytes;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past 256x growth
+constexpr int kBK = 64;                    // cache slots per block
+constexpr int kStages = 3;
+constexpr int kBox = kBK * 128;            // [64 slots][64 dims] bf16
+constexpr int kStageBytes = 5 * kBox;      // K: 3 boxes, V: 2 boxes
+constexpr int kQBox = 128 * 128;           // [128 rows][64 dims], rows >= G*T zero
+constexpr int kQBytes = 3 * kQBox;
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kOffQ + 2 * kQBytes;
+constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+__host__ __device__ constexpr uint32_t s_col(uint32_t b) { return b ? 64u : 0u; }
+constexpr uint32_t kOCol = 128;
 constexpr int kSingleChunkMax = 1024;  // ranges up to this many keys use one chunk
-constexpr int kChunk = 2048;           // keys per chunk otherwise
+constexpr int kChunkShort = 2048;      // keys per chunk for caches up to 16K keys
+constexpr int kChunkLong = 4096;       // and beyond
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kOffStage % 1024 == 0 && kBox % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
 
-__device__ __forceinline__ uint32_t k_off(int key, int chunk) {
-  return uint32_t(key * kKRow + ((chunk ^ (key & 7)) << 4));
-}
-__device__ __forceinline__ uint32_t v_off(int key, int chunk) {
-  return uint32_t(key * kVRow + ((chunk ^ (key & 7)) << 4));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                          uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                        uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-struct SplitRange {
-  int lo, kbeg, kend, nsplit;
+struct Bars {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t q_full[2], q_ready[2], q_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done, o_free, drain;
+  uint32_t tmem_base;
+  int abort;
 };
 
-// Keys the T queries of a sequence of length L can see, and this chunk's part.
-__device__ __forceinline__ SplitRange split_range(int L, int T, int window, int chunk, int split) {
-  SplitRange r;
-  r.lo = window > 0 ? max(0, L - T - window + 1) : 0;
-  r.nsplit = (L - r.lo + chunk - 1) / chunk;
-  r.kbeg = r.lo + split * chunk;
-  r.kend = min(L, r.kbeg + chunk);
-  return r;
+// Slots of the cache a work item covers.  Linear cache: the visible positions
+// [lo, L) (lo > 0 only for a window), slot = position.  Ring: slots
+// [0, min(L, cap)).  Either range is cut into chunks of `chunk` slots.
+struct Item {
+  int b, kvh, split, L, s_beg, s_end, nsplit;
+  int ring_r, ring_off;  // slot s holds position s + ring_off + (s < ring_r ? cap : 0)
+};
+
+__device__ __forceinline__ bool slot_range(int L, const DecodeArgs& a, int& lo, int& hi) {
+  if (a.is_ring) {
+    lo = 0;
+    hi = min(L, a.cap);
+  } else {
+    lo = a.window > 0 ? max(0, L - a.T - a.window + 1) : 0;
+    hi = L;
+  }
+  return hi > lo;
 }
 
-// MT: 16-row m-tiles per CTA (1, 2 or 4); the 4 warps = MT m-tiles x KW key groups.
-template <int MT>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
-  constexpr int KW = 4 / MT;
-  constexpr int KPW = kBK / KW;   // keys per warp per block
-  constexpr int NT = KPW / 8;     // n-tiles of 8 keys
-  extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ bool length_ok(int L, const DecodeArgs& a) {
+  return L >= a.T && L <= a.max_seqlen_k && (a.is_ring || L <= a.cap);
+}
+
+// Virtual item v = (split, b, kvh), split-major so that the items of one CTA
+// mix long and short sequences.  Returns 1 for a work item, 0 for an item past
+// a sequence's last chunk, -1 for a sequence whose device-resident length the
+// host could not check and that is skipped.
+__device__ __forceinline__ int item_info(int v, const DecodeArgs& a, Item& it) {
+  const int per = a.B * a.hkv;
+  it.split = v / per;
+  const int rem = v - it.split * per;
+  it.b = rem / a.hkv;
+  it.kvh = rem - it.b * a.hkv;
+  it.L = __ldg(a.seqlens + it.b);
+  if (!length_ok(it.L, a)) return -1;
+  int lo, hi;
+  if (!slot_range(it.L, a, lo, hi)) return 0;
+  const int chunk = a.nsplit > 1 ? a.chunk : (1 << 30);
+  it.nsplit = (hi - lo + chunk - 1) / chunk;
+  if (it.nsplit > a.nsplit) return -1;  // would not fit the workspace the host sized
+  if (it.split >= it.nsplit) return 0;
+  it.s_beg = lo + it.split * chunk;
+  it.s_end = min(hi, it.s_beg + chunk);
+  // a ring keeps the last cap positions [L - cap, L): slot s holds the one
+  // congruent to s (never written, and negative, while L < cap)
+  it.ring_r = 0;
+  it.ring_off = 0;
+  if (a.is_ring) {
+    const int base = it.L - a.cap;
+    int r = base % a.cap;
+    if (r < 0) r += a.cap;
+    it.ring_r = r;
+    it.ring_off = base - r;
+  }
+  return 1;
+}
+
+template <int BN>
+__device__ __forceinline__ void ld_row(uint32_t taddr, uint32_t (&s)[BN]) {
+#pragma unroll
+  for (int c = 0; c < BN; c += 32) tmem_ld32_nowait(taddr + c, s + c);
+  tmem_ld_wait();
+#pragma unroll
+  for (int e = 0; e < BN; ++e) tmem_reg_fence(s[e]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                  const __grid_constant__ CUtensorMap mapV, const DecodeArgs a, int nvirt) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int mt = warp % MT, kg = warp / MT;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int G = a.hq / a.hkv;
   const int T = a.T;
-  const int L = __ldg(a.seqlens + b);
-  if (L < T || L > a.max_seqlen_k || (!a.is_ring && L > a.cap)) {
-    // a device-resident length the host could not check: skip, and say so
-    if (threadIdx.x == 0 && split == 0 && kvh == 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
-    return;
-  }
-  const int chunk = a.nsplit > 1 ? a.chunk : (1 << 30);
-  const SplitRange sr = split_range(L, T, a.window, chunk, split);
-  if (sr.kbeg >= sr.kend) return;  // no keys in this chunk (short sequence)
-
-  // ---- the warp's 16 query rows: r = t * G + hh
   const int rows = G * T;
-  const int r0 = mt * 16 + gid, r1 = r0 + 8;
-  const bool v0 = r0 < rows, v1 = r1 < rows;
-  const int t0r = v0 ? r0 / G : T - 1, t1r = v1 ? r1 / G : T - 1;
-  const int p0 = L - T + t0r, p1 = L - T + t1r;  // query positions
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  const long q0 = ((long(b) * T + t0r) * a.hq + kvh * G + (v0 ? r0 % G : 0)) * kDqk;
-  const long q1 = ((long(b) * T + t1r) * a.hq + kvh * G + (v1 ? r1 % G : 0)) * kDqk;
-  uint32_t qa[12][4];
-#pragma unroll
-  for (int kk = 0; kk < 12; ++kk) {
-    const int c = kk * 16 + 2 * tig;
-    qa[kk][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q + q0 + c)) : 0u;
-    qa[kk][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q + q1 + c)) : 0u;
-    qa[kk][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q + q0 + c + 8)) : 0u;
-    qa[kk][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q + q1 + c + 8)) : 0u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_ready[i], 128);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      // one P barrier per S buffer: QK_{j+1} is issued before PV_j waits for
+      // P_j, so the softmax may finish block j+1 before that wait begins
+      mbar_init(&bars->p_full[i], 128);
+    }
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_free, 128);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
   }
-  // RoPE on dims 0..63: dim d (k-step d/16) pairs with d + 32 (k-step + 2),
-  // which this thread holds in the same register slot.
-#pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-    for (int reg = 0; reg < 4; ++reg) {
-      const int d = kk * 16 + ((reg & 2) ? 8 : 0) + 2 * tig;
-      const int pos = (reg & 1) ? p1 : p0;
-      const float2 x = unpack_bf16x2(qa[kk][reg]);
-      const float2 y = unpack_bf16x2(qa[kk + 2][reg]);
-      const float2 c0 = rope_cos_sin(pos, a.freqs.hi[d], a.freqs.lo[d]);
-      const float2 c1 = rope_cos_sin(pos, a.freqs.hi[d + 1], a.freqs.lo[d + 1]);
-      const float a0 = x.x * c0.x - y.x * c0.y, a1 = x.y * c1.x - y.y * c1.y;
-      const float b0 = y.x * c0.x + x.x * c0.y, b1 = y.y * c1.x + x.y * c1.y;
-      if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
-        record_status(a.ctl, HATTN_ERR_INVALID_ARG);
-      qa[kk][reg] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
-      qa[kk + 2][reg] = pack_f16x2(b0, b1);
-    }
+  // padding rows of both Q tiles stay zero (TMA writes only the first G*T rows)
+  for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) mbar_fence_init();
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&mapQ);
+    tma_prefetch_map(&mapK);
+    tma_prefetch_map(&mapV);
   }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
 
-  // ---- key blocks
-  const uint8_t* kc = static_cast<const uint8_t*>(a.k_cache);
-  const uint8_t* vc = static_cast<const uint8_t*>(a.v_cache);
-  const long head_row0 = (long(b) * a.hkv + kvh) * a.cap;
-  const int nb = (sr.kend - sr.kbeg + kBK - 1) / kBK;
-  const uint32_t sbase = smem_u32(smem);
-
-  auto load_block = [&](int blk, int stage) {
-    const uint32_t ks = sbase + stage * kStageBytes;
-    const uint32_t vs = ks + kBK * kKRow;
-    const int key0 = sr.kbeg + blk * kBK;
-    for (int e = threadIdx.x; e < kBK * 24; e += kThreads) {
-      const int key = e / 24, ch = e - key * 24;
-      const int kp = key0 + key;
-      const bool in = kp < sr.kend;
-      const long slot = a.is_ring ? (kp % a.cap) : kp;
-      const uint8_t* src = kc + (head_row0 + (in ? slot : 0)) * kKRow + ch * 16;
-      cp_async16(ks + k_off(key, ch), src, in ? 16u : 0u);
-    }
-    for (int e = threadIdx.x; e < kBK * 16; e += kThreads) {
-      const int key = e >> 4, ch = e & 15;
-      const int kp = key0 + key;
-      const bool in = kp < sr.kend;
-      const long slot = a.is_ring ? (kp % a.cap) : kp;
-      const uint8_t* src = vc + (head_row0 + (in ? slot : 0)) * kVRow + ch * 16;
-      cp_async16(vs + v_off(key, ch), src, in ? 16u : 0u);
-    }
-    cp_async_commit();
-  };
-
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  // l: exact sums (for lse); lr: sums of the bf16-rounded weights PV uses (for out)
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
-
-  load_block(0, 0);
-  for (int blk = 0; blk < nb; ++blk) {
-    const int stage = blk & 1;
-    if (blk + 1 < nb) {
-      load_block(blk + 1, stage ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t ks = sbase + stage * kStageBytes;
-    const uint32_t vs = ks + kBK * kKRow;
-    const int key_w = kg * KPW;  // warp's first key within the block
-    float s[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 12; ++kk) {
-#pragma unroll
-      for (int n = 0; n < NT; n += 2) {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int key = key_w + (n + (mi >> 1)) * 8 + rr;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ks + k_off(key, kk * 2 + (mi & 1)), b0, b1, b2, b3);
-        if (kk < 4) {  // rotated dims: fp16 x fp16
-          mma_f16(s[n], qa[kk], b0, b1);
-          mma_f16(s[n + 1], qa[kk], b2, b3);
-        } else {
-          mma_bf16(s[n], qa[kk], b0, b1);
-          mma_bf16(s[n + 1], qa[kk], b2, b3);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t pos = 0, qf = 0;
+      bool ok = true;
+      const uint32_t q_bytes = 3u * uint32_t(rows) * 128u;
+      for (int v = blockIdx.x; v < nvirt && ok; v += gridDim.x) {
+        Item it;
+        if (item_info(v, a, it) != 1) continue;
+        const uint32_t qb = qf & 1u;
+        if (!mbar_wait(&bars->q_empty[qb], ((qf >> 1) & 1u) ^ 1u, a.ctl, abort)) break;
+        mbar_arrive_expect_tx(&bars->q_full[qb], q_bytes);
+        for (int i = 0; i < 3; ++i)
+          tma_load_3d(smem + kOffQ + qb * kQBytes + i * kQBox, &mapQ, &bars->q_full[qb], 64 * i,
+                      it.kvh * G, it.b * T);
+        ++qf;
+        const int plane = it.b * a.hkv + it.kvh;
+        const int nb = (it.s_end - it.s_beg + kBK - 1) / kBK;
+        for (int blk = 0; blk < nb; ++blk, ++pos) {
+          const uint32_t st = pos % kStages;
+          if (!mbar_wait(&bars->empty[st], ((pos / kStages) & 1u) ^ 1u, a.ctl, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
+          uint8_t* dst = smem + kOffStage + st * kStageBytes;
+          const int row = it.s_beg + blk * kBK;
+          for (int i = 0; i < 3; ++i)
+            tma_load_3d(dst + i * kBox, &mapK, &bars->full[st], 64 * i, row, plane);
+          for (int i = 0; i < 2; ++i)
+            tma_load_3d(dst + (3 + i) * kBox, &mapV, &bars->full[st], 64 * i, row, plane);
         }
       }
-    }
-    // mask, block max, online update (base 2)
-    const int kp_w = sr.kbeg + blk * kBK + key_w;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int kp = kp_w + n * 8 + 2 * tig + e;
-        const bool in = kp < sr.kend;
-        const bool vis0 = in && kp <= p0 && (a.window == 0 || p0 - kp < a.window);
-        const bool vis1 = in && kp <= p1 && (a.window == 0 || p1 - kp < a.window);
-        s[n][e] = vis0 ? s[n][e] * a.scale_log2 : -INFINITY;
-        s[n][2 + e] = vis1 ? s[n][2 + e] * a.scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, s[n][e]);
-        mx1 = fmaxf(mx1, s[n][2 + e]);
+      // never leave with copies in flight into this CTA's shared memory
+      for (uint32_t i = 0; i < 2; ++i) {
+        const uint32_t fills = qf > i ? (qf - i + 1) / 2 : 0;
+        if (fills) mbar_wait_drain(&bars->q_full[i], (fills - 1) & 1u, a.ctl);
+      }
+      for (uint32_t s = 0; s < uint32_t(kStages); ++s) {
+        const uint32_t fills = pos > s ? (pos - s + kStages - 1) / kStages : 0;
+        if (fills) mbar_wait_drain(&bars->full[s], (fills - 1) & 1u, a.ctl);
       }
     }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_rot = make_idesc_f16(128, kBK, 0, 0);   // dims 0..63
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, kBK, 0, 0);    // dims 64..191
+      constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, 0, 1);
+      const uint32_t sbase = smem_u32(smem);
+      uint32_t qc = 0, items = 0;
+      uint32_t qk = 0, pv = 0;  // QK / PV products issued so far (global block counters)
+      bool ok = true;
+      auto issue_qk = [&](uint32_t qb, uint32_t blk_global) -> bool {
+        const uint32_t st = blk_global % kStages;
+        if (!mbar_wait(&bars->full[st], (blk_global / kStages) & 1u, a.ctl, abort)) return false;
+        tc_fence_after();
+        const uint32_t qbase = sbase + kOffQ + qb * kQBytes;
+        const uint32_t kbase = sbase + kOffStage + st * kStageBytes;
+        const uint32_t d = tmem + s_col(blk_global & 1u);
 #pragma unroll
-    for (int off = 1; off <= 2; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
-    m0 = mn0;
-    m1 = mn1;
-    float rs0 = 0.f, rs1 = 0.f, rr0 = 0.f, rr1 = 0.f;
-    uint32_t pa[NT / 2][4];
+        for (int kk = 0; kk < 12; ++kk) {
+          const uint64_t adesc = make_sdesc_sw128(qbase + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
+          const uint64_t bdesc = make_sdesc_sw128(kbase + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+          umma_ss(d, adesc, bdesc, kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->s_full[blk_global & 1u]);
+        return true;
+      };
+      auto issue_pv = [&](uint32_t blk_global, bool first) -> bool {
+        if (!mbar_wait(&bars->p_full[blk_global & 1u], (blk_global >> 1) & 1u, a.ctl, abort))
+          return false;
+        if (first && items > 0 && !mbar_wait(&bars->o_free, (items - 1) & 1u, a.ctl, abort))
+          return false;
+        tc_fence_after();
+        const uint32_t st = blk_global % kStages;
+        const uint32_t vbase = sbase + kOffStage + st * kStageBytes + 3 * kBox;
+        const uint32_t p = tmem + s_col(blk_global & 1u);
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const float e0 = fast_exp2(s[n][0] - ms0), e1 = fast_exp2(s[n][1] - ms0);
-      const float e2 = fast_exp2(s[n][2] - ms1), e3 = fast_exp2(s[n][3] - ms1);
-      const uint32_t u01 = pack_bf16x2(e0, e1), u23 = pack_bf16x2(e2, e3);
-      const float2 r01 = unpack_bf16x2(u01), r23 = unpack_bf16x2(u23);
-      rs0 += e0 + e1;
-      rs1 += e2 + e3;
-      rr0 += r01.x + r01.y;
-      rr1 += r23.x + r23.y;
-      pa[n >> 1][(n & 1) * 2 + 0] = u01;
-      pa[n >> 1][(n & 1) * 2 + 1] = u23;
-    }
-    l0 = l0 * al0 + rs0;
-    l1 = l1 * al1 + rs1;
-    lr0 = lr0 * al0 + rr0;
-    lr1 = lr1 * al1 + rr1;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= al0;
-      o[n][1] *= al0;
-      o[n][2] *= al1;
-      o[n][3] *= al1;
-    }
-    // O += P V
-#pragma unroll
-    for (int j2 = 0; j2 < NT / 2; ++j2) {
-      const uint32_t afr[4] = {pa[j2][0], pa[j2][1], pa[j2][2], pa[j2][3]};
-      const int k0 = key_w + j2 * 16;
-#pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int key = k0 + (mi & 1) * 8 + rr;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vs + v_off(key, 2 * np + (mi >> 1)), b0, b1, b2, b3);
-        mma_bf16(o[2 * np], afr, b0, b1);
-        mma_bf16(o[2 * np + 1], afr, b2, b3);
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_ts(tmem + kOCol, p + kk * 8, make_sdesc_sw128(vbase + kk * 2048, kBox, 1024),
+                  idesc_o, (!first || kk > 0) ? 1u : 0u);
+        umma_commit(&bars->pv_done);
+        umma_commit(&bars->empty[st]);  // K and V of this block are consumed
+        return true;
+      };
+      for (int v = blockIdx.x; v < nvirt && ok; v += gridDim.x) {
+        Item it;
+        if (item_info(v, a, it) != 1) continue;
+        const uint32_t qb = qc & 1u;
+        if (!mbar_wait(&bars->q_ready[qb], (qc >> 1) & 1u, a.ctl, abort)) break;
+        ++qc;
+        const int nb = (it.s_end - it.s_beg + kBK - 1) / kBK;
+        const uint32_t b0 = qk;  // global index of this item's block 0
+        // QK_0, QK_1, PV_0, QK_2, PV_1, ...; once the item's last QK is
+        // issued its Q buffer may be refilled
+        if (!issue_qk(qb, qk)) break;
+        ++qk;
+        if (nb == 1) umma_commit(&bars->q_empty[qb]);
+        for (int j = 0; j < nb && ok; ++j) {
+          if (j + 1 < nb) {
+            if (!issue_qk(qb, qk)) { ok = false; break; }
+            ++qk;
+            if (j + 2 == nb) umma_commit(&bars->q_empty[qb]);
+          }
+          if (!issue_pv(b0 + j, j == 0)) { ok = false; break; }
+          ++pv;
+        }
+        ++items;
       }
-    }
-    __syncthreads();  // the stage is refilled next iteration
-  }
-
-  // ---- finish: row sums over the quad, then merge the KW key groups
-#pragma unroll
-  for (int off = 1; off <= 2; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    lr0 += __shfl_xor_sync(0xffffffffu, lr0, off);
-    lr1 += __shfl_xor_sync(0xffffffffu, lr1, off);
-  }
-  float* red = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][128] + m, l, lr
-  if (KW > 1) {
-    float* ow = red + warp * (16 * 128);
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int c = n * 8 + 2 * tig;
-      ow[gid * 128 + c] = o[n][0];
-      ow[gid * 128 + c + 1] = o[n][1];
-      ow[(gid + 8) * 128 + c] = o[n][2];
-      ow[(gid + 8) * 128 + c + 1] = o[n][3];
-    }
-    float* ml = red + 4 * 16 * 128 + warp * 48;
-    if (tig == 0) {
-      ml[gid] = m0;
-      ml[gid + 8] = m1;
-      ml[16 + gid] = l0;
-      ml[16 + gid + 8] = l1;
-      ml[32 + gid] = lr0;
-      ml[32 + gid + 8] = lr1;
-    }
-    __syncthreads();
-    if (kg != 0) return;
-    float mm0 = m0, mm1 = m1;
-    for (int w = 1; w < KW; ++w) {
-      const float* mlw = red + 4 * 16 * 128 + (w * MT + mt) * 48;
-      mm0 = fmaxf(mm0, mlw[gid]);
-      mm1 = fmaxf(mm1, mlw[gid + 8]);
-    }
-    const float ms0 = mm0 == -INFINITY ? 0.f : mm0, ms1 = mm1 == -INFINITY ? 0.f : mm1;
-    const float f0 = fast_exp2(m0 - ms0), f1 = fast_exp2(m1 - ms1);
-    l0 *= f0;
-    l1 *= f1;
-    lr0 *= f0;
-    lr1 *= f1;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= f0;
-      o[n][1] *= f0;
-      o[n][2] *= f1;
-      o[n][3] *= f1;
-    }
-    for (int w = 1; w < KW; ++w) {
-      const int ww = w * MT + mt;
-      const float* mlw = red + 4 * 16 * 128 + ww * 48;
-      const float g0 = fast_exp2(mlw[gid] - ms0), g1 = fast_exp2(mlw[gid + 8] - ms1);
-      l0 += mlw[16 + gid] * g0;
-      l1 += mlw[16 + gid + 8] * g1;
-      lr0 += mlw[32 + gid] * g0;
-      lr1 += mlw[32 + gid + 8] * g1;
-      const float* ow2 = red + ww * (16 * 128);
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int c = n * 8 + 2 * tig;
-        o[n][0] += ow2[gid * 128 + c] * g0;
-        o[n][1] += ow2[gid * 128 + c + 1] * g0;
-        o[n][2] += ow2[(gid + 8) * 128 + c] * g1;
-        o[n][3] += ow2[(gid + 8) * 128 + c + 1] * g1;
-      }
-    }
-    m0 = mm0;
-    m1 = mm1;
-  }
-
-  // ---- write
-  if (a.nsplit == 1) {
-    // add the sink and finish the rows
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const bool valid = half ? v1 : v0;
-      const int r = half ? r1 : r0;
-      const float m = half ? m1 : m0;
-      const float l = half ? l1 : l0;
-      const float lr = half ? lr1 : lr0;
-      if (!valid) continue;
-      const int t = r / G, hh = r % G, h = kvh * G + hh;
-      const float sl2 = __ldg(a.sink + h) * kLog2e;
-      const float mt_ = fmaxf(m, sl2);
-      const float msub = mt_ == -INFINITY ? 0.f : mt_;
-      const float fo = fast_exp2(m - msub);
-      const float sw = fast_exp2(sl2 - msub);
-      const float lt = l * fo + sw;
-      const float sc = fo / (lr * fo + sw);
-      const long orow = (long(b) * T + t) * a.hq + h;
-      uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDv);
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int c = n * 8 + 2 * tig;
-        op[c >> 1] = pack_bf16x2(o[n][half * 2] * sc, o[n][half * 2 + 1] * sc);
-      }
-      if (tig == 0 && a.lse) a.lse[orow] = (msub + log2f(lt)) * kLn2;
+      // every MMA issued must be complete before TMEM is released
+      umma_commit(&bars->drain);
+      mbar_wait_drain(&bars->drain, 0, a.ctl);
     }
   } else {
+    // ------------------------------------------------------------ softmax rows
+    const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;            // tile row
+    const bool active = quad * 32 < rows;      // warp has at least one real row
+    const bool real = r < rows;
+    const int t = real ? r / G : 0, hh = real ? r % G : 0;
+    const uint32_t lane_addr = uint32_t(quad * 32) << 16;
+    uint32_t qc = 0, blk = 0, items = 0;
+    // the previous item's row, finished after the next item's Q is rotated
+    bool have_prev = false;
+    float pm = 0.f, pl = 0.f, plr = 0.f;
+    long porow = 0;
+    int pb = 0, ph = 0, psplit = 0, pnsplit = 1;
+    bool ok = true;
+
+    auto epilogue = [&]() -> bool {
+      if (!warp_wait(&bars->pv_done, (blk - 1) & 1u, a.ctl, abort)) return false;
+      tc_fence_after();
+      if (active) {
+        const uint32_t t_o = tmem + lane_addr + kOCol;
+        float sc, lse_v = 0.f;
+        if (pnsplit == 1) {  // add the sink and finish the row
+          const float sl2 = __ldg(a.sink + ph) * kLog2e;
+          const float mt_ = fmaxf(pm, sl2);
+          const float msub = mt_ == -INFINITY ? 0.f : mt_;
+          const float fo = fast_exp2(pm - msub);
+          const float sw = fast_exp2(sl2 - msub);
+          sc = fo / (plr * fo + sw);
+          lse_v = (msub + log2f(pl * fo + sw)) * kLn2;
+        } else {
+          sc = plr > 0.f ? 1.f / plr : 0.f;
+          lse_v = pl > 0.f ? pm + log2f(pl) : -INFINITY;
+        }
+        const long prow = ((long(pb) * a.hq + ph) * T + t) * a.nsplit + psplit;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const bool valid = half ? v1 : v0;
-      const int r = half ? r1 : r0;
-      const float m = half ? m1 : m0;
-      const float l = half ? l1 : l0;
-      const float lr = half ? lr1 : lr0;
-      if (!valid) continue;
-      const int t = r / G, hh = r % G, h = kvh * G + hh;
-      const long prow = ((long(b) * a.hq + h) * T + t) * a.nsplit + split;
-      const float inv = lr > 0.f ? 1.f / lr : 0.f;
-      float2* pp = reinterpret_cast<float2*>(a.part_o + prow * kDv);
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t v[32];
+          tmem_ld32_nowait(t_o + c, v);
+          tmem_ld_wait();
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int c = n * 8 + 2 * tig;
-        pp[c >> 1] = make_float2(o[n][half * 2] * inv, o[n][half * 2 + 1] * inv);
+          for (int e = 0; e < 32; ++e) tmem_reg_fence(v[e]);
+          if (real) {
+            if (pnsplit == 1) {
+              uint4* op = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + porow * 256 + c * 2);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                op[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * sc, __uint_as_float(v[8 * e + 1]) * sc),
+                                   pack_bf16x2(__uint_as_float(v[8 * e + 2]) * sc, __uint_as_float(v[8 * e + 3]) * sc),
+                                   pack_bf16x2(__uint_as_float(v[8 * e + 4]) * sc, __uint_as_float(v[8 * e + 5]) * sc),
+                                   pack_bf16x2(__uint_as_float(v[8 * e + 6]) * sc, __uint_as_float(v[8 * e + 7]) * sc));
+            } else {
+              float4* pp = reinterpret_cast<float4*>(a.part_o + prow * kDv + c);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                pp[e] = make_float4(__uint_as_float(v[4 * e]) * sc, __uint_as_float(v[4 * e + 1]) * sc,
+                                    __uint_as_float(v[4 * e + 2]) * sc, __uint_as_float(v[4 * e + 3]) * sc);
+            }
+          }
+        }
+        if (real) {
+          if (pnsplit == 1) {
+            if (a.lse) a.lse[porow] = lse_v;
+          } else {
+            a.part_lse[prow] = lse_v;
+          }
+        }
       }
-      if (tig == 0) a.part_lse[prow] = l > 0.f ? m + log2f(l) : -INFINITY;
+      tc_fence_before();
+      mbar_arrive(&bars->o_free);
+      return true;
+    };
+
+    for (int v = blockIdx.x; v < nvirt; v += gridDim.x) {
+      Item it;
+      const int st_item = item_info(v, a, it);
+      if (st_item != 1) {
+        if (st_item < 0 && warp == 2 && lane == 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+        continue;
+      }
+      const uint32_t qb = qc & 1u;
+      if (!warp_wait(&bars->q_full[qb], (qc >> 1) & 1u, a.ctl, abort)) { ok = false; break; }
+      ++qc;
+      const int p = it.L - T + t;  // this row's query position
+      if (real) {
+        // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
+        // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
+        uint8_t* qrow = smem + kOffQ + qb * kQBytes + r * 128;
+        uint4 ch[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) ch[c] = *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t* x = reinterpret_cast<uint32_t*>(&ch[c]);
+          uint32_t* y = reinterpret_cast<uint32_t*>(&ch[c + 4]);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int i = 8 * c + 2 * w;
+            const float2 xv = unpack_bf16x2(x[w]);
+            const float2 yv = unpack_bf16x2(y[w]);
+            const float2 c0 = rope_cos_sin(p, a.freqs.hi[i], a.freqs.lo[i]);
+            const float2 c1 = rope_cos_sin(p, a.freqs.hi[i + 1], a.freqs.lo[i + 1]);
+            const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
+            const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
+            if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
+              record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+            x[w] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
+            y[w] = pack_f16x2(b0, b1);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(&bars->q_ready[qb]);
+      if (have_prev && !epilogue()) { ok = false; break; }
+      float m = -INFINITY, l = 0.f, lr = 0.f;
+      const int nb = (it.s_end - it.s_beg + kBK - 1) / kBK;
+      for (int j = 0; j < nb; ++j, ++blk) {
+        const uint32_t sb = blk & 1u;
+        if (!warp_wait(&bars->s_full[sb], (blk >> 1) & 1u, a.ctl, abort)) { ok = false; break; }
+        tc_fence_after();
+        const int sbase_slot = it.s_beg + j * kBK;
+        const int valid_rows = it.s_end - sbase_slot;
+        if (valid_rows < kBK) {
+          // Slots past the item's end were loaded from cache memory the item
+          // does not own (a linear cache's unwritten tail); their weights are
+          // 0, but 0 * NaN is not, so zero those V rows before PV reads them.
+          uint8_t* vrow = smem + kOffStage + (blk % kStages) * kStageBytes + 3 * kBox;
+          for (int e = threadIdx.x - 64; e < (kBK - valid_rows) * 16; e += 128) {
+            const int rr = valid_rows + (e >> 4), c16 = e & 15;
+            *reinterpret_cast<uint4*>(vrow + (c16 >> 3) * kBox + rr * 128 + (c16 & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+        }
+        if (active) {
+          const uint32_t t_s = tmem + lane_addr + s_col(sb);
+          uint32_t s[kBK];
+          ld_row<kBK>(t_s, s);
+          // visibility of slot sl for this row
+          const bool full = !a.is_ring && a.window == 0 &&
+                            sbase_slot + kBK <= min(it.s_end, it.L - T + 1);
+          if (!full) {
+#pragma unroll
+            for (int c = 0; c < kBK; ++c) {
+              const int sl = sbase_slot + c;
+              const int kp = sl + it.ring_off + (sl < it.ring_r ? a.cap : 0);
+              const bool vis = real && sl < it.s_end && kp >= 0 && kp <= p &&
+                               (a.window == 0 || p - kp < a.window);
+              if (!vis) s[c] = __float_as_uint(-INFINITY);
+            }
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBK; c += 2)
+            mx = fmax3f(mx, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+          const float m_new = fmaxf(m, mx * a.scale_log2);
+          const bool resc = m_new > m + kRescaleThreshold;
+          float alpha = 1.f;
+          if (resc) {
+            alpha = fast_exp2(m - m_new);  // 0 when m was -inf
+            m = m_new;
+            l *= alpha;
+            lr *= alpha;
+          }
+          const float msub = (m == -INFINITY) ? 0.f : m;
+          const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+          const uint64_t nm2 = f2_pack(-msub, -msub);
+          uint64_t acc = f2_pack(0.f, 0.f), acc_r = f2_pack(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < kBK; c += 16) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float2 x = f2_unpack(f2_fma(
+                  f2_pack(__uint_as_float(s[c + e]), __uint_as_float(s[c + e + 1])), sc2, nm2));
+              const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+              const uint32_t u = pack_bf16x2(p0, p1);
+              pk[e >> 1] = u;
+              acc = f2_add(acc, f2_pack(p0, p1));
+              acc_r = f2_add(acc_r,
+                             f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)));
+            }
+            tmem_st8(t_s + (c >> 1), pk);  // P (bf16 pairs) over consumed S columns
+          }
+          const float2 sum = f2_unpack(acc), sum_r = f2_unpack(acc_r);
+          l += sum.x + sum.y;
+          lr += sum_r.x + sum_r.y;
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+            // O holds the earlier blocks scaled by 2^-m_old: rescale it once
+            // the PV of the previous block has landed
+            if (!warp_wait(&bars->pv_done, (blk - 1) & 1u, a.ctl, abort)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t t_o = tmem + lane_addr + kOCol;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+              uint32_t v[32];
+              tmem_ld32_nowait(t_o + c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                tmem_reg_fence(v[e]);
+                v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              }
+              tmem_st32(t_o + c, v);
+            }
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[sb]);
+      }
+      if (!ok) break;
+      have_prev = true;
+      pm = m;
+      pl = l;
+      plr = lr;
+      pb = it.b;
+      ph = it.kvh * G + hh;
+      porow = (long(it.b) * T + t) * a.hq + ph;
+      psplit = it.split;
+      pnsplit = it.nsplit;
+      ++items;
     }
+    if (ok && have_prev) epilogue();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// One warp per output row (b, t, h): combine the chunks' (O_i, lse_i) and the
-// sink: lse = log2(sum_i 2^lse_i + 2^s), O = sum_i 2^(lse_i - lse) O_i.
+// One warp per output row (b, t, h) of a sequence cut into several chunks:
+// combine the chunks' (O_i, lse_i) and the sink:
+// lse = log2(sum_i 2^lse_i + 2^s), O = sum_i 2^(lse_i - lse) O_i.
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a) {
   const int lane = threadIdx.x & 31;
   const long row = long(blockIdx.x) * 8 + (threadIdx.x >> 5);  // (b, t, h)
@@ -437,16 +555,19 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a) {
   const int t = int((row / a.hq) % T);
   const int b = int(row / (long(a.hq) * T));
   const int L = __ldg(a.seqlens + b);
-  if (L < T || L > a.max_seqlen_k || (!a.is_ring && L > a.cap)) return;  // reported above
-  const SplitRange sr = split_range(L, T, a.window, a.chunk, 0);
+  if (!length_ok(L, a)) return;  // reported by the decode kernel
+  int lo, hi;
+  slot_range(L, a, lo, hi);
+  const int nsplit = (hi - lo + a.chunk - 1) / a.chunk;
+  if (nsplit <= 1) return;  // a one-chunk sequence was finished by the decode kernel
   const long prow0 = ((long(b) * a.hq + h) * T + t) * a.nsplit;
   const float sl2 = __ldg(a.sink + h) * kLog2e;
   float M = sl2;
-  for (int i = 0; i < sr.nsplit; ++i) M = fmaxf(M, __ldg(a.part_lse + prow0 + i));
+  for (int i = 0; i < nsplit; ++i) M = fmaxf(M, __ldg(a.part_lse + prow0 + i));
   const float msub = M == -INFINITY ? 0.f : M;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = fast_exp2(sl2 - msub);
-  for (int i = 0; i < sr.nsplit; ++i) {
+  for (int i = 0; i < nsplit; ++i) {
     const float w = fast_exp2(__ldg(a.part_lse + prow0 + i) - msub);
     den += w;
     const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + (prow0 + i) * kDv) + lane);
@@ -463,35 +584,46 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a) {
   if (lane == 0 && a.lse) a.lse[row] = (msub + log2f(den)) * kLn2;
 }
 
-template <int MT>
-cudaError_t launch_mt(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(a.nsplit, a.hkv, a.B);
-  decode_kernel<MT><<<grid, kThreads, kSmemBytes, s>>>(a);
+  const int G = a.hq / a.hkv;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, long(a.B) * a.T, a.hq, kDqk, G, a.T) ||
+      !make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, kBK, 1) ||
+      !make_map(&mv, a.v_cache, long(a.B) * a.hkv, a.cap, kDv, kBK, 1))
+    return cudaErrorInvalidValue;
+  const long nvirt = long(a.nsplit) * a.B * a.hkv;
+  const int grid = int(nvirt < num_sms() ? nvirt : num_sms());
+  decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, a, int(nvirt));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.nsplit == 1) return e;
-  const long rows = long(a.B) * a.T * a.hq;
-  decode_merge_kernel<<<dim3(unsigned((rows + 7) / 8)), 256, 0, s>>>(a);
+  const long nrows = long(a.B) * a.T * a.hq;
+  decode_merge_kernel<<<dim3(unsigned((nrows + 7) / 8)), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_num_splits(int max_seqlen_k, int T, int window, int* chunk) {
-  const int range = window > 0 ? (max_seqlen_k < window + T - 1 ? max_seqlen_k : window + T - 1)
-                               : max_seqlen_k;
+int decode_num_splits(int max_seqlen_k, int T, int window, int is_ring, int cap, int* chunk) {
+  int range;
+  if (is_ring)
+    range = max_seqlen_k < cap ? max_seqlen_k : cap;
+  else if (window > 0)
+    range = max_seqlen_k < window + T - 1 ? max_seqlen_k : window + T - 1;
+  else
+    range = max_seqlen_k;
   if (range <= kSingleChunkMax) {
     *chunk = range > 0 ? range : 1;
     return 1;
   }
-  *chunk = kChunk;
-  return (range + kChunk - 1) / kChunk;
+  *chunk = range > 16384 ? kChunkLong : kChunkShort;
+  return (range + *chunk - 1) / *chunk;
 }
 
 size_t decode_workspace_bytes(int B, int T, int hq, int nsplit) {
@@ -502,11 +634,6 @@ size_t decode_workspace_bytes(int B, int T, int hq, int nsplit) {
   return ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  const int rows = (a.hq / a.hkv) * a.T;
-  if (rows <= 16) return launch_mt<1>(a, s);
-  if (rows <= 32) return launch_mt<2>(a, s);
-  return launch_mt<4>(a, s);
-}
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) { return launch_decode_kernel(a, s); }
 
 }  // namespace hattn

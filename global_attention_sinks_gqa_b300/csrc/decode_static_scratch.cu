@@ -50,7 +50,7 @@ extern "C" hattn_status_t hattn_decode_static_scratch(
     int cap, int is_ring, int window, int max_seqlen_k, int rope_dim, float rope_base,
     float softmax_scale, void* stream) {
   const size_t need =
-      hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window);
+      hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window, cap, is_ring);
   if (need > size_t(HATTN_DECODE_STATIC_SCRATCH_BYTES)) return HATTN_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {

@@ -194,12 +194,12 @@ hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const 
 }
 
 size_t hattn_decode_workspace_size(int B, int T, int hq, int hkv, int dv, int max_seqlen_k,
-                                   int window) {
+                                   int window, int cap, int is_ring) {
   (void)hkv;
   (void)dv;
-  if (B <= 0 || T <= 0 || hq <= 0 || max_seqlen_k <= 0 || window < 0) return 0;
+  if (B <= 0 || T <= 0 || hq <= 0 || max_seqlen_k <= 0 || window < 0 || cap <= 0) return 0;
   int chunk = 0;
-  const int nsplit = decode_num_splits(max_seqlen_k, T, window, &chunk);
+  const int nsplit = decode_num_splits(max_seqlen_k, T, window, is_ring != 0, cap, &chunk);
   return decode_workspace_bytes(B, T, hq, nsplit);
 }
 
@@ -243,7 +243,7 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
   a.max_seqlen_k = max_seqlen_k;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   make_rope_freqs(rope_base, &a.freqs);
-  a.nsplit = decode_num_splits(max_seqlen_k, T, window, &a.chunk);
+  a.nsplit = decode_num_splits(max_seqlen_k, T, window, is_ring, cap, &a.chunk);
   const size_t need = decode_workspace_bytes(B, T, hq, a.nsplit);
   a.part_o = nullptr;
   a.part_lse = nullptr;

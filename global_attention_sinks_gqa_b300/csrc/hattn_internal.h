@@ -29,6 +29,15 @@ struct RopeFreqs {
 
 void make_rope_freqs(float base, RopeFreqs* f);
 
+// ---- host helpers (prefill_tc.cu) -------------------------------------------
+// 3-D TMA map over a [rows, heads, dim] bf16 tensor: 64-element (128-byte)
+// inner box of box_heads x box_rows, 128-byte swizzle, out-of-range rows read
+// as zero.  False if the driver entry point is missing or encoding fails.
+bool make_map(CUtensorMap* m, const void* base, long rows, int heads, int dim, int box_heads,
+              int box_rows);
+// Number of SMs of the current device.
+int num_sms();
+
 // ---- rope / append (rope_append.cu) --------------------------------------
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
@@ -76,7 +85,7 @@ struct DecodeArgs {
   int chunk;        // keys per split
   DeviceCtl ctl;
 };
-int decode_num_splits(int max_seqlen_k, int T, int window, int* chunk);
+int decode_num_splits(int max_seqlen_k, int T, int window, int is_ring, int cap, int* chunk);
 size_t decode_workspace_bytes(int B, int T, int hq, int nsplit);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

@@ -136,10 +136,13 @@ hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const 
 
 /*
  * Bytes of workspace hattn_decode() needs for a batch whose longest
- * sequence holds max_seqlen_k tokens (0 when one pass per KV head suffices).
+ * sequence holds max_seqlen_k tokens, with the same cap, is_ring and window
+ * as the hattn_decode() call (0 when one pass per KV head suffices: a
+ * window or ring of at most 1024 keys).  A linear cache is cut into chunks
+ * of 2048 keys (4096 beyond 16K keys); a ring into chunks of its cap slots.
  */
 size_t hattn_decode_workspace_size(int B, int T, int hq, int hkv, int dv, int max_seqlen_k,
-                                   int window);
+                                   int window, int cap, int is_ring);
 
 /*
  * Decode / MTP-verify step: the last T tokens of
@@ -173,9 +176,9 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
 /*
  * Size of the fixed device array hattn_decode_static_scratch() uses as its
  * scratch (32 MiB): enough for B * hq * T * chunks <= 65,000 partial rows of
- * 516 bytes, chunks = ceil(keys / 2048) -- e.g. batch 8 x 64 heads x 4 tokens
- * over up to 32K keys (32,768 rows).  A window layer whose window fits in one
- * chunk needs no scratch at all.
+ * 516 bytes, chunks = ceil(keys / 2048) up to 16K keys, ceil(keys / 4096)
+ * beyond -- e.g. batch 8 x 64 heads x 4 tokens over up to 64K keys (32,768
+ * rows).  A window layer whose ring fits in one chunk needs no scratch at all.
  */
 #define HATTN_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -186,6 +186,23 @@ def test_decode_ga_linear_multi_chunk(T, G):
     _decode_compare(d, max(lens) + 3, False, f"ga T={T} G={G}")
 
 
+@pytest.mark.parametrize("cap,window,T,lens", [
+    (300, 128, 4, [4, 131, 299, 300, 301, 1000, 1234]),    # ring larger than W + T - 1
+    (2100, 2000, 2, [2, 2100, 2101, 5000, 777]),            # ring over two chunks of 2048
+    (5003, 5000, 4, [5003, 9000, 4, 12345]),                # ring over three chunks
+])
+def test_decode_ring_capacities(cap, window, T, lens):
+    d = synth.decode_case(lens, T, 32, 2, window=window, rope_base=1e4, seed=1000 + cap)
+    _decode_compare(d, cap, True, f"ring cap={cap} W={window} T={T}")
+
+
+@pytest.mark.parametrize("window,T", [(128, 4), (1000, 3), (3000, 4)])
+def test_decode_window_over_linear_cache(window, T):
+    lens = [T, 129, 1002, 1500, 3003, 6000]
+    d = synth.decode_case(lens, T, 32, 2, window=window, rope_base=1e4, seed=1100 + window)
+    _decode_compare(d, max(lens) + 5, False, f"linear cache W={window} T={T}")
+
+
 def test_decode_sink_stress():
     lens = [3000, 17, 4096]
     d = synth.decode_case(lens, 4, 64, 4, window=0, rope_base=5e6, seed=900, sink_mean=9.0,

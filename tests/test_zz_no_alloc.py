@@ -26,7 +26,7 @@ def _run_both(d, cap, is_ring, seed):
     q, sink = d.q.to(dev), d.sink.to(dev)
     sl = torch.tensor(d.seqlens, dtype=torch.int32, device=dev)
     maxk = max(d.seqlens)
-    need = ha.hattn_decode_workspace_size(B, T, hq, hkv, 128, maxk, d.window)
+    need = ha.hattn_decode_workspace_size(B, T, hq, hkv, 128, maxk, d.window, cap, int(is_ring))
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     ref_o = torch.empty((B, T, hq, 128), dtype=torch.bfloat16, device=dev)
     ref_l = torch.empty((B, T, hq), dtype=torch.float32, device=dev)
@@ -67,7 +67,7 @@ def test_static_scratch_decode_matches_workspace_decode():
 def test_static_scratch_rejects_steps_beyond_its_size():
     dev = torch.device("cuda")
     B, T, hq, hkv, maxk = 64, 4, 64, 4, 65536  # 1M partial rows: far beyond 32 MiB
-    assert ha.hattn_decode_workspace_size(B, T, hq, hkv, 128, maxk, 0) > 32 * 1024 * 1024
+    assert ha.hattn_decode_workspace_size(B, T, hq, hkv, 128, maxk, 0, maxk, 0) > 32 * 1024 * 1024
     fake = torch.empty(16, dtype=torch.uint8, device=dev)
     st = ha.hattn_decode_static_scratch(fake, fake, fake, fake, fake, fake, fake, B, T, hq, hkv,
                                         192, 128, maxk, 0, 0, maxk, 64, 5e6, 0.07)
