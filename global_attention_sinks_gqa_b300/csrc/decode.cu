@@ -143,6 +143,18 @@ __device__ __forceinline__ void ld_row(uint32_t taddr, uint32_t (&s)[BN]) {
   for (int e = 0; e < BN; ++e) tmem_reg_fence(s[e]);
 }
 
+// cos / sin of RoPE frequency i for this lane's token, when the G lanes
+// sharing a token (lanes l with equal l / G) hold frequencies hl, hl + G, ...
+// in own[] (hl = l % G).  Whole warp calls; i is a compile-time index.
+template <int G>
+__device__ __forceinline__ float2 shared_cos_sin(const float2 (&own)[32 / G], int i, int lane) {
+  if (G == 1) return own[i];
+  const int src = (lane & ~(G - 1)) | (i % G);
+  return make_float2(__shfl_sync(0xffffffffu, own[i / G].x, src),
+                     __shfl_sync(0xffffffffu, own[i / G].y, src));
+}
+
+template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                   const __grid_constant__ CUtensorMap mapV, const DecodeArgs a, int nvirt) {
@@ -152,7 +164,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = a.hq / a.hkv;
   const int T = a.T;
   const int rows = G * T;
 
@@ -314,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;            // tile row
     const bool active = quad * 32 < rows;      // warp has at least one real row
     const bool real = r < rows;
-    const int t = real ? r / G : 0, hh = real ? r % G : 0;
+    const int hh = r % G;                      // = lane % G
+    const int t = real ? r / G : 0;
     const uint32_t lane_addr = uint32_t(quad * 32) << 16;
     uint32_t qc = 0, blk = 0, items = 0;
     // the previous item's row, finished after the next item's Q is rotated
@@ -392,9 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(&bars->q_full[qb], (qc >> 1) & 1u, a.ctl, abort)) { ok = false; break; }
       ++qc;
       const int p = it.L - T + t;  // this row's query position
-      if (real) {
+      if (active) {
         // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
         // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
+        // The G lanes holding one token's heads each evaluate 32/G of the 32
+        // angles and exchange them by shuffles.
+        float2 cs_own[32 / G];
+#pragma unroll
+        for (int k2 = 0; k2 < 32 / G; ++k2)
+          cs_own[k2] = rope_cos_sin(p, a.freqs.hi[hh + G * k2], a.freqs.lo[hh + G * k2]);
         uint8_t* qrow = smem + kOffQ + qb * kQBytes + r * 128;
         uint4 ch[8];
 #pragma unroll
@@ -408,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = 8 * c + 2 * w;
             const float2 xv = unpack_bf16x2(x[w]);
             const float2 yv = unpack_bf16x2(y[w]);
-            const float2 c0 = rope_cos_sin(p, a.freqs.hi[i], a.freqs.lo[i]);
-            const float2 c1 = rope_cos_sin(p, a.freqs.hi[i + 1], a.freqs.lo[i + 1]);
+            const float2 c0 = shared_cos_sin<G>(cs_own, i, lane);
+            const float2 c1 = shared_cos_sin<G>(cs_own, i + 1, lane);
             const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
             const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
             if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
@@ -418,8 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             y[w] = pack_f16x2(b0, b1);
           }
         }
+        if (real) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
+        }
         fence_proxy_async_smem();
       }
       mbar_arrive(&bars->q_ready[qb]);
@@ -585,14 +605,17 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a) {
 }
 
 cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int G = a.hq / a.hkv;
+  auto kern = G == 1 ? decode_kernel<1> : G == 2 ? decode_kernel<2> : G == 4 ? decode_kernel<4>
+              : G == 8 ? decode_kernel<8> : decode_kernel<16>;
+  static bool attr_set[5] = {false, false, false, false, false};
+  const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : 4;
+  if (!attr_set[gi]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[gi] = true;
   }
-  const int G = a.hq / a.hkv;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, a.q, long(a.B) * a.T, a.hq, kDqk, G, a.T) ||
       !make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, kBK, 1) ||
@@ -600,7 +623,7 @@ cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const long nvirt = long(a.nsplit) * a.B * a.hkv;
   const int grid = int(nvirt < num_sms() ? nvirt : num_sms());
-  decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, a, int(nvirt));
+  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, a, int(nvirt));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.nsplit == 1) return e;
   const long nrows = long(a.B) * a.T * a.hq;

@@ -123,6 +123,17 @@ struct Cfg {
 __host__ __device__ constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
 __host__ __device__ constexpr uint32_t o_col(int t) { return t ? 384u : 256u; }
 
+// cos / sin of RoPE frequency i for this lane's token, when the G lanes
+// sharing a token (lanes l with equal l / G) hold frequencies hl, hl + G, ...
+// in own[] (hl = l % G).  Whole warp calls; i is a compile-time index.
+template <int G>
+__device__ __forceinline__ float2 shared_cos_sin(const float2 (&own)[32 / G], int i, int lane) {
+  if (G == 1) return own[i];
+  const int src = (lane & ~(G - 1)) | (i % G);
+  return make_float2(__shfl_sync(0xffffffffu, own[i / G].x, src),
+                     __shfl_sync(0xffffffffu, own[i / G].y, src));
+}
+
 template <int N>
 __device__ __forceinline__ void reg_dealloc() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
@@ -514,7 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qpos = qmin + tl;
       // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
       // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
+      // The G lanes holding one token's heads each evaluate 32/G of the 32
+      // angles and exchange them by shuffles.
       {
+        float2 cs_own[32 / G];
+#pragma unroll
+        for (int k2 = 0; k2 < 32 / G; ++k2)
+          cs_own[k2] = rope_cos_sin(qpos, a.freqs.hi[hl + G * k2], a.freqs.lo[hl + G * k2]);
         uint8_t* qrow = smem + C::kOffQ + t * C::kQBytes + r * 128;
         uint4 ch[8];
 #pragma unroll
@@ -528,8 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = 8 * c + 2 * w;
             const float2 xv = unpack_bf16x2(x[w]);
             const float2 yv = unpack_bf16x2(y[w]);
-            const float2 c0 = rope_cos_sin(qpos, a.freqs.hi[i], a.freqs.lo[i]);
-            const float2 c1 = rope_cos_sin(qpos, a.freqs.hi[i + 1], a.freqs.lo[i + 1]);
+            const float2 c0 = shared_cos_sin<G>(cs_own, i, lane);
+            const float2 c1 = shared_cos_sin<G>(cs_own, i + 1, lane);
             const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
             const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
             if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)

@@ -70,22 +70,58 @@ __device__ __forceinline__ bool rope_key_row(const uint4* src, uint4* dst, int p
 
 constexpr int kRowsPerBlock = 8;  // one warp per row
 
+// Rotated-key pre-pass of prefill: one warp per token, all hkv heads of it.
+// The token's 32 (cos, sin) pairs are computed once (lane i: frequency i) and
+// shared through shared memory by every head; the warp then walks the
+// token's hkv x 24 16-byte chunks with coalesced 128-bit loads and stores.
+// A chunk of dims 0..63 loads its partner chunk (i <-> i + 32) as well.
+constexpr int kTokWarps = 8;
+
 __global__ void __launch_bounds__(256) rope_keys_packed_kernel(
     const uint4* __restrict__ k, uint4* __restrict__ k_rot, const int* __restrict__ cu_seqlens,
     int batch, long total, int hkv, const RopeFreqs f, const DeviceCtl ctl) {
-  const int lane = threadIdx.x & 31;
-  const long row = long(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
-  if (row >= total * hkv) return;
-  const long n = row / hkv;
-  // sequence holding packed token n: largest b with cu[b] <= n
-  int lo = 0, hi = batch;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(cu_seqlens + mid) <= n) lo = mid; else hi = mid - 1;
+  __shared__ float2 cs_tab[kTokWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const long nchunks = long(hkv) * 24;
+  bool overflow = false;
+  for (long n = long(blockIdx.x) * kTokWarps + w; n < total; n += long(gridDim.x) * kTokWarps) {
+    // sequence holding packed token n: largest b with cu[b] <= n
+    int lo = 0, hi = batch;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(cu_seqlens + mid) <= n) lo = mid; else hi = mid - 1;
+    }
+    const int pos = int(n - __ldg(cu_seqlens + lo));
+    __syncwarp();
+    cs_tab[w][lane] = rope_cos_sin(pos, f.hi[lane], f.lo[lane]);
+    __syncwarp();
+    const uint4* src = k + n * nchunks;
+    uint4* dst = k_rot + n * nchunks;
+    for (long q = lane; q < nchunks; q += 32) {
+      const int c = int(q % 24);
+      uint4 x = __ldg(src + q);
+      if (c < 8) {
+        const bool first = c < 4;  // dims i (first half) vs i + 32 (second half)
+        const uint4 pr = __ldg(src + (first ? q + 4 : q - 4));
+        const int i0 = 8 * (c & 3);
+        uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        const uint32_t ps[4] = {pr.x, pr.y, pr.z, pr.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = unpack_bf16x2(xs[e]);
+          const float2 b = unpack_bf16x2(ps[e]);
+          const float2 cs0 = cs_tab[w][i0 + 2 * e], cs1 = cs_tab[w][i0 + 2 * e + 1];
+          const float y0 = first ? a.x * cs0.x - b.x * cs0.y : a.x * cs0.x + b.x * cs0.y;
+          const float y1 = first ? a.y * cs1.x - b.y * cs1.y : a.y * cs1.x + b.y * cs1.y;
+          if (fabsf(y0) > kF16Max || fabsf(y1) > kF16Max) overflow = true;
+          xs[e] = pack_f16x2(y0, y1);
+        }
+        x = make_uint4(xs[0], xs[1], xs[2], xs[3]);
+      }
+      dst[q] = x;
+    }
   }
-  const int pos = int(n - __ldg(cu_seqlens + lo));
-  if (rope_key_row(k + row * 24, k_rot + row * 24, pos, lane, f))
-    record_status(ctl, HATTN_ERR_INVALID_ARG);
+  if (overflow) record_status(ctl, HATTN_ERR_INVALID_ARG);
 }
 
 __global__ void __launch_bounds__(256) kv_append_kernel(
@@ -115,9 +151,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
                                     cudaStream_t s) {
-  const long rows = total * hkv;
-  if (rows == 0) return cudaSuccess;
-  const long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (total == 0) return cudaSuccess;
+  long blocks = (total + kTokWarps - 1) / kTokWarps;
+  const long cap_blocks = long(num_sms()) * 8;  // grid-stride beyond 8 blocks per SM
+  if (blocks > cap_blocks) blocks = cap_blocks;
   rope_keys_packed_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
       static_cast<const uint4*>(k), static_cast<uint4*>(k_rot), cu_seqlens, batch, total, hkv, f,
       ctl);
