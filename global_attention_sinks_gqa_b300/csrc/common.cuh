@@ -366,6 +366,23 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Running max of |x| over packed fp16 pairs: max(|acc|, |a|, |b|) per half.
+// With the sign bits cleared, fp16 magnitudes order like unsigned integers.
+__device__ __forceinline__ uint32_t f16x2_absmax3(uint32_t acc, uint32_t a, uint32_t b) {
+  const uint32_t m = 0x7fff7fffu;
+  return __vmaxu2(__vmaxu2(a & m, b & m), acc);
+}
+// True if either fp16 half is +-inf or NaN (its exponent bits are all ones).
+__device__ __forceinline__ bool f16x2_any_inf(uint32_t x) {
+  return ((x & 0x7c00u) == 0x7c00u) || ((x & 0x7c000000u) == 0x7c000000u);
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -32,10 +32,11 @@
 //               order, so S_t may be rewritten right behind the PV reading P_t.
 //   warps 2-3   idle (they complete warpgroup 0 for the register split)
 //   warps 4-7   tile A, one thread per query row (TMEM lane): RoPE of the Q
-//   warps 8-11  tile B  tile, masked online softmax in base 2 with the running
-//               max started at the sink logit, P written back to TMEM as bf16
-//               over the consumed S columns, lazy O rescaling (only when the
-//               max grows by more than 2^8), and the epilogue O / (l + 2^(s-m)).
+//   warps 8-11  tile B  tile, masked online softmax in base 2 (running max
+//               exact after the first block, then moved only when it grows
+//               by more than 2^8, with O rescaled then), P written back to
+//               TMEM as bf16 over the consumed S columns, and the epilogue,
+//               which folds in the sink: O 2^m / (2^m l + 2^s).
 // TMEM: S_A 0.., S_B 128.., O_A 256..383, O_B 384..511.
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -178,36 +179,54 @@ __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, int nut, 
   return true;
 }
 
-// One block of the online softmax for one query row.  s holds the row's BN raw
-// logits; masked columns become -inf.  Writes P (bf16) into the S columns and
-// updates the running max m, the exact sum l (for lse) and the sum lr of the
-// bf16-rounded weights PV uses (for out; equal to l on unmasked blocks).
-template <int BN, bool MASKED>
-__device__ __forceinline__ void softmax_block(uint32_t (&s)[BN], int c_lo, int c_hi,
-                                              float scale_log2, uint32_t t_s, uint32_t t_o,
-                                              bool may_rescale, float& m, float& l, float& lr) {
-  if (MASKED) {
+// Masks of one block: columns past the causal edge (c > c_hi) and / or
+// before the window's far edge (c < c_lo) become -inf.  A block only pays for
+// the edges that fall inside it.
+template <int BN>
+__device__ __forceinline__ void mask_block(uint32_t (&s)[BN], bool lower, bool upper, int c_lo,
+                                           int c_hi) {
+  if (lower && upper) {
 #pragma unroll
     for (int c = 0; c < BN; ++c)
-      if (c > c_hi || c < c_lo) s[c] = __float_as_uint(-INFINITY);
-  }
-  float mx = -INFINITY;
+      if (unsigned(c - c_lo) > unsigned(c_hi - c_lo)) s[c] = __float_as_uint(-INFINITY);
+  } else if (lower) {
 #pragma unroll
-  for (int c = 0; c + 1 < BN; c += 2)
-    mx = fmax3f(mx, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-  const float m_new = fmaxf(m, mx * scale_log2);
+    for (int c = 0; c < BN; ++c)
+      if (c < c_lo) s[c] = __float_as_uint(-INFINITY);
+  } else if (upper) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c)
+      if (c > c_hi) s[c] = __float_as_uint(-INFINITY);
+  }
+}
+
+// One block of the online softmax for one query row.  s holds the row's BN
+// (masked) raw logits.  Writes P (bf16) into the S columns and updates the
+// running max m (log2 units, -inf before the first block) and the sum l of
+// 2^(x - m).  The first block sets m to its exact maximum, so the dominant
+// key's weight is exactly 1 in bf16; later blocks move m only when the max
+// grows by more than 2^8 (then O, l are rescaled).
+template <int BN>
+__device__ __forceinline__ void softmax_block(uint32_t (&s)[BN], float scale_log2, uint32_t t_s,
+                                              uint32_t t_o, bool may_rescale, float& m, float& l) {
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c + 3 < BN; c += 4) {
+    mx0 = fmax3f(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    mx1 = fmax3f(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+  }
+  const float m_new = fmaxf(m, fmaxf(mx0, mx1) * scale_log2);
   const bool resc = m_new > m + kRescaleThreshold;
   float alpha = 1.f;
   if (resc) {
     alpha = fast_exp2(m - m_new);  // 0 when m was -inf
     m = m_new;
     l *= alpha;
-    lr *= alpha;
   }
   const float msub = (m == -INFINITY) ? 0.f : m;
   const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
   const uint64_t nm2 = f2_pack(-msub, -msub);
-  uint64_t acc = f2_pack(0.f, 0.f), acc_r = f2_pack(0.f, 0.f);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
 #pragma unroll
   for (int c = 0; c < BN; c += 16) {
     uint32_t pk[8];
@@ -216,22 +235,16 @@ __device__ __forceinline__ void softmax_block(uint32_t (&s)[BN], int c_lo, int c
       const float2 x = f2_unpack(
           f2_fma(f2_pack(__uint_as_float(s[c + e]), __uint_as_float(s[c + e + 1])), sc2, nm2));
       const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-      const uint32_t u = pack_bf16x2(p0, p1);
-      pk[e >> 1] = u;
-      acc = f2_add(acc, f2_pack(p0, p1));
-      if (MASKED)
-        acc_r = f2_add(acc_r, f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)));
+      pk[e >> 1] = pack_bf16x2(p0, p1);
+      if (e & 2)
+        acc1 = f2_add(acc1, f2_pack(p0, p1));
+      else
+        acc0 = f2_add(acc0, f2_pack(p0, p1));
     }
     tmem_st8(t_s + (c >> 1), pk);  // P (bf16 pairs) over consumed S columns
   }
-  const float2 sum = f2_unpack(acc);
+  const float2 sum = f2_unpack(f2_add(acc0, acc1));
   l += sum.x + sum.y;
-  if (MASKED) {
-    const float2 sr = f2_unpack(acc_r);
-    lr += sr.x + sr.y;
-  } else {
-    lr += sum.x + sum.y;
-  }
   if (may_rescale && __any_sync(0xffffffffu, resc)) {
     // O holds the earlier blocks scaled by 2^-m_old; the PV that wrote them is
     // complete (the S block just waited for was committed after it), and the
@@ -319,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t pos = 0;            // ring positions filled so far
-      uint32_t qfills[2] = {0, 0};
+      uint32_t qfills0 = 0, qfills1 = 0;  // Q loads issued into the tile A / B buffer
       bool ok = true;
       auto load_box = [&](const CUtensorMap* map, int dim0, int g, int row) -> bool {
         const uint32_t slot = pos % NSLOT;
@@ -337,8 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K_0 first (its slots free up while the previous unit finishes), then
         // the two Q tiles, then V_0, K_1, V_1, ...
         for (int i = 0; i < 3 && ok; ++i) ok = load_box(&mapK, 64 * i, ui.g, row0);
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!mbar_wait(&bars->q_empty[t], (qfills[t] & 1u) ^ 1u, a.ctl, abort)) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          uint32_t& qf = t ? qfills1 : qfills0;
+          if (!mbar_wait(&bars->q_empty[t], (qf & 1u) ^ 1u, a.ctl, abort)) {
             ok = false;
             break;
           }
@@ -347,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 3; ++i)
             tma_load_3d(qdst + i * C::kQBox, &mapQ, &bars->q_full[t], 64 * i, ui.g * G,
                         ui.tok0 + ui.t0 + t * TQ);
-          ++qfills[t];
+          ++qf;
         }
         for (int j = 0; j < ui.nblk && ok; ++j) {
           for (int i = 0; i < 2 && ok; ++i) ok = load_box(&mapV, 64 * i, ui.g, row0 + j * BN);
@@ -357,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // never leave with copies in flight into this CTA's shared memory
-      for (int t = 0; t < 2; ++t)
-        if (qfills[t]) mbar_wait_drain(&bars->q_full[t], (qfills[t] - 1) & 1u, a.ctl);
+      if (qfills0) mbar_wait_drain(&bars->q_full[0], (qfills0 - 1) & 1u, a.ctl);
+      if (qfills1) mbar_wait_drain(&bars->q_full[1], (qfills1 - 1) & 1u, a.ctl);
       for (uint32_t sl = 0; sl < uint32_t(NSLOT); ++sl) {
         const uint32_t fills = pos > sl ? (pos - sl + NSLOT - 1) / NSLOT : 0;
         if (fills) mbar_wait_drain(&bars->kv_full[sl], (fills - 1) & 1u, a.ctl);
@@ -480,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t blk = 0, uc = 0;
     // the previous unit's row, finished after the next unit's Q is rotated
     bool have_prev = false;
-    float pm = 0.f, pl = 0.f, plr = 0.f, psink = 0.f;
+    float pm = 0.f, pl = 0.f, psink = 0.f;
     bool pvalid = false;
     long porow = 0;
     uint32_t pblk = 0;
@@ -488,10 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto epilogue = [&]() -> bool {
       if (!warp_wait(&bars->pv_done[t], (pblk - 1) & 1u, a.ctl, abort)) return false;
       tc_fence_after();
-      const float msub = (pm == -INFINITY) ? 0.f : pm;
-      const float sink_w = exp2f(psink - msub);
-      const float l_tot = pl + sink_w;
-      const float inv = 1.f / (plr + sink_w);
+      // fold in the sink: denominator 2^m l + 2^s, taken relative to max(m, s)
+      const float mt = fmaxf(pm, psink);
+      const float msub = (mt == -INFINITY) ? 0.f : mt;
+      const float fo = exp2f(pm - msub);
+      const float l_tot = pl * fo + exp2f(psink - msub);
+      const float inv = fo / l_tot;
+      const uint64_t inv2 = f2_pack(inv, inv);
       uint4* optr = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + porow * 256);
 #pragma unroll
       for (int c = 0; c < 128; c += 32) {
@@ -502,8 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; ++e) tmem_reg_fence(v[e]);
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+        for (int e = 0; e < 16; ++e) {
+          const float2 y = f2_unpack(
+              f2_mul(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), inv2));
+          pk[e] = pack_bf16x2(y.x, y.y);
+        }
         if (pvalid) {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -536,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 ch[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) ch[c] = *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
+        uint32_t big = 0u;  // |rotated| of every pair, as fp16 (inf once out of range)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t* x = reinterpret_cast<uint32_t*>(&ch[c]);
@@ -549,12 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 c1 = shared_cos_sin<G>(cs_own, i + 1, lane);
             const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
             const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
-            if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
-              record_status(a.ctl, HATTN_ERR_INVALID_ARG);
             x[w] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
             y[w] = pack_f16x2(b0, b1);
+            big = f16x2_absmax3(big, x[w], y[w]);
           }
         }
+        if (f16x2_any_inf(big)) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
 #pragma unroll
         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
         fence_proxy_async_smem();
@@ -563,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (have_prev && !epilogue()) { ok = false; break; }
       const int h = ui.g * G + hl;
       const float sink_l2 = __ldg(a.sink + h) * kLog2e;
-      float m = sink_l2;  // running max (log2 units), started at the sink logit
-      float l = 0.f, lr = 0.f;
+      float m = -INFINITY;  // running max (log2 units); the sink joins at the end
+      float l = 0.f;
       const int qmax = qmin + TQ - 1;
       for (int j = 0; j < ui.nblk; ++j, ++blk) {
         if (!warp_wait(&bars->s_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
@@ -572,16 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb = ui.kstart + j * BN;  // position of column 0
         uint32_t s[BN];
         load_s_row<BN>(t_s, s);
-        // the block needs a mask if any row of the tile loses a column to the
-        // causal edge or (sliding window) to the window's far edge
-        const bool masked = (kb + BN - 1 > qmin) || (WIN && kb < qmax - a.window + 1);
-        if (masked) {
-          const int c_hi = qpos - kb;
-          const int c_lo = WIN ? qpos - a.window + 1 - kb : -1;
-          softmax_block<BN, true>(s, c_lo, c_hi, a.scale_log2, t_s, t_o, j > 0, m, l, lr);
-        } else {
-          softmax_block<BN, false>(s, 0, BN, a.scale_log2, t_s, t_o, j > 0, m, l, lr);
-        }
+        // masks where a row of the tile loses columns to the causal edge
+        // (upper) or, with a window, to the window's far edge (lower)
+        const bool upper = kb + BN - 1 > qmin;
+        const bool lower = WIN && kb < qmax - a.window + 1;
+        mask_block<BN>(s, lower, upper, qpos - a.window + 1 - kb, qpos - kb);
+        softmax_block<BN>(s, a.scale_log2, t_s, t_o, j > 0, m, l);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
@@ -590,7 +609,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       have_prev = true;
       pm = m;
       pl = l;
-      plr = lr;
       psink = sink_l2;
       pvalid = qpos < ui.L;
       porow = long(ui.tok0 + qpos) * a.hq + h;

@@ -47,14 +47,15 @@ def oracle_prefill(c: synth.PrefillCase, rows=None, window=None):
                           scale=c.scale, rows=rows)
 
 
-def fill_cache(d: synth.DecodeCase, cap: int, is_ring: bool, upto=None):
+def fill_cache(d: synth.DecodeCase, cap: int, is_ring: bool, upto=None, init: float = 0.0):
     """KV caches holding positions [0, upto_b) of every sequence, written by
     the CUDA append kernel from the un-rotated history (ring: only the last
-    cap positions, which are the ones a ring keeps)."""
+    cap positions, which are the ones a ring keeps).  Slots never written
+    hold `init`."""
     dev = torch.device("cuda")
     B, hkv = d.B, d.hkv
-    kc = torch.zeros((B, hkv, cap, synth.D_QK), dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros((B, hkv, cap, synth.D_V), dtype=torch.bfloat16, device=dev)
+    kc = torch.full((B, hkv, cap, synth.D_QK), init, dtype=torch.bfloat16, device=dev)
+    vc = torch.full((B, hkv, cap, synth.D_V), init, dtype=torch.bfloat16, device=dev)
     kh = d.k_hist if d.k_hist.is_cuda else d.k_hist.to(dev)
     vh = d.v_hist if d.v_hist.is_cuda else d.v_hist.to(dev)
     for b in range(B):

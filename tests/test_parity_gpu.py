@@ -156,9 +156,9 @@ def test_append_writes_rotated_keys_into_slots():
         assert (vc_h.permute(0, 2, 1, 3)[untouched] == 7.0).all()
 
 
-def _decode_compare(d, cap, is_ring, what):
+def _decode_compare(d, cap, is_ring, what, init=0.0):
     dev = torch.device("cuda")
-    kc, vc = fill_cache(d, cap, is_ring)
+    kc, vc = fill_cache(d, cap, is_ring, init=init)
     sl = torch.tensor(d.seqlens, dtype=torch.int32, device=dev)
     out, lse = ha.decode(d.q.to(dev), kc, vc, sl, d.sink.to(dev), max_seqlen_k=max(d.seqlens),
                          window=d.window, is_ring=is_ring, rope_base=d.rope_base,
@@ -201,6 +201,28 @@ def test_decode_window_over_linear_cache(window, T):
     lens = [T, 129, 1002, 1500, 3003, 6000]
     d = synth.decode_case(lens, T, 32, 2, window=window, rope_base=1e4, seed=1100 + window)
     _decode_compare(d, max(lens) + 5, False, f"linear cache W={window} T={T}")
+
+
+@pytest.mark.parametrize("cap,window,T,lens", [
+    (131, 128, 4, [5, 60, 130, 400]),          # ring: slots past L never written
+    (300, 128, 2, [2, 299, 700]),              # general ring path
+    (6000, 0, 4, [3000, 100, 5999, 4]),        # linear cache: the tail past L
+])
+def test_decode_unwritten_slots_hold_nan(cap, window, T, lens):
+    """Cache slots nobody wrote may hold anything, NaN included: a key there
+    has weight 0 and must not turn the output into 0 * NaN."""
+    is_ring = window > 0
+    d = synth.decode_case(lens, T, 32, 2, window=window, rope_base=1e4 if is_ring else 5e6,
+                          seed=1300 + cap)
+    _decode_compare(d, cap, is_ring, f"NaN-filled cache cap={cap}", init=float("nan"))
+
+
+@pytest.mark.parametrize("window,T", [(1, 1), (2, 2), (5, 4), (16, 1)])
+def test_decode_tiny_rings(window, T):
+    cap = window + T - 1
+    d = synth.decode_case([T, T + 1, 7, 50], T, 64, 4, window=window, rope_base=1e4,
+                          seed=1400 + window * 10 + T)
+    _decode_compare(d, cap, True, f"tiny ring W={window} T={T}")
 
 
 def test_decode_sink_stress():
