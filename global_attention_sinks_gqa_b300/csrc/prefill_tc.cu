@@ -96,8 +96,8 @@ constexpr int kThreads = 384;
 // the increase would wait forever; the host checks the kernel's register
 // count against kRegsLaunch before every launch.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsLow = 104;
-constexpr int kRegsHigh = 200;
+constexpr int kRegsLow = 152;
+constexpr int kRegsHigh = 176;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split");
 
 template <int G, int BN>
@@ -403,33 +403,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto release_slots = [&](uint32_t p0, int n) {
         for (int i = 0; i < n; ++i) umma_commit(&bars->kv_empty[(p0 + i) % NSLOT]);
       };
+      // Shared-memory descriptors are built once; a k-step or slot only adds
+      // its byte offset / 16 to the start-address field (addresses stay below
+      // 256 KB, so the 14-bit field never carries).
+      const uint64_t qdesc0 = make_sdesc_sw128(qbase, 16, 1024);
+      const uint64_t kdesc0 = make_sdesc_sw128(rbase, 16, 1024);
+      const uint64_t vdesc0 = make_sdesc_sw128(rbase, C::kSlot, 1024);
       auto issue_qk = [&](int t, uint32_t kpos) {
-        const uint32_t qb = qbase + t * C::kQBytes;
+        const uint64_t qd = qdesc0 + uint64_t((t * C::kQBytes) >> 4);
+        const uint32_t ks0 = kpos % NSLOT;
+        const uint32_t ks1 = ks0 + 1 == uint32_t(NSLOT) ? 0u : ks0 + 1;
+        const uint32_t ks2 = ks1 + 1 == uint32_t(NSLOT) ? 0u : ks1 + 1;
+        const uint64_t kd[3] = {kdesc0 + uint64_t((ks0 * C::kSlot) >> 4),
+                                kdesc0 + uint64_t((ks1 * C::kSlot) >> 4),
+                                kdesc0 + uint64_t((ks2 * C::kSlot) >> 4)};
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          const uint32_t kslot = (kpos + (kk >> 2)) % NSLOT;
-          const uint64_t adesc = make_sdesc_sw128(qb + (kk >> 2) * C::kQBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bdesc = make_sdesc_sw128(rbase + kslot * C::kSlot + (kk & 3) * 32, 16, 1024);
-          umma_ss(tmem + s_col(t), adesc, bdesc, kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 12; ++kk)
+          umma_ss(tmem + s_col(t), qd + uint64_t(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4),
+                  kd[kk >> 2] + uint64_t(((kk & 3) * 32) >> 4), kk < 4 ? idesc_rot : idesc_s,
+                  kk > 0 ? 1u : 0u);
       };
       auto issue_pv = [&](int t, uint32_t vpos, bool acc) {
-        const uint32_t s0 = vpos % NSLOT, s1 = (vpos + 1) % NSLOT;
-        const uint32_t v0 = rbase + s0 * C::kSlot, v1 = rbase + s1 * C::kSlot;
+        const uint32_t s0 = vpos % NSLOT;
+        const uint32_t s1 = s0 + 1 == uint32_t(NSLOT) ? 0u : s0 + 1;
+        const uint64_t vd0 = vdesc0 + uint64_t((s0 * C::kSlot) >> 4);
+        const uint64_t vd1 = vdesc0 + uint64_t((s1 * C::kSlot) >> 4);
         const uint32_t p_tmem = tmem + s_col(t);
         if (s1 == s0 + 1) {  // the two 64-dim halves of V are adjacent: one N=128 MMA per k-step
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tmem + o_col(t), p_tmem + kk * 8, make_sdesc_sw128(v0 + kk * 2048, C::kSlot, 1024),
-                    idesc_o, (acc || kk > 0) ? 1u : 0u);
+            umma_ts(tmem + o_col(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o,
+                    (acc || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            umma_ts(tmem + o_col(t), p_tmem + kk * 8, make_sdesc_sw128(v0 + kk * 2048, C::kSlot, 1024),
-                    idesc_o64, (acc || kk > 0) ? 1u : 0u);
-            umma_ts(tmem + o_col(t) + 64, p_tmem + kk * 8,
-                    make_sdesc_sw128(v1 + kk * 2048, C::kSlot, 1024), idesc_o64,
+            umma_ts(tmem + o_col(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o64,
                     (acc || kk > 0) ? 1u : 0u);
+            umma_ts(tmem + o_col(t) + 64, p_tmem + kk * 8, vd1 + uint64_t((kk * 2048) >> 4),
+                    idesc_o64, (acc || kk > 0) ? 1u : 0u);
           }
         }
       };
@@ -501,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long porow = 0;
     uint32_t pblk = 0;
 
+    const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
     auto epilogue = [&]() -> bool {
       if (!warp_wait(&bars->pv_done[t], (pblk - 1) & 1u, a.ctl, abort)) return false;
       tc_fence_after();
@@ -511,25 +523,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float l_tot = pl * fo + exp2f(psink - msub);
       const float inv = fo / l_tot;
       const uint64_t inv2 = f2_pack(inv, inv);
-      uint4* optr = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + porow * 256);
+      uint8_t* orow_ptr = static_cast<uint8_t*>(a.out) + porow * 256;
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t v[32];
-        tmem_ld32_nowait(t_o + c, v);
+      for (int half = 0; half < 2; ++half) {  // 64 columns in flight per wait
+        uint32_t v[64];
+        tmem_ld32_nowait(t_o + half * 64, v);
+        tmem_ld32_nowait(t_o + half * 64 + 32, v + 32);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) tmem_reg_fence(v[e]);
-        uint32_t pk[16];
+        for (int e = 0; e < 64; ++e) tmem_reg_fence(v[e]);
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 32; ++e) {
           const float2 y = f2_unpack(
               f2_mul(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), inv2));
           pk[e] = pack_bf16x2(y.x, y.y);
         }
         if (pvalid) {
+          uint8_t* dst = orow_ptr + half * 128;
+          if (out32) {  // 32-byte stores: one full sector each
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            optr[(c >> 3) + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            for (int e = 0; e < 4; ++e) st_global_v8(dst + 32 * e, pk + 8 * e);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              reinterpret_cast<uint4*>(dst)[e] =
+                  make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
         }
       }
       if (pvalid && a.lse != nullptr) a.lse[porow] = (msub + log2f(l_tot)) * kLn2;
