@@ -30,6 +30,7 @@
 //               (S: M=128, N=BN, K=192 from shared memory; PV: P from TMEM,
 //               V from shared memory).  The tensor core runs them in issue
 //               order, so S_t may be rewritten right behind the PV reading P_t.
+//               (Two issuers, one per tile, measured slower.)
 //   warps 2-3   idle (they complete warpgroup 0 for the register split)
 //   warps 4-7   tile A, one thread per query row (TMEM lane): RoPE of the Q
 //   warps 8-11  tile B  tile, masked online softmax in base 2 (running max
@@ -144,6 +145,8 @@ __device__ __forceinline__ void reg_alloc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+constexpr int kCuCache = 128;  // batches up to 127 sequences keep cu_seqlens in shared memory
+
 template <int NSLOT>
 struct Bars {
   uint64_t q_full[2], q_ready[2], q_empty[2];
@@ -152,6 +155,7 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int cu[kCuCache];
 };
 
 struct UnitInfo {
@@ -161,7 +165,8 @@ struct UnitInfo {
 // Unit u of the persistent loop.  Global units run latest (longest) first so
 // the tail of the schedule is short; window units run in order.
 template <int G, int BN, bool WIN>
-__device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, int nut, UnitInfo& ui) {
+__device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, const int* cu, int nut,
+                                          UnitInfo& ui) {
   constexpr int UT = 256 / G;
   const int per = a.batch * a.hkv;
   const int q_ord = u / per;
@@ -169,8 +174,8 @@ __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, int nut, 
   const int qt = WIN ? q_ord : (nut - 1 - q_ord);
   ui.b = rem / a.hkv;
   ui.g = rem - ui.b * a.hkv;
-  ui.tok0 = __ldg(a.cu_seqlens + ui.b);
-  ui.L = __ldg(a.cu_seqlens + ui.b + 1) - ui.tok0;
+  ui.tok0 = cu[ui.b];
+  ui.L = cu[ui.b + 1] - ui.tok0;
   ui.t0 = qt * UT;
   if (ui.t0 >= ui.L) return false;
   const int qend = min(ui.t0 + UT, ui.L);  // one past the last valid query
@@ -283,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<G, BN>;
   constexpr int TQ = C::TQ;
   constexpr int NSLOT = C::NSLOT;
+  static_assert(sizeof(Bars<NSLOT>) <= C::kBarBytes, "barrier block");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -320,11 +326,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
+  const bool cu_cached = a.batch + 1 <= kCuCache;
+  if (cu_cached)
+    for (int i = threadIdx.x; i <= a.batch; i += kThreads) bars->cu[i] = __ldg(a.cu_seqlens + i);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   uint8_t* ring = smem + C::kOffRing;
+  const int* cu = cu_cached ? bars->cu : a.cu_seqlens;
 
   if (warp < 4) {
     reg_dealloc<kRegsLow>();  // one instruction for all of warpgroup 0
@@ -345,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         UnitInfo ui;
-        if (!unit_info<G, BN, WIN>(u, a, nut, ui)) continue;
+        if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
         const int row0 = ui.tok0 + ui.kstart;
         // K_0 first (its slots free up while the previous unit finishes), then
         // the two Q tiles, then V_0, K_1, V_1, ...
@@ -446,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         UnitInfo ui;
-        if (!unit_info<G, BN, WIN>(u, a, nut, ui)) continue;
+        if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
         const uint32_t k0 = pos;
         pos += 3;
         if (!wait_slots(k0, 3)) break;
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             issue_pv(t, vp, j > 0);
-            umma_commit(&bars->pv_done[t]);
+            if (!more) umma_commit(&bars->pv_done[t]);  // the unit's O_t is complete
             if (t == 1) release_slots(vp, 2);
             if (more) {
               if (t == 0 && !wait_slots(kn, 3)) { ok = false; break; }
@@ -510,11 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float pm = 0.f, pl = 0.f, psink = 0.f;
     bool pvalid = false;
     long porow = 0;
-    uint32_t pblk = 0;
+    uint32_t puc = 0;  // index of the unit the epilogue finishes
 
     const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
     auto epilogue = [&]() -> bool {
-      if (!warp_wait(&bars->pv_done[t], (pblk - 1) & 1u, a.ctl, abort)) return false;
+      if (!warp_wait(&bars->pv_done[t], puc & 1u, a.ctl, abort)) return false;
       tc_fence_after();
       // fold in the sink: denominator 2^m l + 2^s, taken relative to max(m, s)
       const float mt = fmaxf(pm, psink);
@@ -561,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       UnitInfo ui;
-      if (!unit_info<G, BN, WIN>(u, a, nut, ui)) continue;
+      if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
       if (!warp_wait(&bars->q_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
       const int qmin = ui.t0 + t * TQ;           // first token of this tile
       const int qpos = qmin + tl;
@@ -632,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       psink = sink_l2;
       pvalid = qpos < ui.L;
       porow = long(ui.tok0 + qpos) * a.hq + h;
-      pblk = blk;
+      puc = uc;
       ++uc;
     }
     if (ok && have_prev) epilogue();
