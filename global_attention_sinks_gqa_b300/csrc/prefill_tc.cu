@@ -38,7 +38,8 @@
 //               by more than 2^8, with O rescaled then), P written back to
 //               TMEM as bf16 over the consumed S columns, and the epilogue,
 //               which folds in the sink: O 2^m / (2^m l + 2^s).
-// TMEM: S_A 0.., S_B 128.., O_A 256..383, O_B 384..511.
+// TMEM: S_A 0.., S_B 128.., O_A 256..383, O_B 384..511 (several key blocks
+// per unit), or S_A 0.., O_A 128..255, S_B 256.., O_B 384..511 (one block).
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -101,7 +102,9 @@ constexpr int kRegsLow = 152;
 constexpr int kRegsHigh = 176;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split");
 
-template <int G, int BN>
+// ONE: a unit's whole key band is one block of BN <= 256 keys (sliding
+// window units); otherwise blocks of BN <= 128 keys with an online softmax.
+template <int G, int BN, bool ONE>
 struct Cfg {
   static constexpr int TQ = 128 / G;                // tokens per tile
   static constexpr int UT = 2 * TQ;                 // tokens per unit (tiles A and B)
@@ -116,14 +119,23 @@ struct Cfg {
   static constexpr int kOffBar = kOffRing + NSLOT * kSlot;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "BN");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= (ONE ? 256 : 128), "BN");
   static_assert(kSlot % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-  static_assert(NSLOT >= 8, "ring must hold a K and a V block with room to prefetch");
+  static_assert(NSLOT >= (ONE ? 5 : 8), "ring must hold a K and a V block (and room to prefetch)");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
 
-__host__ __device__ constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
-__host__ __device__ constexpr uint32_t o_col(int t) { return t ? 384u : 256u; }
+// TMEM columns of tile t.  Blocks of <= 128 keys: S_A 0, S_B 128, O_A 256,
+// O_B 384.  One block of up to 256 keys: S_t at 256 t and O_t at 256 t + 128,
+// over the upper S columns, which are dead once the softmax has read them (P
+// takes the first BN / 2 columns); the next S_t is written only after the
+// epilogue has read O_t.
+template <bool ONE>
+__host__ __device__ constexpr uint32_t s_col(int t) { return ONE ? 256u * t : (t ? 128u : 0u); }
+template <bool ONE>
+__host__ __device__ constexpr uint32_t o_col(int t) {
+  return ONE ? 256u * t + 128u : (t ? 384u : 256u);
+}
 
 // cos / sin of RoPE frequency i for this lane's token, when the G lanes
 // sharing a token (lanes l with equal l / G) hold frequencies hl, hl + G, ...
@@ -269,6 +281,45 @@ __device__ __forceinline__ void softmax_block(uint32_t (&s)[BN], float scale_log
   }
 }
 
+// P = 2^(x * scale - msub) of n raw logits, written as bf16 pairs into the
+// TMEM columns starting at t_p; returns the sum of the fp32 weights.
+template <int N>
+__device__ __forceinline__ float exp_pack_store(const uint32_t (&s)[N], float scale_log2, float msub,
+                                                uint32_t t_p) {
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+  const uint64_t nm2 = f2_pack(-msub, -msub);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < N; c += 16) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const float2 x = f2_unpack(
+          f2_fma(f2_pack(__uint_as_float(s[c + e]), __uint_as_float(s[c + e + 1])), sc2, nm2));
+      const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+      pk[e >> 1] = pack_bf16x2(p0, p1);
+      if (e & 2)
+        acc1 = f2_add(acc1, f2_pack(p0, p1));
+      else
+        acc0 = f2_add(acc0, f2_pack(p0, p1));
+    }
+    tmem_st8(t_p + (c >> 1), pk);
+  }
+  const float2 sum = f2_unpack(f2_add(acc0, acc1));
+  return sum.x + sum.y;
+}
+
+template <int N>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[N]) {
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c + 3 < N; c += 4) {
+    mx0 = fmax3f(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    mx1 = fmax3f(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+  }
+  return fmaxf(mx0, mx1);
+}
+
 template <int BN>
 __device__ __forceinline__ void load_s_row(uint32_t t_s, uint32_t (&s)[BN]) {
   int c = 0;
@@ -281,11 +332,54 @@ __device__ __forceinline__ void load_s_row(uint32_t t_s, uint32_t (&s)[BN]) {
   for (int e = 0; e < BN; ++e) tmem_reg_fence(s[e]);
 }
 
-template <int G, int BN, bool WIN>
+// The whole key band of a unit as one block of BN columns, in two halves of
+// H1 and H2 columns (registers).  Half 1 sets the max m; half 2 is taken
+// against m unless its own max exceeds m by more than 2^8, in which case m
+// moves and half 1 is taken again (rare: the row's weights would otherwise
+// grow past 256 in bf16).  c_lo / c_hi: this row's visible columns;
+// lo_max / hi_min: the largest c_lo and smallest c_hi over the tile, which
+// decide which edges a half has to mask.  Returns m (log2 units, -inf if no
+// column is visible) and l = sum of 2^(x - m).
+template <int BN>
+__device__ __forceinline__ void softmax_one(uint32_t t_s, float scale_log2, int c_lo, int c_hi,
+                                            int lo_max, int hi_min, float& m, float& l) {
+  constexpr int H1 = ((BN / 2 + 15) / 16) * 16;
+  constexpr int H2 = BN - H1;
+  const bool lower1 = lo_max > 0, upper1 = hi_min < H1 - 1;
+  const bool lower2 = lo_max > H1, upper2 = hi_min < BN - 1;
+  float l1;
+  {
+    uint32_t s1[H1];
+    load_s_row<H1>(t_s, s1);
+    mask_block<H1>(s1, lower1, upper1, c_lo, c_hi);
+    m = row_max<H1>(s1) * scale_log2;
+    l1 = exp_pack_store<H1>(s1, scale_log2, m == -INFINITY ? 0.f : m, t_s);
+  }
+  bool redo;
+  float l2;
+  {
+    uint32_t s2[H2];
+    load_s_row<H2>(t_s + H1, s2);
+    mask_block<H2>(s2, lower2, upper2, c_lo - H1, c_hi - H1);
+    const float m2 = fmaxf(m, row_max<H2>(s2) * scale_log2);
+    redo = m2 > m + kRescaleThreshold;
+    if (redo) m = m2;
+    l2 = exp_pack_store<H2>(s2, scale_log2, m == -INFINITY ? 0.f : m, t_s + H1 / 2);
+  }
+  if (__any_sync(0xffffffffu, redo)) {
+    uint32_t s1[H1];
+    load_s_row<H1>(t_s, s1);
+    mask_block<H1>(s1, lower1, upper1, c_lo, c_hi);
+    l1 = exp_pack_store<H1>(s1, scale_log2, m == -INFINITY ? 0.f : m, t_s);
+  }
+  l = l1 + l2;
+}
+
+template <int G, int BN, bool WIN, bool ONE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapV, const PrefillArgs a) {
-  using C = Cfg<G, BN>;
+  using C = Cfg<G, BN, ONE>;
   constexpr int TQ = C::TQ;
   constexpr int NSLOT = C::NSLOT;
   static_assert(sizeof(Bars<NSLOT>) <= C::kBarBytes, "barrier block");
@@ -429,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 kdesc0 + uint64_t((ks2 * C::kSlot) >> 4)};
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk)
-          umma_ss(tmem + s_col(t), qd + uint64_t(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4),
+          umma_ss(tmem + s_col<ONE>(t), qd + uint64_t(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4),
                   kd[kk >> 2] + uint64_t(((kk & 3) * 32) >> 4), kk < 4 ? idesc_rot : idesc_s,
                   kk > 0 ? 1u : 0u);
       };
@@ -438,22 +532,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s1 = s0 + 1 == uint32_t(NSLOT) ? 0u : s0 + 1;
         const uint64_t vd0 = vdesc0 + uint64_t((s0 * C::kSlot) >> 4);
         const uint64_t vd1 = vdesc0 + uint64_t((s1 * C::kSlot) >> 4);
-        const uint32_t p_tmem = tmem + s_col(t);
+        const uint32_t p_tmem = tmem + s_col<ONE>(t);
         if (s1 == s0 + 1) {  // the two 64-dim halves of V are adjacent: one N=128 MMA per k-step
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tmem + o_col(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o,
+            umma_ts(tmem + o_col<ONE>(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o,
                     (acc || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            umma_ts(tmem + o_col(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o64,
+            umma_ts(tmem + o_col<ONE>(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o64,
                     (acc || kk > 0) ? 1u : 0u);
-            umma_ts(tmem + o_col(t) + 64, p_tmem + kk * 8, vd1 + uint64_t((kk * 2048) >> 4),
+            umma_ts(tmem + o_col<ONE>(t) + 64, p_tmem + kk * 8, vd1 + uint64_t((kk * 2048) >> 4),
                     idesc_o64, (acc || kk > 0) ? 1u : 0u);
           }
         }
       };
+      if constexpr (ONE) {
+        // one key block per unit: S_t = Q_t K^T once O_t (over S_t's upper
+        // columns) has been read by the previous unit's epilogue, then
+        // O_t = P_t V
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+          UnitInfo ui;
+          if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
+          const uint32_t k0 = pos;
+          pos += 3;
+          if (!wait_slots(k0, 3)) break;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!mbar_wait(&bars->q_ready[t], uc & 1u, a.ctl, abort) ||
+                (uc > 0 && !mbar_wait(&bars->o_free[t], (uc - 1) & 1u, a.ctl, abort))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(t, k0);
+            umma_commit(&bars->s_full[t]);
+            umma_commit(&bars->q_empty[t]);
+          }
+          if (!ok) break;
+          release_slots(k0, 3);
+          const uint32_t vp = pos;
+          pos += 2;
+          if (!wait_slots(vp, 2)) break;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!mbar_wait(&bars->p_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(t, vp, false);
+            umma_commit(&bars->pv_done[t]);
+          }
+          if (!ok) break;
+          release_slots(vp, 2);
+          ++uc;
+        }
+      } else
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         UnitInfo ui;
         if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
@@ -512,8 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hl = r % G;
     const int tl = r / G;
     const uint32_t lane_addr = uint32_t(quad * 32) << 16;
-    const uint32_t t_s = tmem + lane_addr + s_col(t);
-    const uint32_t t_o = tmem + lane_addr + o_col(t);
+    const uint32_t t_s = tmem + lane_addr + s_col<ONE>(t);
+    const uint32_t t_o = tmem + lane_addr + o_col<ONE>(t);
     uint32_t blk = 0, uc = 0;
     // the previous unit's row, finished after the next unit's Q is rotated
     bool have_prev = false;
@@ -619,6 +750,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY;  // running max (log2 units); the sink joins at the end
       float l = 0.f;
       const int qmax = qmin + TQ - 1;
+      if constexpr (ONE) {
+        if (!warp_wait(&bars->s_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
+        tc_fence_after();
+        const int kb = ui.kstart;  // position of column 0
+        softmax_one<BN>(t_s, a.scale_log2, qpos - a.window + 1 - kb, qpos - kb,
+                        qmax - a.window + 1 - kb, qmin - kb, m, l);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
+        ++blk;
+      } else
       for (int j = 0; j < ui.nblk; ++j, ++blk) {
         if (!warp_wait(&bars->s_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
         tc_fence_after();
@@ -651,19 +793,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg<G, BN>::kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-template <int G, int BN, bool WIN>
+template <int G, int BN, bool WIN, bool ONE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
-  using C = Cfg<G, BN>;
+  using C = Cfg<G, BN, ONE>;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, a.q, a.total, a.hq, kDqk, G, C::TQ) ||
       !make_map(&mk, a.k_rot, a.total, a.hkv, kDqk, 1, BN) ||
       !make_map(&mv, a.v, a.total, a.hkv, kDv, 1, BN))
     return cudaErrorInvalidValue;
-  auto kern = prefill_kernel<G, BN, WIN>;
+  auto kern = prefill_kernel<G, BN, WIN, ONE>;
   static bool attr_set = false;
   if (!attr_set) {
     // The register split inside the kernel needs the launch to allocate
@@ -684,13 +826,22 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Key block: 80 when a window unit's band (W - 1 + 2*TQ keys) fits two
-// blocks of 80, else 128.
+// Key blocks: a window unit whose band (W - 1 + 2*TQ keys) fits one block
+// of 144 (G = 16) or 160 (G = 8) keys runs as one block; other window units
+// use blocks of 80 when the band fits two of them, else 128; global units
+// use 128.
 template <int G>
 cudaError_t launch_g(const PrefillArgs& a, cudaStream_t s) {
-  if (a.window == 0) return launch_t<G, 128, false>(a, s);
-  if (a.window - 1 + 256 / G <= 160) return launch_t<G, 80, true>(a, s);
-  return launch_t<G, 128, true>(a, s);
+  const int band = a.window - 1 + 256 / G;
+  if (a.window == 0) return launch_t<G, 128, false, false>(a, s);
+  if constexpr (G == 16) {
+    if (band <= 144) return launch_t<G, 144, true, true>(a, s);
+  }
+  if constexpr (G == 8) {
+    if (band <= 160) return launch_t<G, 160, true, true>(a, s);
+  }
+  if (band <= 160) return launch_t<G, 80, true, false>(a, s);
+  return launch_t<G, 128, true, false>(a, s);
 }
 
 }  // namespace
