@@ -20,24 +20,24 @@
 // bound by streaming the cache, not by the multiply.
 //
 // CTA roles (192 threads):
-//   warp 0      TMA producer: per item the Q tile (3 boxes [G*T rows][64 dims])
-//               into one of two buffers, and blocks of 64 cache slots (K: 3
-//               boxes, V: 2 boxes of [64 slots][64 dims], 128-byte swizzle)
-//               into a 3-stage ring, running ahead across item boundaries.
+//   warp 0      TMA producer: blocks of 64 cache slots (K: 3 boxes, V: 2 boxes
+//               of [64 slots][64 dims], 128-byte swizzle) into a 5-stage ring,
+//               running ahead across item boundaries.
 //   warp 1      TMEM allocator and single-thread MMA issuer:
-//                 S_j = Q K_j^T (M=128, N=64, K=192) into one of two S buffers,
-//                 O  += P_j V_j (M=128, N=128, K=64, P from TMEM),
+//                 S_j = Q K_j^T (M=128, N=64, K=192; Q from TMEM) into one of
+//                 two S buffers, O += P_j V_j (M=128, N=128, K=64, P from TMEM),
 //               in the order QK_0, QK_1, PV_0, QK_2, PV_1, ... (the tensor core
 //               runs them in issue order, so S may be rewritten right behind
 //               the PV reading the P stored over it).
 //   warps 2-5   one thread per tile row (TMEM lane); warps whose 32 rows are
-//               all padding only keep the barriers: RoPE of the Q rows in
-//               shared memory, masked online softmax in base 2, P written back
-//               to TMEM as bf16, lazy O rescaling, and the epilogue.  A
-//               single-chunk item finishes its rows (sink included); otherwise
-//               it writes (O / l, m + log2 l) and a merge kernel combines the
-//               chunks and the sink with one warp per output row.
-// TMEM: S_0 columns 0..63, S_1 64..127, O 128..255.
+//               all padding only keep the barriers: the row's Q from global
+//               memory, RoPE in registers and into one of two TMEM Q buffers,
+//               masked online softmax in base 2, P written back to TMEM as
+//               bf16, lazy O rescaling, and the epilogue.  A single-chunk item
+//               finishes its rows (sink included); otherwise it writes
+//               (O / l, m + log2 l) and a merge kernel combines the chunks and
+//               the sink with one warp per output row.
+// TMEM: S_0 columns 0..63, S_1 64..127, O 128..255, Q buffers 256.. and 352..
 #include <math.h>
 
 #include "common.cuh"
@@ -50,19 +50,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past 256x growth
 constexpr int kBK = 64;                    // cache slots per block
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kBox = kBK * 128;            // [64 slots][64 dims] bf16
 constexpr int kStageBytes = 5 * kBox;      // K: 3 boxes, V: 2 boxes
-constexpr int kQBox = 128 * 128;           // [128 rows][64 dims], rows >= G*T zero
-constexpr int kQBytes = 3 * kQBox;
-constexpr int kOffQ = 0;
-constexpr int kOffStage = kOffQ + 2 * kQBytes;
+constexpr int kOffStage = 0;
 constexpr int kOffBar = kOffStage + kStages * kStageBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+// TMEM: S_0 0..63, S_1 64..127, O 128..255, Q buffers 256..351 and 352..447
+// (192 dims of a row as 96 packed pairs; rows >= G*T are padding).
+constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t s_col(uint32_t b) { return b ? 64u : 0u; }
 constexpr uint32_t kOCol = 128;
+__host__ __device__ constexpr uint32_t q_col(uint32_t qb) { return 256u + 96u * qb; }
 constexpr int kSingleChunkMax = 1024;  // ranges up to this many keys use one chunk
 constexpr int kChunkShort = 2048;      // keys per chunk for caches up to 16K keys
 constexpr int kChunkLong = 4096;       // and beyond
@@ -71,7 +71,7 @@ static_assert(kOffStage % 1024 == 0 && kBox % 1024 == 0, "swizzle atoms must be 
 
 struct Bars {
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_full[2], q_ready[2], q_empty[2];
+  uint64_t q_ready[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done, o_free, drain;
   uint32_t tmem_base;
   int abort;
@@ -173,7 +173,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_ready[i], 128);
       mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
@@ -186,10 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
   }
-  // padding rows of both Q tiles stay zero (TMA writes only the first G*T rows)
-  for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += kThreads)
-    reinterpret_cast<uint4*>(smem + kOffQ)[i] = make_uint4(0u, 0u, 0u, 0u);
-  fence_proxy_async_smem();
   if (threadIdx.x == 0) mbar_fence_init();
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&mapQ);
@@ -208,19 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t pos = 0, qf = 0;
+      uint32_t pos = 0;
       bool ok = true;
-      const uint32_t q_bytes = 3u * uint32_t(rows) * 128u;
       for (int v = blockIdx.x; v < nvirt && ok; v += gridDim.x) {
         Item it;
         if (item_info(v, a, it) != 1) continue;
-        const uint32_t qb = qf & 1u;
-        if (!mbar_wait(&bars->q_empty[qb], ((qf >> 1) & 1u) ^ 1u, a.ctl, abort)) break;
-        mbar_arrive_expect_tx(&bars->q_full[qb], q_bytes);
-        for (int i = 0; i < 3; ++i)
-          tma_load_3d(smem + kOffQ + qb * kQBytes + i * kQBox, &mapQ, &bars->q_full[qb], 64 * i,
-                      it.kvh * G, it.b * T);
-        ++qf;
         const int plane = it.b * a.hkv + it.kvh;
         const int nb = (it.s_end - it.s_beg + kBK - 1) / kBK;
         for (int blk = 0; blk < nb; ++blk, ++pos) {
@@ -239,10 +226,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // never leave with copies in flight into this CTA's shared memory
-      for (uint32_t i = 0; i < 2; ++i) {
-        const uint32_t fills = qf > i ? (qf - i + 1) / 2 : 0;
-        if (fills) mbar_wait_drain(&bars->q_full[i], (fills - 1) & 1u, a.ctl);
-      }
       for (uint32_t s = 0; s < uint32_t(kStages); ++s) {
         const uint32_t fills = pos > s ? (pos - s + kStages - 1) / kStages : 0;
         if (fills) mbar_wait_drain(&bars->full[s], (fills - 1) & 1u, a.ctl);
@@ -262,15 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = blk_global % kStages;
         if (!mbar_wait(&bars->full[st], (blk_global / kStages) & 1u, a.ctl, abort)) return false;
         tc_fence_after();
-        const uint32_t qbase = sbase + kOffQ + qb * kQBytes;
         const uint32_t kbase = sbase + kOffStage + st * kStageBytes;
         const uint32_t d = tmem + s_col(blk_global & 1u);
+        const uint64_t kdesc = make_sdesc_sw128(kbase, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          const uint64_t adesc = make_sdesc_sw128(qbase + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bdesc = make_sdesc_sw128(kbase + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-          umma_ss(d, adesc, bdesc, kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 12; ++kk)  // A = Q from TMEM (8 columns per k-step)
+          umma_ts(d, tmem + q_col(qb) + kk * 8,
+                  kdesc + uint64_t(((kk >> 2) * kBox + (kk & 3) * 32) >> 4),
+                  kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full[blk_global & 1u]);
         return true;
       };
@@ -400,48 +382,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (st_item < 0 && warp == 2 && lane == 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
         continue;
       }
+      // ---- Q: this row from global memory, RoPE on dims 0..63 in registers
+      // (pairs (i, i + 32); the G lanes holding one token's heads each
+      // evaluate 32/G of the 32 angles and exchange them by shuffles), into
+      // TMEM Q buffer qb once the item that used it last has issued its
+      // final QK^T
       const uint32_t qb = qc & 1u;
-      if (!warp_wait(&bars->q_full[qb], (qc >> 1) & 1u, a.ctl, abort)) { ok = false; break; }
+      if (!warp_wait(&bars->q_empty[qb], ((qc >> 1) & 1u) ^ 1u, a.ctl, abort)) { ok = false; break; }
       ++qc;
       const int p = it.L - T + t;  // this row's query position
       if (active) {
-        // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
-        // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
-        // The G lanes holding one token's heads each evaluate 32/G of the 32
-        // angles and exchange them by shuffles.
         float2 cs_own[32 / G];
 #pragma unroll
         for (int k2 = 0; k2 < 32 / G; ++k2)
           cs_own[k2] = rope_cos_sin(p, a.freqs.hi[hh + G * k2], a.freqs.lo[hh + G * k2]);
-        uint8_t* qrow = smem + kOffQ + qb * kQBytes + r * 128;
-        uint4 ch[8];
+        uint32_t qw[96];
+        const uint4* qsrc = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(a.q) +
+            ((long(it.b) * T + t) * a.hq + it.kvh * G + hh) * kDqk);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) ch[c] = *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t* x = reinterpret_cast<uint32_t*>(&ch[c]);
-          uint32_t* y = reinterpret_cast<uint32_t*>(&ch[c + 4]);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int i = 8 * c + 2 * w;
-            const float2 xv = unpack_bf16x2(x[w]);
-            const float2 yv = unpack_bf16x2(y[w]);
-            const float2 c0 = shared_cos_sin<G>(cs_own, i, lane);
-            const float2 c1 = shared_cos_sin<G>(cs_own, i + 1, lane);
-            const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
-            const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
-            if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
-              record_status(a.ctl, HATTN_ERR_INVALID_ARG);
-            x[w] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
-            y[w] = pack_f16x2(b0, b1);
-          }
+        for (int c = 0; c < 24; ++c) {
+          const uint4 v = real ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+          qw[4 * c] = v.x;
+          qw[4 * c + 1] = v.y;
+          qw[4 * c + 2] = v.z;
+          qw[4 * c + 3] = v.w;
         }
-        if (real) {
+        uint32_t big = 0u;  // |rotated| of every pair, as fp16 (inf once out of range)
 #pragma unroll
-          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
+        for (int w = 0; w < 16; ++w) {  // word w holds dims 2w, 2w+1; word w + 16 dims + 32
+          const int i = 2 * w;
+          const float2 xv = unpack_bf16x2(qw[w]);
+          const float2 yv = unpack_bf16x2(qw[w + 16]);
+          const float2 c0 = shared_cos_sin<G>(cs_own, i, lane);
+          const float2 c1 = shared_cos_sin<G>(cs_own, i + 1, lane);
+          const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
+          const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
+          qw[w] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
+          qw[w + 16] = pack_f16x2(b0, b1);
+          big = f16x2_absmax3(big, qw[w], qw[w + 16]);
         }
-        fence_proxy_async_smem();
+        if (real && f16x2_any_inf(big)) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+        const uint32_t t_q = tmem + lane_addr + q_col(qb);
+        tmem_st32(t_q, qw);
+        tmem_st32(t_q + 32, qw + 32);
+        tmem_st32(t_q + 64, qw + 64);
+        tmem_st_wait();
       }
+      tc_fence_before();
       mbar_arrive(&bars->q_ready[qb]);
       if (have_prev && !epilogue()) { ok = false; break; }
       float m = -INFINITY, l = 0.f;
