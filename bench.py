@@ -147,6 +147,16 @@ def measured_peaks():
         return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def step_config(world: int = 1):
+    return {"workload": "swa_prefill_32k + ga_prefill_32k + decode_b64_t4 (swa ring 131 "
+                        "+ ga 8K-64K)",
+            "swa_prefill": "seq 32768, 64q/8kv, W=128, d_qk 192, d_v 128, rope 64 @1e4",
+            "ga_prefill": "seq 32768, 64q/4kv, global, rope 64 @5e6",
+            "decode": "batch 64 x 4 verify tokens; swa 8kv ring 131; ga 4kv L~U[8192,65536]",
+            "l2": "inputs larger than L2 (no flush needed)",
+            "parallelism": f"replicas x{world}"}
+
+
 # --------------------------------------------------------------------- CUDA arm
 class Workload:
     """Device-resident inputs and outputs of one step, plus pinned host copies
@@ -325,13 +335,7 @@ def run_cuda(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks)",
-        "config": {"workload": "swa_prefill_32k + ga_prefill_32k + decode_b64_t4 (swa ring 131 "
-                               "+ ga 8K-64K)",
-                   "swa_prefill": "seq 32768, 64q/8kv, W=128, d_qk 192, d_v 128, rope 64 @1e4",
-                   "ga_prefill": "seq 32768, 64q/4kv, global, rope 64 @5e6",
-                   "decode": "batch 64 x 4 verify tokens; swa 8kv ring 131; ga 4kv L~U[8192,65536]",
-                   "l2": "inputs larger than L2 (no flush needed)",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(world),
         "parts": parts,
         "roofline": {"bound": "tensor", "kernel": "prefill GA (hattn_prefill window=0)",
                      "achieved": round(ga["flops"] / ga_s / 1e12, 2),
@@ -398,45 +402,54 @@ def run_e2e(wl, args, stream, sptr):
 
 
 # --------------------------------------------------------------------- CPU oracle arm
+_CPU_CASES = {}
+
+
+def _cpu_case(name):
+    """The seeded host copy of a prefill workload (built once per process)."""
+    if name not in _CPU_CASES:
+        c = synth.CONFIGS[name]
+        _CPU_CASES[name] = synth.prefill_case(c["seqlens"], c["hq"], c["hkv"], window=c["window"],
+                                              rope_base=c["rope_base"], seed=c["seed"])
+    return _CPU_CASES[name]
+
+
 def cpu_baseline(budget_s: float = 20.0):
     """The fp64 oracle as it stands, timed on this host's cores on a bounded row
-    sample of the same step; reported as algorithmic TFLOP/s of the sample."""
+    sample of the same step (about budget_s seconds of CPU work: a third on
+    sliding-window rows, the rest on global rows); reported as algorithmic
+    TFLOP/s of the sample."""
     import oracle
     cf = synth.CONFIGS
     done_flops, secs = 0.0, 0.0
     samples = []
-    # SWA prefill rows (32K, 64/8): rows are independent; sample evenly spaced rows
+    # SWA prefill rows (32K, 64/8): rows are independent; evenly spaced batches
     c = cf["swa_prefill_32k"]
-    pc = synth.prefill_case(c["seqlens"], c["hq"], c["hkv"], window=c["window"],
-                            rope_base=c["rope_base"], seed=c["seed"])
+    pc = _cpu_case("swa_prefill_32k")
     S = pc.total
-    rows = np.linspace(0, S - 1, 256).astype(np.int64)
-    t0 = time.perf_counter()
-    oracle.prefill(pc.q, pc.k, pc.v, pc.sink, [0, S], window=c["window"],
-                   rope_base=c["rope_base"], scale=pc.scale, rows=rows)
-    dt = time.perf_counter() - t0
-    f = sum(PAIR_FLOPS * pc.hq * min(int(r) + 1, c["window"]) for r in rows)
-    done_flops += f
-    secs += dt
-    samples.append(f"swa_prefill_32k: {len(rows)} of {S} rows")
-    del pc
-    # GA prefill rows (32K, 64/4): a few rows spread over the sequence
+    n_rows, t0 = 0, time.perf_counter()
+    rs = np.random.RandomState(0)
+    while time.perf_counter() - t0 < budget_s / 3 and n_rows < S:
+        rows = np.sort(rs.choice(S, size=512, replace=False))
+        oracle.prefill(pc.q, pc.k, pc.v, pc.sink, [0, S], window=c["window"],
+                       rope_base=c["rope_base"], scale=pc.scale, rows=rows)
+        done_flops += sum(PAIR_FLOPS * pc.hq * min(int(r) + 1, c["window"]) for r in rows)
+        n_rows += len(rows)
+    secs += time.perf_counter() - t0
+    samples.append(f"swa_prefill_32k: {n_rows} of {S} rows")
+    # GA prefill rows (32K, 64/4): rows spread over the sequence until the budget is spent
     c = cf["ga_prefill_32k"]
-    pc = synth.prefill_case(c["seqlens"], c["hq"], c["hkv"], window=0, rope_base=c["rope_base"],
-                            seed=c["seed"])
-    rows = np.array([1023, 8191, 16383, 24575, 32767])
-    remaining = max(2.0, budget_s - secs)
-    n_ok = 0
-    t0 = time.perf_counter()
-    for r in rows:
+    pc = _cpu_case("ga_prefill_32k")
+    order = rs.permutation(S)
+    n_ok, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s - secs and n_ok < S:
+        r = int(order[n_ok])
         oracle.prefill(pc.q, pc.k, pc.v, pc.sink, [0, S], window=0, rope_base=c["rope_base"],
                        scale=pc.scale, rows=[r])
+        done_flops += PAIR_FLOPS * pc.hq * (r + 1)
         n_ok += 1
-        done_flops += PAIR_FLOPS * pc.hq * (int(r) + 1)
-        if time.perf_counter() - t0 > remaining:
-            break
     secs += time.perf_counter() - t0
-    samples.append(f"ga_prefill_32k: {n_ok} rows at positions {rows[:n_ok].tolist()}")
+    samples.append(f"ga_prefill_32k: {n_ok} random rows of {S}")
     return {"value": round(done_flops / secs / 1e12, 6), "unit": "TFLOP/s",
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "; ".join(samples) + f"; {secs:.1f} s of fp64 CPU work"}
@@ -446,12 +459,14 @@ def run_reference(args):
     """--impl reference: the CPU oracle as the reference arm, K bounded steps."""
     import oracle
     steps_ms = []
+    # each step a bounded sample: the whole run stays within a few minutes
+    budget = max(2.0, min(args.cpu_budget, 120.0 / max(1, args.steps)))
     for _ in range(args.warmup):
-        cpu_baseline(budget_s=2.0)
+        cpu_baseline(budget_s=1.0)
     vals = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        cb = cpu_baseline(budget_s=args.cpu_budget)
+        cb = cpu_baseline(budget_s=budget)
         steps_ms.append((time.perf_counter() - t0) * 1e3)
         vals.append(cb["value"])
     v = statistics.mean(vals)
@@ -460,8 +475,7 @@ def run_reference(args):
             "ms_per_step": round(statistics.mean(steps_ms), 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1))",
-            "config": {"workload": "swa_prefill_32k + ga_prefill_32k (row samples)",
-                       "parallelism": "host cores"},
+            "config": step_config(1),
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": cb["sample"]},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -482,6 +496,84 @@ def max_over_ranks(x, world):
     t = torch.tensor([x], dtype=torch.float64, device="cuda")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def run_hybrid_block(args):
+    """Config 5: one hybrid block at seq 262144 -- 5 sliding-window layers (64q/8kv,
+    W=128, base 1e4) then 1 global layer (64q/4kv, base 5e6), fresh N(0,1) inputs
+    per layer, all resident in HBM; one step = the 6 layer calls."""
+    import global_attention_sinks_gqa_b300 as ha
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg = synth.CONFIGS["hybrid_block_256k"]
+    S = cfg["seqlens"][0]
+    layers = []
+    for li in range(cfg["n_swa"] + 1):
+        kind = "swa" if li < cfg["n_swa"] else "ga"
+        p = cfg[kind]
+        c = synth.prefill_case([S], p["hq"], p["hkv"], window=p["window"],
+                               rope_base=p["rope_base"], seed=cfg["seed"] * 100 + li, device=dev)
+        layers.append(dict(kind=kind, case=c,
+                           out=torch.empty((S, c.hq, D_V), dtype=torch.bfloat16, device=dev),
+                           lse=torch.empty((S, c.hq), dtype=torch.float32, device=dev),
+                           ws=torch.empty(ha.hattn_prefill_workspace_size(S, c.hkv, D_QK),
+                                          dtype=torch.uint8, device=dev),
+                           flops=prefill_flops(S, c.hq, c.window),
+                           bytes=prefill_bytes(S, c.hq, c.hkv)))
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def step(ev=None):
+        for i, lay in enumerate(layers):
+            c = lay["case"]
+            if ev is not None:
+                ev[i][0].record(stream)
+            st = ha.hattn_prefill(c.q, c.k, c.v, c.sink, lay["out"], lay["lse"], 1, c.cu_seqlens,
+                                  S, S, c.hq, c.hkv, D_QK, D_V, R, c.rope_base, c.window,
+                                  c.scale, lay["ws"], lay["ws"].numel(), sptr)
+            assert st == 0, ha.status_string(st)
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in layers] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for k in range(args.steps):
+            step(ev[k])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    ha.check_device_status()
+    ms = start.elapsed_time(stop) / args.steps
+    hbm, tf_burst, tf_sust, src = measured_peaks()
+    flops = sum(l["flops"] for l in layers)
+    byts = sum(l["bytes"] for l in layers)
+    parts = {}
+    for i, lay in enumerate(layers):
+        t = statistics.mean(e[i][0].elapsed_time(e[i][1]) for e in ev) / 1e3
+        bf = lay["flops"] / (tf_sust * 1e12)
+        bb = lay["bytes"] / (hbm * 1e9)
+        parts[f"layer{i}_{lay['kind']}"] = dict(ms=t * 1e3, tflops=lay["flops"] / t / 1e12,
+                                                 gbs=lay["bytes"] / t / 1e9,
+                                                 roofline_frac=max(bf, bb) / t)
+    frac = sum(max(l["flops"] / (tf_sust * 1e12), l["bytes"] / (hbm * 1e9)) for l in layers)
+    return {"metric": METRIC, "value": round(flops / (ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks)",
+            "config": {"workload": "hybrid_block_256k: seq 262144, 5 SWA layers (64q/8kv, W=128, "
+                                   "base 1e4) + 1 GA layer (64q/4kv, base 5e6)",
+                       "l2": "inputs larger than L2 (no flush needed)"},
+            "block_roofline_frac": round(frac / (ms / 1e3), 4),
+            "algorithmic": {"flops": flops, "bytes": byts},
+            "parts": parts, "clocks": clk.summary()}
 
 
 def run_profile_case(args):
@@ -547,9 +639,14 @@ def main():
                     help="swa_prefill | ga_prefill | decode_swa | decode_ga: one call, for ncu")
     ap.add_argument("--seq", type=int, default=0, help="prefill length for --profile-case")
     ap.add_argument("--batch", type=int, default=0, help="decode batch for --profile-case")
+    ap.add_argument("--workload", default="step", choices=["step", "hybrid_block_256k"],
+                    help="step: the default bench step; hybrid_block_256k: config 5 alone")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
+        return
+    if args.workload == "hybrid_block_256k":
+        print(json.dumps(run_hybrid_block(args)))
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
