@@ -964,6 +964,338 @@ cudaError_t launch_ring(const DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Rings of at most 144 slots with at most 32 query rows (the window layer at
+// W = 128, T <= 4, G <= 8) on the tensor cores.  One CTA per (sequence, KV
+// head), two warps, two CTAs per SM:
+//   warp 1   TMEM allocator; lane 0 loads the item with one TMA round (Q: 3
+//            boxes of [G*T rows][64 dims]; the ring: K 3 boxes, V 2 boxes of
+//            [cap slots][64 dims]) and issues S = Q K^T (M=128, N = cap
+//            rounded up to 16, K=192) and O = P V (K = N).  Tile rows past
+//            G*T read whatever follows the Q tile in shared memory: their S,
+//            P and O rows are never used.
+//   warp 0   one thread per query row: RoPE of its Q row in shared memory,
+//            the masked softmax over the whole ring in one pass (a row sees
+//            a cyclic interval of slots), P to TMEM, and the epilogue with
+//            the sink.
+// TMEM: S columns 0..N-1, O 128..255 over S's upper columns (dead once the
+// softmax has read them).
+// ---------------------------------------------------------------------------
+constexpr int kRingTcMaxCap = 144;
+constexpr int kRingTcCols = 144;                // S columns the softmax reads
+constexpr int kRingTcQBox = 32 * 128;           // [32 rows][64 dims]
+constexpr int kRingTcOffK = 3 * kRingTcQBox;
+__host__ __device__ constexpr int ring_tc_rows(int cap) { return (cap + 15) & ~15; }
+__host__ __device__ constexpr int ring_tc_bar_offset(int cap) {
+  return kRingTcOffK + 5 * ring_tc_rows(cap) * 128;
+}
+__host__ __device__ constexpr int ring_tc_smem(int cap) {
+  return ring_tc_bar_offset(cap) + 128 + 1024;  // + barriers + alignment slack
+}
+
+struct RingTcBars {
+  uint64_t full, q_ready, s_full, p_full, pv_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Masked base-2 weights of n columns of one row, written as bf16 pairs at
+// t_p; the row sees the columns c < cap with (c - s_lo) mod cap < nvis.
+template <int N>
+__device__ __forceinline__ void ring_mask(uint32_t (&s)[N], int c0, int s_lo, int nvis, int cap) {
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    const int c = c0 + e;
+    int d = c - s_lo;
+    d += d < 0 ? cap : 0;
+    if (!(d < nvis && c < cap)) s[e] = __float_as_uint(-INFINITY);
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(64)
+    decode_ring_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
+                          const __grid_constant__ CUtensorMap mapK,
+                          const __grid_constant__ CUtensorMap mapV, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, rows = G * T;
+  const int b = blockIdx.x / a.hkv, kvh = blockIdx.x - b * a.hkv;
+  const int RR = ring_tc_rows(a.cap);
+  const int kbox = RR * 128;
+  uint8_t* ks = smem + kRingTcOffK;
+  uint8_t* vs = ks + 3 * kbox;
+  RingTcBars* bars = reinterpret_cast<RingTcBars*>(smem + ring_tc_bar_offset(a.cap));
+  volatile int* abort = &bars->abort;
+  const int L = __ldg(a.seqlens + b);
+  if (!length_ok(L, a)) {
+    if (threadIdx.x == 0 && kvh == 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+    return;
+  }
+  if (threadIdx.x == 32) {
+    mbar_init(&bars->full, 1);
+    mbar_init(&bars->q_ready, 32);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_full, 32);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 256);
+    tmem_relinquish();
+  }
+  // V rows past cap are read by the last PV k-step: make them zero
+  for (int e = threadIdx.x; e < (RR - a.cap) * 16; e += 64) {
+    const int rr = a.cap + (e >> 4), c16 = e & 15;
+    *reinterpret_cast<uint4*>(vs + (c16 >> 3) * kbox + rr * 128 + (c16 & 7) * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  if (threadIdx.x == 32) {
+    tma_prefetch_map(&mapQ);
+    tma_prefetch_map(&mapK);
+    tma_prefetch_map(&mapV);
+    mbar_arrive_expect_tx(&bars->full, uint32_t(3 * rows * 128 + 5 * a.cap * 128));
+    const int plane = b * a.hkv + kvh;
+    for (int i = 0; i < 3; ++i)
+      tma_load_3d(smem + i * kRingTcQBox, &mapQ, &bars->full, 64 * i, kvh * G, b * T);
+    for (int i = 0; i < 3; ++i) tma_load_3d(ks + i * kbox, &mapK, &bars->full, 64 * i, 0, plane);
+    for (int i = 0; i < 2; ++i)
+      tma_load_3d(vs + i * kbox, &mapV, &bars->full, 64 * i, 0, plane);
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ rows
+    const int r = lane;
+    const bool real = r < rows;
+    const int t = real ? r / G : 0, hh = r % G;
+    const int p = L - T + t;  // this row's query position
+    bool ok = warp_wait(&bars->full, 0, a.ctl, abort);
+    if (ok) {
+      const int nslots = min(L, a.cap);  // slots written so far
+      for (int e = lane; e < (a.cap - nslots) * 16; e += 32) {  // never written: zero V
+        const int rr = nslots + (e >> 4), c16 = e & 15;
+        *reinterpret_cast<uint4*>(vs + (c16 >> 3) * kbox + rr * 128 + (c16 & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      // RoPE of this row's dims 0..63 (box 0, 128-byte rows, 16-byte chunks
+      // swizzled by row % 8); the G lanes of one token share its 32 angles
+      float2 cs_own[32 / G];
+#pragma unroll
+      for (int k2 = 0; k2 < 32 / G; ++k2)
+        cs_own[k2] = rope_cos_sin(p, a.freqs.hi[hh + G * k2], a.freqs.lo[hh + G * k2]);
+      uint8_t* qrow = smem + r * 128;
+      uint4 ch[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ch[c] = *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
+      uint32_t big = 0u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t* x = reinterpret_cast<uint32_t*>(&ch[c]);
+        uint32_t* y = reinterpret_cast<uint32_t*>(&ch[c + 4]);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int i = 8 * c + 2 * w;
+          const float2 xv = unpack_bf16x2(x[w]);
+          const float2 yv = unpack_bf16x2(y[w]);
+          const float2 c0 = shared_cos_sin<G>(cs_own, i, lane);
+          const float2 c1 = shared_cos_sin<G>(cs_own, i + 1, lane);
+          const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
+          const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
+          x[w] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
+          y[w] = pack_f16x2(b0, b1);
+          big = f16x2_absmax3(big, x[w], y[w]);
+        }
+      }
+      if (real) {
+        if (f16x2_any_inf(big)) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->q_ready);
+      ok = warp_wait(&bars->s_full, 0, a.ctl, abort);
+    } else {
+      mbar_wait_drain(&bars->full, 0, a.ctl);  // never leave with copies in flight
+    }
+    float m = -INFINITY, l = 0.f;
+    if (ok) {
+      tc_fence_after();
+      // visible positions [lo, p] sit in the cyclic slot interval starting at
+      // lo mod cap (a ring holds the last cap >= W + T - 1 positions)
+      const int lo = max(p - a.window + 1, 0);
+      const int nvis = real ? p - lo + 1 : 0;
+      const int s_lo = lo % a.cap;
+      const uint32_t t_s = tmem + (uint32_t(0) << 16);
+      constexpr int H1 = 80, H2 = kRingTcCols - H1;
+      float l1;
+      {
+        uint32_t s1[H1];
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) tmem_ld32_nowait(t_s + c, s1 + c);
+        tmem_ld16_nowait(t_s + 64, s1 + 64);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < H1; ++e) tmem_reg_fence(s1[e]);
+        ring_mask<H1>(s1, 0, s_lo, nvis, a.cap);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < H1; e += 2) mx = fmax3f(mx, __uint_as_float(s1[e]), __uint_as_float(s1[e + 1]));
+        m = mx * a.scale_log2;
+        uint32_t s2[H2];
+#pragma unroll
+        for (int c = 0; c < H2; c += 32) tmem_ld32_nowait(t_s + H1 + c, s2 + c);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < H2; ++e) tmem_reg_fence(s2[e]);
+        ring_mask<H2>(s2, H1, s_lo, nvis, a.cap);
+        float mx2 = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < H2; e += 2) mx2 = fmax3f(mx2, __uint_as_float(s2[e]), __uint_as_float(s2[e + 1]));
+        m = fmaxf(m, mx2 * a.scale_log2);  // exact max over the whole ring
+        const float msub = m == -INFINITY ? 0.f : m;
+        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+        const uint64_t nm2 = f2_pack(-msub, -msub);
+        uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < H1; c += 16) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float2 x = f2_unpack(
+                f2_fma(f2_pack(__uint_as_float(s1[c + e]), __uint_as_float(s1[c + e + 1])), sc2, nm2));
+            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+            acc = f2_add(acc, f2_pack(p0, p1));
+          }
+          tmem_st8(t_s + (c >> 1), pk);
+        }
+#pragma unroll
+        for (int c = 0; c < H2; c += 16) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float2 x = f2_unpack(
+                f2_fma(f2_pack(__uint_as_float(s2[c + e]), __uint_as_float(s2[c + e + 1])), sc2, nm2));
+            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+            acc = f2_add(acc, f2_pack(p0, p1));
+          }
+          tmem_st8(t_s + ((H1 + c) >> 1), pk);
+        }
+        const float2 sum = f2_unpack(acc);
+        l1 = sum.x + sum.y;
+      }
+      l = l1;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+      ok = warp_wait(&bars->pv_done, 0, a.ctl, abort);
+    }
+    if (ok) {
+      // ---- epilogue: add the sink, finish the row
+      tc_fence_after();
+      const int h = kvh * G + hh;
+      const float sl2 = __ldg(a.sink + h) * kLog2e;
+      const float mt_ = fmaxf(m, sl2);
+      const float msub = mt_ == -INFINITY ? 0.f : mt_;
+      const float fo = fast_exp2(m - msub);
+      const float sw = fast_exp2(sl2 - msub);
+      const float sc = fo / (l * fo + sw);
+      const uint64_t sc2 = f2_pack(sc, sc);
+      const long orow = (long(b) * T + t) * a.hq + h;
+      uint8_t* op = static_cast<uint8_t*>(a.out) + orow * 256;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[64];
+        tmem_ld32_nowait(tmem + 128 + half * 64, v);
+        tmem_ld32_nowait(tmem + 128 + half * 64 + 32, v + 32);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 64; ++e) tmem_reg_fence(v[e]);
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float2 y = f2_unpack(
+              f2_mul(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2));
+          pk[e] = pack_bf16x2(y.x, y.y);
+        }
+        if (real) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            reinterpret_cast<uint4*>(op + half * 128)[e] =
+                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      if (real && a.lse) a.lse[orow] = (msub + log2f(l * fo + sw)) * kLn2;
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t idesc_rot = make_idesc_f16(128, RR, 0, 0);
+    const uint32_t idesc_s = make_idesc_bf16(128, RR, 0, 0);
+    constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, 0, 1);
+    if (mbar_wait(&bars->q_ready, 0, a.ctl, abort)) {
+      tc_fence_after();
+      const uint64_t qd = make_sdesc_sw128(sbase, 16, 1024);
+      const uint64_t kd = make_sdesc_sw128(sbase + kRingTcOffK, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 12; ++kk)
+        umma_ss(tmem, qd + uint64_t(((kk >> 2) * kRingTcQBox + (kk & 3) * 32) >> 4),
+                kd + uint64_t(((kk >> 2) * kbox + (kk & 3) * 32) >> 4),
+                kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
+      umma_commit(&bars->s_full);
+      if (mbar_wait(&bars->p_full, 0, a.ctl, abort)) {
+        tc_fence_after();
+        const uint64_t vd = make_sdesc_sw128(sbase + kRingTcOffK + 3 * kbox, kbox, 1024);
+        for (int kk = 0; kk < RR / 16; ++kk)
+          umma_ts(tmem + 128, tmem + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_o,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(&bars->pv_done);
+      }
+    }
+    // every MMA issued must be complete before TMEM is released
+    umma_commit(&bars->drain);
+    mbar_wait_drain(&bars->drain, 0, a.ctl);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+template <int G>
+cudaError_t launch_ring_tc(const DecodeArgs& a, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_ring_tc_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         ring_tc_smem(kRingTcMaxCap));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, long(a.B) * a.T, a.hq, kDqk, G, a.T) ||
+      !make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, a.cap, 1) ||
+      !make_map(&mv, a.v_cache, long(a.B) * a.hkv, a.cap, kDv, a.cap, 1))
+    return cudaErrorInvalidValue;
+  // the full-size footprint for every ring keeps two CTAs on an SM, which is
+  // what their 2 x 256 TMEM columns allow
+  decode_ring_tc_kernel<G>
+      <<<unsigned(long(a.B) * a.hkv), 64, ring_tc_smem(kRingTcMaxCap), s>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {
   const int G = a.hq / a.hkv;
   auto kern = G == 1 ? decode_kernel<1> : G == 2 ? decode_kernel<2> : G == 4 ? decode_kernel<4>
@@ -1018,9 +1350,20 @@ size_t decode_workspace_bytes(int B, int T, int hq, int nsplit) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  const int G = a.hq / a.hkv;
+  // a ring of <= 144 slots with <= 32 query rows: tensor cores, one CTA per item
+  if (a.is_ring && a.cap <= kRingTcMaxCap && a.nsplit == 1 && G * a.T <= 32) {
+    switch (G) {
+      case 1: return launch_ring_tc<1>(a, s);
+      case 2: return launch_ring_tc<2>(a, s);
+      case 4: return launch_ring_tc<4>(a, s);
+      case 8: return launch_ring_tc<8>(a, s);
+      default: break;
+    }
+  }
   // a ring small enough to sit in shared memory whole: one CTA per item
   if (a.is_ring && a.cap <= kRingMaxCap && a.nsplit == 1) {
-    const int rows = (a.hq / a.hkv) * a.T;
+    const int rows = G * a.T;
     if (rows <= 16) return launch_ring<1>(a, s);
     if (rows <= 32) return launch_ring<2>(a, s);
     return launch_ring<4>(a, s);
