@@ -966,54 +966,125 @@ cudaError_t launch_ring(const DecodeArgs& a, cudaStream_t s) {
 
 // ---------------------------------------------------------------------------
 // Rings of at most 144 slots with at most 32 query rows (the window layer at
-// W = 128, T <= 4, G <= 8) on the tensor cores.  One CTA per (sequence, KV
-// head), two warps, two CTAs per SM:
-//   warp 1   TMEM allocator; lane 0 loads the item with one TMA round (Q: 3
-//            boxes of [G*T rows][64 dims]; the ring: K 3 boxes, V 2 boxes of
-//            [cap slots][64 dims]) and issues S = Q K^T (M=128, N = cap
-//            rounded up to 16, K=192) and O = P V (K = N).  Tile rows past
-//            G*T read whatever follows the Q tile in shared memory: their S,
-//            P and O rows are never used.
-//   warp 0   one thread per query row: RoPE of its Q row in shared memory,
-//            the masked softmax over the whole ring in one pass (a row sees
-//            a cyclic interval of slots), P to TMEM, and the epilogue with
-//            the sink.
-// TMEM: S columns 0..N-1, O 128..255 over S's upper columns (dead once the
-// softmax has read them).
+// W = 128, T <= 4, G <= 8) on the tensor cores.  Persistent: one CTA per SM
+// walks the items (sequence, KV head) v = blockIdx.x + i * gridDim.x.  Two
+// workers take alternate items, each with its own shared-memory buffer (Q,
+// the ring's K and V), its own half of TMEM and its own TMEM lane quadrant,
+// so that one item's loads, MMAs and softmax overlap the other's.
+//   warp 2   TMEM allocator; lane 0 loads item i into buffer i % 2: Q (3
+//            boxes of [G*T rows][64 dims]) with K (3 boxes of [cap slots][64
+//            dims]) on one barrier, V (2 boxes) on another, the Q/K loads of
+//            an item ahead of the V loads of the one before.  Q/K and V of a
+//            buffer are refilled as soon as the MMAs that read them are done.
+//   worker w = warps w and w + 4 (TMEM lane quadrant w, one lane per query
+//            row; the two warps split each row's work in halves): RoPE of the
+//            Q rows in shared memory; S = Q K^T (M=128, N = cap rounded up to
+//            16, K=192); the masked softmax over the whole ring in one pass (a
+//            row sees a cyclic interval of slots); P to TMEM; O = P V; the
+//            epilogue with the sink.  Lane 0 of warp w issues the MMAs.
+// Worker w's query rows are rows 32w.. of its MMA tile (the lanes its warps
+// read): its A descriptor starts 32w rows before the Q tile.  Other tile rows
+// read whatever shared memory lies there: their S, P and O rows are never
+// used.  TMEM of worker w: S at 256w + 0..143, O at 256w + 128..255 over S's
+// upper columns (dead once the softmax read them).
 // ---------------------------------------------------------------------------
 constexpr int kRingTcMaxCap = 144;
-constexpr int kRingTcCols = 144;                // S columns the softmax reads
-constexpr int kRingTcQBox = 32 * 128;           // [32 rows][64 dims]
+constexpr int kRingTcH0 = 80, kRingTcH1 = 64;    // S columns of the two halves
+constexpr int kRingTcQBox = 32 * 128;            // [32 rows][64 dims]
+constexpr int kRingTcKBox = kRingTcMaxCap * 128; // [144 slots][64 dims]
 constexpr int kRingTcOffK = 3 * kRingTcQBox;
+constexpr int kRingTcOffV = kRingTcOffK + 3 * kRingTcKBox;
+constexpr int kRingTcBuf = kRingTcOffV + 2 * kRingTcKBox;
+constexpr int kRingTcOffCs = 2 * kRingTcBuf;     // (cos, sin) of the item's tokens, per worker
+constexpr int kRingTcCsRow = 32 * 8 + 16;        // one token's 32 pairs (+16: no bank clash)
+constexpr int kRingTcOffRed = kRingTcOffCs + 2 * 4 * kRingTcCsRow;  // [worker][half][max|sum][32]
+constexpr int kRingTcOffBar = kRingTcOffRed + 2 * 2 * 2 * 32 * 4;
+constexpr int kRingTcSmem = kRingTcOffBar + 256 + 1024;  // + barriers + alignment slack
+constexpr int kRingTcThreads = 192;
+static_assert(kRingTcBuf % 1024 == 0 && kRingTcKBox % 1024 == 0, "swizzle atoms");
+static_assert(kRingTcSmem <= 232448, "shared memory");
+static_assert(kRingTcH0 + kRingTcH1 == kRingTcMaxCap, "halves cover the ring");
 __host__ __device__ constexpr int ring_tc_rows(int cap) { return (cap + 15) & ~15; }
-__host__ __device__ constexpr int ring_tc_bar_offset(int cap) {
-  return kRingTcOffK + 5 * ring_tc_rows(cap) * 128;
-}
-__host__ __device__ constexpr int ring_tc_smem(int cap) {
-  return ring_tc_bar_offset(cap) + 128 + 1024;  // + barriers + alignment slack
-}
 
 struct RingTcBars {
-  uint64_t full, q_ready, s_full, p_full, pv_done, drain;
+  uint64_t qk_full[2], v_full[2], qk_empty[2], v_empty[2], s_full[2], pv_done[2], drain[2];
+  uint64_t pair[2];  // the two warps of a worker meet here (one arrival per warp)
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(RingTcBars) <= 256, "barrier block");
 
-// Masked base-2 weights of n columns of one row, written as bf16 pairs at
-// t_p; the row sees the columns c < cap with (c - s_lo) mod cap < nvis.
-template <int N>
-__device__ __forceinline__ void ring_mask(uint32_t (&s)[N], int c0, int s_lo, int nvis, int cap) {
+// Bits [lo, hi) of the 32-bit word holding columns 32k..32k+31.
+__device__ __forceinline__ uint32_t ring_bits(int k, int lo, int hi) {
+  const int a = min(max(lo - 32 * k, 0), 32), b = min(max(hi - 32 * k, 0), 32);
+  const uint32_t below_b = b >= 32 ? 0xffffffffu : (1u << b) - 1u;
+  const uint32_t below_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
+  return below_b & ~below_a;
+}
+
+// Both warps of a worker: a bounded rendezvous on an mbarrier of count 2.
+__device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t& ph, int lane,
+                                          const DecodeArgs& a, volatile int* abort) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = warp_wait(bar, ph, a.ctl, abort);
+  ph ^= 1u;
+  return ok;
+}
+
+// One half of a row's softmax: N S columns C0.. from TMEM; invisible columns
+// (clear bit in vis[]) to -inf; returns their max (unscaled).
+template <int N, int C0>
+__device__ __forceinline__ float ring_load_max(uint32_t t_s, uint32_t (&s)[N],
+                                               const uint32_t (&vis)[5]) {
+#pragma unroll
+  for (int c = 0; c + 32 <= N; c += 32) tmem_ld32_nowait(t_s + C0 + c, s + c);
+  if constexpr (N % 32 == 16) tmem_ld16_nowait(t_s + C0 + N - 16, s + N - 16);
+  tmem_ld_wait();
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int e = 0; e < N; ++e) {
-    const int c = c0 + e;
-    int d = c - s_lo;
-    d += d < 0 ? cap : 0;
-    if (!(d < nvis && c < cap)) s[e] = __float_as_uint(-INFINITY);
+    tmem_reg_fence(s[e]);
+    const int c = C0 + e;
+    if (!(vis[c >> 5] & (1u << (c & 31)))) s[e] = __float_as_uint(-INFINITY);
   }
+#pragma unroll
+  for (int e = 0; e < N; e += 8) {
+    mx[(e >> 3) & 3] = fmax3f(mx[(e >> 3) & 3], __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+    mx[(e >> 3) & 3] = fmax3f(mx[(e >> 3) & 3], __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]));
+    mx[(e >> 3) & 3] = fmax3f(mx[(e >> 3) & 3], __uint_as_float(s[e + 4]), __uint_as_float(s[e + 5]));
+    mx[(e >> 3) & 3] = fmax3f(mx[(e >> 3) & 3], __uint_as_float(s[e + 6]), __uint_as_float(s[e + 7]));
+  }
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// exp2(s * scale - m) of N columns as bf16 pairs into TMEM at taddr (masked
+// columns hold -inf and give 0); returns the fp32 sum of the weights.
+template <int N>
+__device__ __forceinline__ float ring_exp_store(const uint32_t (&s)[N], uint32_t taddr,
+                                                float scale, float m) {
+  const uint64_t sc2 = f2_pack(scale, scale);
+  const uint64_t nm2 = f2_pack(-m, -m);
+  uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+  for (int c = 0; c < N; c += 16) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const float2 x = f2_unpack(
+          f2_fma(f2_pack(__uint_as_float(s[c + e]), __uint_as_float(s[c + e + 1])), sc2, nm2));
+      const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+      pk[e >> 1] = pack_bf16x2(p0, p1);
+      acc[(e >> 1) & 1] = f2_add(acc[(e >> 1) & 1], f2_pack(p0, p1));
+    }
+    tmem_st8(taddr + (c >> 1), pk);
+  }
+  const float2 s0 = f2_unpack(acc[0]), s1 = f2_unpack(acc[1]);
+  return (s0.x + s0.y) + (s1.x + s1.y);
 }
 
 template <int G>
-__global__ void __launch_bounds__(64)
+__global__ void __launch_bounds__(kRingTcThreads, 1)
     decode_ring_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                           const __grid_constant__ CUtensorMap mapK,
                           const __grid_constant__ CUtensorMap mapV, const DecodeArgs a) {
@@ -1022,187 +1093,268 @@ __global__ void __launch_bounds__(64)
                                              ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, rows = G * T;
-  const int b = blockIdx.x / a.hkv, kvh = blockIdx.x - b * a.hkv;
+  const int nitems = a.B * a.hkv;
   const int RR = ring_tc_rows(a.cap);
-  const int kbox = RR * 128;
-  uint8_t* ks = smem + kRingTcOffK;
-  uint8_t* vs = ks + 3 * kbox;
-  RingTcBars* bars = reinterpret_cast<RingTcBars*>(smem + ring_tc_bar_offset(a.cap));
+  RingTcBars* bars = reinterpret_cast<RingTcBars*>(smem + kRingTcOffBar);
   volatile int* abort = &bars->abort;
-  const int L = __ldg(a.seqlens + b);
-  if (!length_ok(L, a)) {
-    if (threadIdx.x == 0 && kvh == 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
-    return;
-  }
-  if (threadIdx.x == 32) {
-    mbar_init(&bars->full, 1);
-    mbar_init(&bars->q_ready, 32);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_full, 32);
-    mbar_init(&bars->pv_done, 1);
-    mbar_init(&bars->drain, 1);
+  if (threadIdx.x == 64) {
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&bars->qk_full[j], 1);
+      mbar_init(&bars->v_full[j], 1);
+      mbar_init(&bars->qk_empty[j], 1);
+      mbar_init(&bars->v_empty[j], 1);
+      mbar_init(&bars->s_full[j], 1);
+      mbar_init(&bars->pv_done[j], 1);
+      mbar_init(&bars->drain[j], 1);
+      mbar_init(&bars->pair[j], 2);
+    }
     bars->abort = 0;
     mbar_fence_init();
   }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 256);
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
-  // V rows past cap are read by the last PV k-step: make them zero
-  for (int e = threadIdx.x; e < (RR - a.cap) * 16; e += 64) {
-    const int rr = a.cap + (e >> 4), c16 = e & 15;
-    *reinterpret_cast<uint4*>(vs + (c16 >> 3) * kbox + rr * 128 + (c16 & 7) * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
+  // V rows past cap are read by the last PV k-step and never loaded: zero
+  // them once in both buffers
+  for (int e = threadIdx.x; e < 2 * (kRingTcMaxCap - a.cap) * 16; e += kRingTcThreads) {
+    const int j = e & 1, rr = a.cap + (e >> 5), c16 = (e >> 1) & 15;
+    *reinterpret_cast<uint4*>(smem + j * kRingTcBuf + kRingTcOffV + (c16 >> 3) * kRingTcKBox +
+                              rr * 128 + (c16 & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  if (threadIdx.x == 32) {
-    tma_prefetch_map(&mapQ);
-    tma_prefetch_map(&mapK);
-    tma_prefetch_map(&mapV);
-    mbar_arrive_expect_tx(&bars->full, uint32_t(3 * rows * 128 + 5 * a.cap * 128));
-    const int plane = b * a.hkv + kvh;
-    for (int i = 0; i < 3; ++i)
-      tma_load_3d(smem + i * kRingTcQBox, &mapQ, &bars->full, 64 * i, kvh * G, b * T);
-    for (int i = 0; i < 3; ++i) tma_load_3d(ks + i * kbox, &mapK, &bars->full, 64 * i, 0, plane);
-    for (int i = 0; i < 2; ++i)
-      tma_load_3d(vs + i * kbox, &mapV, &bars->full, 64 * i, 0, plane);
-  }
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ rows
+  if (warp == 2) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&mapQ);
+      tma_prefetch_map(&mapK);
+      tma_prefetch_map(&mapV);
+      int qk_uses[2] = {0, 0}, v_uses[2] = {0, 0};
+      // Q/K of item iq once its buffer's Q/K are free; V of item iv once that
+      // item's Q/K have landed (the softmax needs them first) and its
+      // buffer's V is free.  Q/K run at most two items ahead of V, so that
+      // the full-barrier phase V tests is still the current one.
+      const int nmine = (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1;
+      int iq = 0, iv = 0;
+      uint64_t t_last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (iv < nmine) {
+        bool prog = false;
+        if (iq < nmine && iq < iv + 2) {
+          const int j = iq & 1, use = iq >> 1;
+          if (use == 0 || mbar_test_wait(&bars->qk_empty[j], (use - 1) & 1u)) {
+            const int v = blockIdx.x + iq * gridDim.x;
+            const int b = v / a.hkv, kvh = v - b * a.hkv;
+            uint8_t* buf = smem + j * kRingTcBuf;
+            mbar_arrive_expect_tx(&bars->qk_full[j], uint32_t(3 * rows * 128 + 3 * a.cap * 128));
+            for (int k = 0; k < 3; ++k)
+              tma_load_3d(buf + k * kRingTcQBox, &mapQ, &bars->qk_full[j], 64 * k, kvh * G, b * T);
+            for (int k = 0; k < 3; ++k)
+              tma_load_3d(buf + kRingTcOffK + k * kRingTcKBox, &mapK, &bars->qk_full[j], 64 * k,
+                          0, v);
+            qk_uses[j] = use + 1;
+            ++iq;
+            prog = true;
+          }
+        }
+        if (iv < iq) {
+          const int j = iv & 1, use = iv >> 1;
+          if (mbar_test_wait(&bars->qk_full[j], use & 1u) &&
+              (use == 0 || mbar_test_wait(&bars->v_empty[j], (use - 1) & 1u))) {
+            const int v = blockIdx.x + iv * gridDim.x;
+            uint8_t* buf = smem + j * kRingTcBuf;
+            mbar_arrive_expect_tx(&bars->v_full[j], uint32_t(2 * a.cap * 128));
+            for (int k = 0; k < 2; ++k)
+              tma_load_3d(buf + kRingTcOffV + k * kRingTcKBox, &mapV, &bars->v_full[j], 64 * k, 0,
+                          v);
+            v_uses[j] = use + 1;
+            ++iv;
+            prog = true;
+          }
+        }
+        if (prog) {
+          t_last = globaltimer_ns();
+          spins = 0;
+        } else if (((++spins) & 15u) == 0u) {
+          if (*abort) break;
+          if (globaltimer_ns() - t_last > a.ctl.wait_limit_ns) {
+            record_status(a.ctl, HATTN_ERR_TIMEOUT);
+            *abort = 1;
+            break;
+          }
+        }
+      }
+      // never leave with copies in flight
+      for (int j = 0; j < 2; ++j) {
+        if (qk_uses[j]) mbar_wait_drain(&bars->qk_full[j], (qk_uses[j] - 1) & 1u, a.ctl);
+        if (v_uses[j]) mbar_wait_drain(&bars->v_full[j], (v_uses[j] - 1) & 1u, a.ctl);
+      }
+    }
+  } else if (warp != 3) {
+    // ------------------------------------------------------------ workers
+    const int w = warp & 3;          // worker = TMEM lane quadrant
+    const int hf = warp >> 2;        // half of the row's work
+    const bool issuer = hf == 0 && lane == 0;
     const int r = lane;
     const bool real = r < rows;
     const int t = real ? r / G : 0, hh = r % G;
-    const int p = L - T + t;  // this row's query position
-    bool ok = warp_wait(&bars->full, 0, a.ctl, abort);
-    if (ok) {
-      const int nslots = min(L, a.cap);  // slots written so far
-      for (int e = lane; e < (a.cap - nslots) * 16; e += 32) {  // never written: zero V
-        const int rr = nslots + (e >> 4), c16 = e & 15;
-        *reinterpret_cast<uint4*>(vs + (c16 >> 3) * kbox + rr * 128 + (c16 & 7) * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+    uint8_t* buf = smem + w * kRingTcBuf;
+    uint8_t* cs_tab = smem + kRingTcOffCs + w * 4 * kRingTcCsRow;
+    float* red = reinterpret_cast<float*>(smem + kRingTcOffRed) + w * 128;  // [half][max|sum][32]
+    const uint32_t sbuf = smem_u32(buf);
+    const uint32_t t_s = tmem + (uint32_t(32 * w) << 16) + 256u * w;
+    const uint32_t d_s = tmem + 256u * w;  // MMA accumulator (lane field 0)
+    uint32_t pph = 0;                      // phase of this worker's pair barrier
+    bool issued = false;
+    uint32_t nv = 0;  // items this worker computed: phases of s_full and pv_done
+    for (int i = w;; i += 2) {
+      const int v = blockIdx.x + i * gridDim.x;
+      if (v >= nitems) break;
+      const uint32_t ph = uint32_t(i >> 1) & 1u;
+      const int b = v / a.hkv, kvh = v - b * a.hkv;
+      const int L = __ldg(a.seqlens + b);
+      const bool valid = length_ok(L, a);
+      if (valid) {
+        // (cos, sin) of the 16 frequencies this half rotates, at each of the
+        // T query positions
+        const int f = 16 * hf + (lane & 15);
+        for (int tt = lane >> 4; tt < T; tt += 2)
+          *reinterpret_cast<float2*>(cs_tab + tt * kRingTcCsRow + f * 8) =
+              rope_cos_sin(L - T + tt, a.freqs.hi[f], a.freqs.lo[f]);
       }
-      // RoPE of this row's dims 0..63 (box 0, 128-byte rows, 16-byte chunks
-      // swizzled by row % 8); the G lanes of one token share its 32 angles
-      float2 cs_own[32 / G];
+      __syncwarp();
+      if (!warp_wait(&bars->qk_full[w], ph, a.ctl, abort)) break;
+      const int p = L - T + t;  // this row's query position
+      if (valid) {
+        // RoPE of this row's dim pairs (f, f + 32), f in this half's 16:
+        // chunks c and c + 4 of box 0 (128-byte rows, 16-byte chunks
+        // swizzled by row % 8)
+        const uint8_t* cs_row = cs_tab + t * kRingTcCsRow;
+        uint8_t* qrow = buf + r * 128;
+        uint32_t big = 0u;
 #pragma unroll
-      for (int k2 = 0; k2 < 32 / G; ++k2)
-        cs_own[k2] = rope_cos_sin(p, a.freqs.hi[hh + G * k2], a.freqs.lo[hh + G * k2]);
-      uint8_t* qrow = smem + r * 128;
-      uint4 ch[8];
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * hf + cc;
+          uint4 cx = *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
+          uint4 cy = *reinterpret_cast<uint4*>(qrow + (((c + 4) ^ (r & 7)) << 4));
+          uint32_t* x = reinterpret_cast<uint32_t*>(&cx);
+          uint32_t* y = reinterpret_cast<uint32_t*>(&cy);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ch[c] = *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
-      uint32_t big = 0u;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t* x = reinterpret_cast<uint32_t*>(&ch[c]);
-        uint32_t* y = reinterpret_cast<uint32_t*>(&ch[c + 4]);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int i = 8 * c + 2 * w;
-          const float2 xv = unpack_bf16x2(x[w]);
-          const float2 yv = unpack_bf16x2(y[w]);
-          const float2 c0 = shared_cos_sin<G>(cs_own, i, lane);
-          const float2 c1 = shared_cos_sin<G>(cs_own, i + 1, lane);
-          const float a0 = xv.x * c0.x - yv.x * c0.y, a1 = xv.y * c1.x - yv.y * c1.y;
-          const float b0 = yv.x * c0.x + xv.x * c0.y, b1 = yv.y * c1.x + xv.y * c1.y;
-          x[w] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
-          y[w] = pack_f16x2(b0, b1);
-          big = f16x2_absmax3(big, x[w], y[w]);
+          for (int q = 0; q < 4; ++q) {
+            const float4 cs = *reinterpret_cast<const float4*>(cs_row + (8 * c + 2 * q) * 8);
+            const float2 xv = unpack_bf16x2(x[q]);
+            const float2 yv = unpack_bf16x2(y[q]);
+            const float a0 = xv.x * cs.x - yv.x * cs.y, a1 = xv.y * cs.z - yv.y * cs.w;
+            const float b0 = yv.x * cs.x + xv.x * cs.y, b1 = yv.y * cs.z + xv.y * cs.w;
+            x[q] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
+            y[q] = pack_f16x2(b0, b1);
+            big = f16x2_absmax3(big, x[q], y[q]);
+          }
+          if (real) {
+            *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = cx;
+            *reinterpret_cast<uint4*>(qrow + (((c + 4) ^ (r & 7)) << 4)) = cy;
+          }
         }
+        if (real && f16x2_any_inf(big)) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+        fence_proxy_async_smem();
+      } else if (lane == 0 && hf == 0 && kvh == 0) {
+        record_status(a.ctl, HATTN_ERR_INVALID_ARG);
       }
-      if (real) {
-        if (f16x2_any_inf(big)) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+      // both halves' Q rows are written and their reads of this TMEM half
+      // (the previous item's epilogue) complete
+      tc_fence_before();
+      if (!pair_sync(&bars->pair[w], pph, lane, a, abort)) break;
+      if (!valid) {
+        // nothing to compute: hand the buffer back once V has landed too
+        const bool ok = warp_wait(&bars->v_full[w], ph, a.ctl, abort);
+        if (issuer) {
+          mbar_arrive(&bars->qk_empty[w]);
+          mbar_arrive(&bars->v_empty[w]);
+        }
+        if (!ok) break;
+        continue;
+      }
+      if (issuer) {
+        tc_fence_after();
+        const uint32_t idesc_rot = make_idesc_f16(128, RR, 0, 0);
+        const uint32_t idesc_s = make_idesc_bf16(128, RR, 0, 0);
+        const uint64_t qd = make_sdesc_sw128(sbuf - uint32_t(w * kRingTcQBox), 16, 1024);
+        const uint64_t kd = make_sdesc_sw128(sbuf + kRingTcOffK, 16, 1024);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4)) = ch[c];
+        for (int kk = 0; kk < 12; ++kk)
+          umma_ss(d_s, qd + uint64_t(((kk >> 2) * kRingTcQBox + (kk & 3) * 32) >> 4),
+                  kd + uint64_t(((kk >> 2) * kRingTcKBox + (kk & 3) * 32) >> 4),
+                  kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit(&bars->s_full[w]);
+        umma_commit(&bars->qk_empty[w]);  // Q and K of the buffer may be refilled
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->q_ready);
-      ok = warp_wait(&bars->s_full, 0, a.ctl, abort);
-    } else {
-      mbar_wait_drain(&bars->full, 0, a.ctl);  // never leave with copies in flight
-    }
-    float m = -INFINITY, l = 0.f;
-    if (ok) {
-      tc_fence_after();
+      issued = true;
       // visible positions [lo, p] sit in the cyclic slot interval starting at
       // lo mod cap (a ring holds the last cap >= W + T - 1 positions)
       const int lo = max(p - a.window + 1, 0);
       const int nvis = real ? p - lo + 1 : 0;
       const int s_lo = lo % a.cap;
-      const uint32_t t_s = tmem + (uint32_t(0) << 16);
-      constexpr int H1 = 80, H2 = kRingTcCols - H1;
-      float l1;
-      {
-        uint32_t s1[H1];
+      const int e1 = min(s_lo + nvis, a.cap), e2 = s_lo + nvis - a.cap;
+      uint32_t vis[5];
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) tmem_ld32_nowait(t_s + c, s1 + c);
-        tmem_ld16_nowait(t_s + 64, s1 + 64);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < H1; ++e) tmem_reg_fence(s1[e]);
-        ring_mask<H1>(s1, 0, s_lo, nvis, a.cap);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < H1; e += 2) mx = fmax3f(mx, __uint_as_float(s1[e]), __uint_as_float(s1[e + 1]));
-        m = mx * a.scale_log2;
-        uint32_t s2[H2];
-#pragma unroll
-        for (int c = 0; c < H2; c += 32) tmem_ld32_nowait(t_s + H1 + c, s2 + c);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < H2; ++e) tmem_reg_fence(s2[e]);
-        ring_mask<H2>(s2, H1, s_lo, nvis, a.cap);
-        float mx2 = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < H2; e += 2) mx2 = fmax3f(mx2, __uint_as_float(s2[e]), __uint_as_float(s2[e + 1]));
-        m = fmaxf(m, mx2 * a.scale_log2);  // exact max over the whole ring
-        const float msub = m == -INFINITY ? 0.f : m;
-        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-        const uint64_t nm2 = f2_pack(-msub, -msub);
-        uint64_t acc = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < H1; c += 16) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float2 x = f2_unpack(
-                f2_fma(f2_pack(__uint_as_float(s1[c + e]), __uint_as_float(s1[c + e + 1])), sc2, nm2));
-            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-            acc = f2_add(acc, f2_pack(p0, p1));
-          }
-          tmem_st8(t_s + (c >> 1), pk);
-        }
-#pragma unroll
-        for (int c = 0; c < H2; c += 16) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float2 x = f2_unpack(
-                f2_fma(f2_pack(__uint_as_float(s2[c + e]), __uint_as_float(s2[c + e + 1])), sc2, nm2));
-            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-            acc = f2_add(acc, f2_pack(p0, p1));
-          }
-          tmem_st8(t_s + ((H1 + c) >> 1), pk);
-        }
-        const float2 sum = f2_unpack(acc);
-        l1 = sum.x + sum.y;
-      }
-      l = l1;
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full);
-      ok = warp_wait(&bars->pv_done, 0, a.ctl, abort);
-    }
-    if (ok) {
-      // ---- epilogue: add the sink, finish the row
+      for (int k = 0; k < 5; ++k) vis[k] = ring_bits(k, s_lo, e1) | ring_bits(k, 0, e2);
+      const uint32_t phc = nv++ & 1u;
+      if (!warp_wait(&bars->s_full[w], phc, a.ctl, abort)) break;
       tc_fence_after();
+      float m, l_own;
+      if (hf == 0) {
+        uint32_t s[kRingTcH0];
+        red[lane] = ring_load_max<kRingTcH0, 0>(t_s, s, vis);
+        tc_fence_before();  // S reads done before the other half writes P
+        if (!pair_sync(&bars->pair[w], pph, lane, a, abort)) break;
+        tc_fence_after();
+        m = fmaxf(red[lane], red[64 + lane]) * a.scale_log2;  // exact max over the ring
+        l_own = ring_exp_store<kRingTcH0>(s, t_s, a.scale_log2, m == -INFINITY ? 0.f : m);
+      } else {
+        uint32_t s[kRingTcH1];
+        red[64 + lane] = ring_load_max<kRingTcH1, kRingTcH0>(t_s, s, vis);
+        tc_fence_before();  // S reads done before the other half writes P
+        if (!pair_sync(&bars->pair[w], pph, lane, a, abort)) break;
+        tc_fence_after();
+        m = fmaxf(red[lane], red[64 + lane]) * a.scale_log2;
+        l_own = ring_exp_store<kRingTcH1>(s, t_s + kRingTcH0 / 2, a.scale_log2,
+                                          m == -INFINITY ? 0.f : m);
+      }
+      red[32 + 64 * hf + lane] = l_own;
+      tmem_st_wait();
+      if (!warp_wait(&bars->v_full[w], ph, a.ctl, abort)) break;
+      const int nslots = min(L, a.cap);  // slots written so far; the rest may hold anything
+      if (nslots < a.cap) {
+        uint8_t* vs = buf + kRingTcOffV;
+        for (int e = 32 * hf + lane; e < (a.cap - nslots) * 16; e += 64) {
+          const int rr = nslots + (e >> 4), c16 = e & 15;
+          *reinterpret_cast<uint4*>(vs + (c16 >> 3) * kRingTcKBox + rr * 128 + (c16 & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+      }
+      // both halves' P columns are in TMEM, V is complete
+      tc_fence_before();
+      if (!pair_sync(&bars->pair[w], pph, lane, a, abort)) break;
+      if (issuer) {
+        tc_fence_after();
+        constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, 0, 1);
+        const uint64_t vd = make_sdesc_sw128(sbuf + kRingTcOffV, kRingTcKBox, 1024);
+        for (int kk = 0; kk < RR / 16; ++kk)
+          umma_ts(d_s + 128, d_s + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_o,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(&bars->pv_done[w]);
+        umma_commit(&bars->v_empty[w]);  // V of the buffer may be refilled
+      }
+      const float l = red[32 + lane] + red[96 + lane];
+      if (!warp_wait(&bars->pv_done[w], phc, a.ctl, abort)) break;
+      tc_fence_after();
+      // ---- epilogue: add the sink, finish this half of the row
       const int h = kvh * G + hh;
       const float sl2 = __ldg(a.sink + h) * kLog2e;
       const float mt_ = fmaxf(m, sl2);
@@ -1212,65 +1364,40 @@ __global__ void __launch_bounds__(64)
       const float sc = fo / (l * fo + sw);
       const uint64_t sc2 = f2_pack(sc, sc);
       const long orow = (long(b) * T + t) * a.hq + h;
-      uint8_t* op = static_cast<uint8_t*>(a.out) + orow * 256;
+      uint4* op = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + orow * 256 + hf * 128);
+      uint32_t o[64];
+      tmem_ld32_nowait(t_s + 128 + hf * 64, o);
+      tmem_ld32_nowait(t_s + 128 + hf * 64 + 32, o + 32);
+      tmem_ld_wait();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[64];
-        tmem_ld32_nowait(tmem + 128 + half * 64, v);
-        tmem_ld32_nowait(tmem + 128 + half * 64 + 32, v + 32);
-        tmem_ld_wait();
+      for (int e = 0; e < 64; ++e) tmem_reg_fence(o[e]);
+      uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) tmem_reg_fence(v[e]);
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float2 y = f2_unpack(
-              f2_mul(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sc2));
-          pk[e] = pack_bf16x2(y.x, y.y);
-        }
-        if (real) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            reinterpret_cast<uint4*>(op + half * 128)[e] =
-                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
+      for (int e = 0; e < 32; ++e) {
+        const float2 y = f2_unpack(
+            f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), sc2));
+        pk[e] = pack_bf16x2(y.x, y.y);
       }
-      if (real && a.lse) a.lse[orow] = (msub + log2f(l * fo + sw)) * kLn2;
-    }
-  } else if (lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t idesc_rot = make_idesc_f16(128, RR, 0, 0);
-    const uint32_t idesc_s = make_idesc_bf16(128, RR, 0, 0);
-    constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, 0, 1);
-    if (mbar_wait(&bars->q_ready, 0, a.ctl, abort)) {
-      tc_fence_after();
-      const uint64_t qd = make_sdesc_sw128(sbase, 16, 1024);
-      const uint64_t kd = make_sdesc_sw128(sbase + kRingTcOffK, 16, 1024);
+      if (real) {
 #pragma unroll
-      for (int kk = 0; kk < 12; ++kk)
-        umma_ss(tmem, qd + uint64_t(((kk >> 2) * kRingTcQBox + (kk & 3) * 32) >> 4),
-                kd + uint64_t(((kk >> 2) * kbox + (kk & 3) * 32) >> 4),
-                kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
-      umma_commit(&bars->s_full);
-      if (mbar_wait(&bars->p_full, 0, a.ctl, abort)) {
-        tc_fence_after();
-        const uint64_t vd = make_sdesc_sw128(sbase + kRingTcOffK + 3 * kbox, kbox, 1024);
-        for (int kk = 0; kk < RR / 16; ++kk)
-          umma_ts(tmem + 128, tmem + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_o,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(&bars->pv_done);
+        for (int e = 0; e < 8; ++e)
+          op[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        if (hf == 0 && a.lse) a.lse[orow] = (msub + log2f(l * fo + sw)) * kLn2;
       }
     }
-    // every MMA issued must be complete before TMEM is released
-    umma_commit(&bars->drain);
-    mbar_wait_drain(&bars->drain, 0, a.ctl);
+    // every MMA this worker issued must be complete before TMEM is released
+    tc_fence_before();
+    __syncwarp();
+    if (issuer && issued) {
+      umma_commit(&bars->drain[w]);
+      mbar_wait_drain(&bars->drain[w], 0, a.ctl);
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -1278,9 +1405,8 @@ template <int G>
 cudaError_t launch_ring_tc(const DecodeArgs& a, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_ring_tc_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         ring_tc_smem(kRingTcMaxCap));
+    cudaError_t e = cudaFuncSetAttribute(
+        decode_ring_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingTcSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1289,10 +1415,9 @@ cudaError_t launch_ring_tc(const DecodeArgs& a, cudaStream_t s) {
       !make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, a.cap, 1) ||
       !make_map(&mv, a.v_cache, long(a.B) * a.hkv, a.cap, kDv, a.cap, 1))
     return cudaErrorInvalidValue;
-  // the full-size footprint for every ring keeps two CTAs on an SM, which is
-  // what their 2 x 256 TMEM columns allow
-  decode_ring_tc_kernel<G>
-      <<<unsigned(long(a.B) * a.hkv), 64, ring_tc_smem(kRingTcMaxCap), s>>>(mq, mk, mv, a);
+  const long items = long(a.B) * a.hkv;
+  const int grid = int(items < num_sms() ? items : num_sms());
+  decode_ring_tc_kernel<G><<<unsigned(grid), kRingTcThreads, kRingTcSmem, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
