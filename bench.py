@@ -239,19 +239,22 @@ class Workload:
         return 2
 
     def run_decode(self, dd, stream, q=None, k_new=None, v_new=None):
+        """One decode / verify step of the layer: the append of the T new
+        tokens and the attention over the cache, one C-ABI call."""
         ha, p = self.ha, dd["p"]
-        st = ha.hattn_rope_kv_append(dd["k_new"] if k_new is None else k_new,
-                                     dd["v_new"] if v_new is None else v_new, dd["start"],
-                                     dd["kc"], dd["vc"], self.B, self.T, p["hkv"], D_QK, D_V,
-                                     dd["cap"], 1 if dd["ring"] else 0, R, p["rope_base"], stream)
+        st = ha.hattn_decode_append(dd["q"] if q is None else q,
+                                    dd["k_new"] if k_new is None else k_new,
+                                    dd["v_new"] if v_new is None else v_new, dd["kc"], dd["vc"],
+                                    dd["seqlens"], dd["sink"], dd["out"], dd["lse"], self.B,
+                                    self.T, p["hq"], p["hkv"], D_QK, D_V, dd["cap"],
+                                    1 if dd["ring"] else 0, p["window"], self.lmax, R,
+                                    p["rope_base"], 1.0 / math.sqrt(D_QK), dd["ws"],
+                                    dd["ws"].numel(), stream)
         assert st == 0, ha.status_string(st)
-        st = ha.hattn_decode(dd["q"] if q is None else q, dd["kc"], dd["vc"], dd["seqlens"],
-                             dd["sink"], dd["out"], dd["lse"], self.B, self.T, p["hq"], p["hkv"],
-                             D_QK, D_V, dd["cap"], 1 if dd["ring"] else 0, p["window"],
-                             self.lmax, R, p["rope_base"], 1.0 / math.sqrt(D_QK), dd["ws"],
-                             dd["ws"].numel(), stream)
-        assert st == 0, ha.status_string(st)
-        return 2 + (1 if dd["ws_n"] else 0)
+        # a ring of <= 144 slots with <= 32 rows per KV head runs the append
+        # inside the attention kernel; otherwise the append kernel goes first
+        fused = dd["ring"] and dd["cap"] <= 144 and (p["hq"] // p["hkv"]) * self.T <= 32
+        return (1 if fused else 2) + (1 if dd["ws_n"] else 0)
 
     def flops(self):
         return sum(l["flops"] for l in self.layers) + sum(d["flops"] for d in self.dec)

@@ -46,6 +46,8 @@ SIGNATURES = {
     "hattn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "hattn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                           _F, _F, _P, _Z, _P]),
+    "hattn_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                 _I, _I, _I, _I, _F, _F, _P, _Z, _P]),
     "hattn_decode_static_scratch": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                          _I, _I, _I, _I, _F, _F, _P]),
     "hattn_check_device_status": (_I, [_P]),
@@ -144,6 +146,16 @@ def hattn_decode(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv, 
         int(workspace_bytes), _stream(stream))
 
 
+def hattn_decode_append(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq,
+                        hkv, dqk, dv, cap, is_ring, window, max_seqlen_k, rope_dim, rope_base,
+                        softmax_scale, workspace, workspace_bytes, stream=None) -> int:
+    return load_library().hattn_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens_k),
+        _ptr(sink), _ptr(out), _ptr(lse), int(B), int(T), int(hq), int(hkv), int(dqk), int(dv),
+        int(cap), int(is_ring), int(window), int(max_seqlen_k), int(rope_dim), float(rope_base),
+        float(softmax_scale), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
 def hattn_decode_static_scratch(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv,
                                 dqk, dv, cap, is_ring, window, max_seqlen_k, rope_dim, rope_base,
                                 softmax_scale, stream=None) -> int:
@@ -224,6 +236,33 @@ def decode(q, k_cache, v_cache, seqlens_k, sink, *, max_seqlen_k: int, window: i
                         cap, 1 if is_ring else 0, window, max_seqlen_k, ROPE_DIM, rope_base,
                         softmax_scale, workspace, workspace.numel() if workspace is not None else 0),
            "hattn_decode")
+    return out, lse
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, *, max_seqlen_k: int,
+                  window: int, is_ring: bool, rope_base: float,
+                  softmax_scale: float | None = None, out=None, lse=None, workspace=None,
+                  with_lse: bool = True):
+    """Append the T = q.shape[1] new tokens' K/V to the caches and run the
+    decode / verify step over them; returns (out, lse)."""
+    B, T, hq, dqk = q.shape
+    hkv, cap = k_cache.shape[1], k_cache.shape[2]
+    dv = v_cache.shape[3]
+    if softmax_scale is None:
+        softmax_scale = dqk ** -0.5
+    if out is None:
+        out = torch.empty((B, T, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((B, T, hq), dtype=torch.float32, device=q.device)
+    need = hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window, cap,
+                                       1 if is_ring else 0)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(hattn_decode_append(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, out, lse, B, T,
+                               hq, hkv, dqk, dv, cap, 1 if is_ring else 0, window, max_seqlen_k,
+                               ROPE_DIM, rope_base, softmax_scale, workspace,
+                               workspace.numel() if workspace is not None else 0),
+           "hattn_decode_append")
     return out, lse
 
 

@@ -972,9 +972,10 @@ cudaError_t launch_ring(const DecodeArgs& a, cudaStream_t s) {
 // the ring's K and V), its own half of TMEM and its own TMEM lane quadrant,
 // so that one item's loads, MMAs and softmax overlap the other's.
 //   warp 2   TMEM allocator; lane 0 loads item i into buffer i % 2: Q (3
-//            boxes of [G*T rows][64 dims]) with K (3 boxes of [cap slots][64
-//            dims]) on one barrier, V (2 boxes) on another, the Q/K loads of
-//            an item ahead of the V loads of the one before.  Q/K and V of a
+//            boxes of [G*T rows][64 dims]), K (3 boxes of [cap slots][64
+//            dims]) and V (2 boxes), each on its own barrier, the Q/K loads
+//            of an item ahead of the V loads of the one before (the first
+//            two items' Q/K before the rest of the setup).  Q/K and V of a
 //            buffer are refilled as soon as the MMAs that read them are done.
 //   worker w = warps w and w + 4 (TMEM lane quadrant w, one lane per query
 //            row; the two warps split each row's work in halves): RoPE of the
@@ -1007,8 +1008,8 @@ static_assert(kRingTcH0 + kRingTcH1 == kRingTcMaxCap, "halves cover the ring");
 __host__ __device__ constexpr int ring_tc_rows(int cap) { return (cap + 15) & ~15; }
 
 struct RingTcBars {
-  uint64_t qk_full[2], v_full[2], qk_empty[2], v_empty[2], s_full[2], pv_done[2], drain[2];
-  uint64_t pair[2];  // the two warps of a worker meet here (one arrival per warp)
+  uint64_t q_full[2], k_full[2], v_full[2], qk_empty[2], v_empty[2], s_full[2], pv_done[2];
+  uint64_t drain[2], pair[2];  // the two warps of a worker meet here (one arrival per warp)
   uint32_t tmem_base;
   int abort;
 };
@@ -1097,9 +1098,24 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
   const int RR = ring_tc_rows(a.cap);
   RingTcBars* bars = reinterpret_cast<RingTcBars*>(smem + kRingTcOffBar);
   volatile int* abort = &bars->abort;
+  // Q (3 boxes of [G*T rows][64 dims]) on q_full, K (3 boxes of [cap slots]
+  // [64 dims]) on k_full of buffer j = i % 2
+  auto load_qk = [&](int i) {
+    const int v = blockIdx.x + i * gridDim.x;
+    const int b = v / a.hkv, kvh = v - b * a.hkv, j = i & 1;
+    uint8_t* buf = smem + j * kRingTcBuf;
+    mbar_arrive_expect_tx(&bars->q_full[j], uint32_t(3 * rows * 128));
+    for (int k = 0; k < 3; ++k)
+      tma_load_3d(buf + k * kRingTcQBox, &mapQ, &bars->q_full[j], 64 * k, kvh * G, b * T);
+    mbar_arrive_expect_tx(&bars->k_full[j], uint32_t(3 * a.cap * 128));
+    for (int k = 0; k < 3; ++k)
+      tma_load_3d(buf + kRingTcOffK + k * kRingTcKBox, &mapK, &bars->k_full[j], 64 * k, 0, v);
+  };
+  const int nmine = (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1;  // items of this CTA
   if (threadIdx.x == 64) {
     for (int j = 0; j < 2; ++j) {
-      mbar_init(&bars->qk_full[j], 1);
+      mbar_init(&bars->q_full[j], 1);
+      mbar_init(&bars->k_full[j], 1);
       mbar_init(&bars->v_full[j], 1);
       mbar_init(&bars->qk_empty[j], 1);
       mbar_init(&bars->v_empty[j], 1);
@@ -1110,8 +1126,15 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
     }
     bars->abort = 0;
     mbar_fence_init();
+    fence_proxy_async_smem();
+    // the first two items' Q/K go out before the rest of the setup
+    tma_prefetch_map(&mapQ);
+    tma_prefetch_map(&mapK);
+    tma_prefetch_map(&mapV);
+    for (int i = 0; i < 2 && i < nmine; ++i) load_qk(i);
   }
   if (warp == 2) {
+    __syncwarp();
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -1131,32 +1154,20 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
   if (warp == 2) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_map(&mapQ);
-      tma_prefetch_map(&mapK);
-      tma_prefetch_map(&mapV);
-      int qk_uses[2] = {0, 0}, v_uses[2] = {0, 0};
+      int qk_uses[2] = {nmine > 0 ? 1 : 0, nmine > 1 ? 1 : 0}, v_uses[2] = {0, 0};
       // Q/K of item iq once its buffer's Q/K are free; V of item iv once that
-      // item's Q/K have landed (the softmax needs them first) and its
-      // buffer's V is free.  Q/K run at most two items ahead of V, so that
-      // the full-barrier phase V tests is still the current one.
-      const int nmine = (nitems - 1 - int(blockIdx.x)) / int(gridDim.x) + 1;
-      int iq = 0, iv = 0;
+      // item's K has landed (the softmax needs it first) and its buffer's V
+      // is free.  Q/K run at most two items ahead of V, so that the
+      // full-barrier phase V tests is still the current one.
+      int iq = nmine < 2 ? nmine : 2, iv = 0;
       uint64_t t_last = globaltimer_ns();
       uint32_t spins = 0;
       while (iv < nmine) {
         bool prog = false;
         if (iq < nmine && iq < iv + 2) {
           const int j = iq & 1, use = iq >> 1;
-          if (use == 0 || mbar_test_wait(&bars->qk_empty[j], (use - 1) & 1u)) {
-            const int v = blockIdx.x + iq * gridDim.x;
-            const int b = v / a.hkv, kvh = v - b * a.hkv;
-            uint8_t* buf = smem + j * kRingTcBuf;
-            mbar_arrive_expect_tx(&bars->qk_full[j], uint32_t(3 * rows * 128 + 3 * a.cap * 128));
-            for (int k = 0; k < 3; ++k)
-              tma_load_3d(buf + k * kRingTcQBox, &mapQ, &bars->qk_full[j], 64 * k, kvh * G, b * T);
-            for (int k = 0; k < 3; ++k)
-              tma_load_3d(buf + kRingTcOffK + k * kRingTcKBox, &mapK, &bars->qk_full[j], 64 * k,
-                          0, v);
+          if (mbar_test_wait(&bars->qk_empty[j], (use - 1) & 1u)) {
+            load_qk(iq);
             qk_uses[j] = use + 1;
             ++iq;
             prog = true;
@@ -1164,7 +1175,7 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
         }
         if (iv < iq) {
           const int j = iv & 1, use = iv >> 1;
-          if (mbar_test_wait(&bars->qk_full[j], use & 1u) &&
+          if (mbar_test_wait(&bars->k_full[j], use & 1u) &&
               (use == 0 || mbar_test_wait(&bars->v_empty[j], (use - 1) & 1u))) {
             const int v = blockIdx.x + iv * gridDim.x;
             uint8_t* buf = smem + j * kRingTcBuf;
@@ -1191,7 +1202,10 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       }
       // never leave with copies in flight
       for (int j = 0; j < 2; ++j) {
-        if (qk_uses[j]) mbar_wait_drain(&bars->qk_full[j], (qk_uses[j] - 1) & 1u, a.ctl);
+        if (qk_uses[j]) {
+          mbar_wait_drain(&bars->q_full[j], (qk_uses[j] - 1) & 1u, a.ctl);
+          mbar_wait_drain(&bars->k_full[j], (qk_uses[j] - 1) & 1u, a.ctl);
+        }
         if (v_uses[j]) mbar_wait_drain(&bars->v_full[j], (v_uses[j] - 1) & 1u, a.ctl);
       }
     }
@@ -1212,13 +1226,53 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
     uint32_t pph = 0;                      // phase of this worker's pair barrier
     bool issued = false;
     uint32_t nv = 0;  // items this worker computed: phases of s_full and pv_done
+    // the sequence length and this row's sink logit of the worker's next
+    // item are loaded one item ahead: their latency hides behind the
+    // current item instead of stalling its start and its epilogue
+    auto item_len = [&](int i) {
+      const int v = blockIdx.x + i * gridDim.x;
+      return v < nitems ? __ldg(a.seqlens + v / a.hkv) : 0;
+    };
+    auto item_sink = [&](int i) {
+      const int v = blockIdx.x + i * gridDim.x;
+      return v < nitems ? __ldg(a.sink + (v % a.hkv) * G + hh) : 0.f;
+    };
+    int L_next = item_len(w);
+    float sink_next = item_sink(w);
     for (int i = w;; i += 2) {
       const int v = blockIdx.x + i * gridDim.x;
       if (v >= nitems) break;
       const uint32_t ph = uint32_t(i >> 1) & 1u;
       const int b = v / a.hkv, kvh = v - b * a.hkv;
-      const int L = __ldg(a.seqlens + b);
+      const int L = L_next;
+      const float sink_row = sink_next;
+      L_next = item_len(i + 2);
+      sink_next = item_sink(i + 2);
       const bool valid = length_ok(L, a);
+      // fused append: this lane's share of the T new tokens' K and V, read
+      // now so that the loads overlap the wait for the ring.  K pairs of
+      // chunks (c, c + 4), c in this half's two rotated chunks: lanes < 2T;
+      // the other 16 K chunks and the 16 V chunks of each token: task
+      // e = 32 hf + lane < 16 T.
+      const bool fuse = a.k_new != nullptr && valid;
+      const int e_task = 32 * hf + lane;
+      const int kp_t = lane >> 1, kp_c = 2 * hf + (lane & 1);
+      const int pl_t = e_task >> 4, pl_c = 8 + (e_task & 15), v_c = e_task & 15;
+      uint4 kp_x = make_uint4(0u, 0u, 0u, 0u), kp_y = kp_x, kpl = kp_x, vpl = kp_x;
+      if (fuse) {
+        const uint4* kn = static_cast<const uint4*>(a.k_new);
+        const uint4* vn = static_cast<const uint4*>(a.v_new);
+        if (lane < 2 * T) {
+          const long row = (long(b) * T + kp_t) * a.hkv + kvh;
+          kp_x = __ldg(kn + row * 24 + kp_c);
+          kp_y = __ldg(kn + row * 24 + kp_c + 4);
+        }
+        if (e_task < 16 * T) {
+          const long row = (long(b) * T + pl_t) * a.hkv + kvh;
+          kpl = __ldg(kn + row * 24 + pl_c);
+          vpl = __ldg(vn + row * 16 + v_c);
+        }
+      }
       if (valid) {
         // (cos, sin) of the 16 frequencies this half rotates, at each of the
         // T query positions
@@ -1228,7 +1282,7 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
               rope_cos_sin(L - T + tt, a.freqs.hi[f], a.freqs.lo[f]);
       }
       __syncwarp();
-      if (!warp_wait(&bars->qk_full[w], ph, a.ctl, abort)) break;
+      if (!warp_wait(&bars->q_full[w], ph, a.ctl, abort)) break;
       const int p = L - T + t;  // this row's query position
       if (valid) {
         // RoPE of this row's dim pairs (f, f + 32), f in this half's 16:
@@ -1265,8 +1319,46 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       } else if (lane == 0 && hf == 0 && kvh == 0) {
         record_status(a.ctl, HATTN_ERR_INVALID_ARG);
       }
-      // both halves' Q rows are written and their reads of this TMEM half
-      // (the previous item's epilogue) complete
+      // both halves' Q rows are written, K has landed, and their reads of
+      // this TMEM half (the previous item's epilogue) are complete
+      if (!warp_wait(&bars->k_full[w], ph, a.ctl, abort)) break;
+      const long plane = long(b) * a.hkv + kvh;
+      if (fuse) {
+        // the new keys over their slots' stale rows: in the loaded ring
+        // (after the load, before the MMA reads it) and in the cache
+        uint8_t* ks = buf + kRingTcOffK;
+        uint4* kc = static_cast<uint4*>(const_cast<void*>(a.k_cache));
+        if (lane < 2 * T) {
+          const int slot = (L - T + kp_t) % a.cap;
+          const uint8_t* cs_row = cs_tab + kp_t * kRingTcCsRow;
+          uint32_t* x = reinterpret_cast<uint32_t*>(&kp_x);
+          uint32_t* y = reinterpret_cast<uint32_t*>(&kp_y);
+          bool over = false;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 cs = *reinterpret_cast<const float4*>(cs_row + (8 * kp_c + 2 * q) * 8);
+            const float2 xv = unpack_bf16x2(x[q]);
+            const float2 yv = unpack_bf16x2(y[q]);
+            const float a0 = xv.x * cs.x - yv.x * cs.y, a1 = xv.y * cs.z - yv.y * cs.w;
+            const float b0 = yv.x * cs.x + xv.x * cs.y, b1 = yv.y * cs.z + xv.y * cs.w;
+            over |= fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max;
+            x[q] = pack_f16x2(a0, a1);  // rotated dims are stored as fp16
+            y[q] = pack_f16x2(b0, b1);
+          }
+          if (over) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+          *reinterpret_cast<uint4*>(ks + slot * 128 + ((kp_c ^ (slot & 7)) << 4)) = kp_x;
+          *reinterpret_cast<uint4*>(ks + slot * 128 + (((kp_c + 4) ^ (slot & 7)) << 4)) = kp_y;
+          kc[(plane * a.cap + slot) * 24 + kp_c] = kp_x;
+          kc[(plane * a.cap + slot) * 24 + kp_c + 4] = kp_y;
+        }
+        if (e_task < 16 * T) {
+          const int slot = (L - T + pl_t) % a.cap;
+          *reinterpret_cast<uint4*>(ks + (pl_c >> 3) * kRingTcKBox + slot * 128 +
+                                    (((pl_c & 7) ^ (slot & 7)) << 4)) = kpl;
+          kc[(plane * a.cap + slot) * 24 + pl_c] = kpl;
+        }
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
       if (!pair_sync(&bars->pair[w], pph, lane, a, abort)) break;
       if (!valid) {
@@ -1328,6 +1420,15 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       red[32 + 64 * hf + lane] = l_own;
       tmem_st_wait();
       if (!warp_wait(&bars->v_full[w], ph, a.ctl, abort)) break;
+      if (fuse && e_task < 16 * T) {
+        // the new values over their slots' stale rows, in the ring and the cache
+        const int slot = (L - T + pl_t) % a.cap;
+        *reinterpret_cast<uint4*>(buf + kRingTcOffV + (v_c >> 3) * kRingTcKBox + slot * 128 +
+                                  (((v_c & 7) ^ (slot & 7)) << 4)) = vpl;
+        static_cast<uint4*>(const_cast<void*>(a.v_cache))[(plane * a.cap + slot) * 16 + v_c] =
+            vpl;
+        fence_proxy_async_smem();
+      }
       const int nslots = min(L, a.cap);  // slots written so far; the rest may hold anything
       if (nslots < a.cap) {
         uint8_t* vs = buf + kRingTcOffV;
@@ -1356,7 +1457,7 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       tc_fence_after();
       // ---- epilogue: add the sink, finish this half of the row
       const int h = kvh * G + hh;
-      const float sl2 = __ldg(a.sink + h) * kLog2e;
+      const float sl2 = sink_row * kLog2e;
       const float mt_ = fmaxf(m, sl2);
       const float msub = mt_ == -INFINITY ? 0.f : mt_;
       const float fo = fast_exp2(m - msub);
@@ -1474,10 +1575,22 @@ size_t decode_workspace_bytes(int B, int T, int hq, int nsplit) {
   return ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeArgs& a_in, cudaStream_t s) {
+  DecodeArgs a = a_in;
   const int G = a.hq / a.hkv;
-  // a ring of <= 144 slots with <= 32 query rows: tensor cores, one CTA per item
-  if (a.is_ring && a.cap <= kRingTcMaxCap && a.nsplit == 1 && G * a.T <= 32) {
+  const bool ring_tc = a.is_ring && a.cap <= kRingTcMaxCap && a.nsplit == 1 && G * a.T <= 32 &&
+                       (G == 1 || G == 2 || G == 4 || G == 8);
+  if (a.k_new && !ring_tc) {
+    // the append as its own launch ahead of the step
+    cudaError_t e = launch_kv_append(a.k_new, a.v_new, a.seqlens, const_cast<void*>(a.k_cache),
+                                     const_cast<void*>(a.v_cache), a.B, a.T, a.hkv, a.cap,
+                                     a.is_ring, a.freqs, a.ctl, s, true);
+    if (e != cudaSuccess) return e;
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+  }
+  // a ring of <= 144 slots with <= 32 query rows: tensor cores, the append fused
+  if (ring_tc) {
     switch (G) {
       case 1: return launch_ring_tc<1>(a, s);
       case 2: return launch_ring_tc<2>(a, s);

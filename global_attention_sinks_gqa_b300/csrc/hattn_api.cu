@@ -203,12 +203,15 @@ size_t hattn_decode_workspace_size(int B, int T, int hq, int hkv, int dv, int ma
   return decode_workspace_bytes(B, T, hq, nsplit);
 }
 
-hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_cache,
-                            const int* seqlens_k, const float* sink, void* out, float* lse, int B,
-                            int T, int hq, int hkv, int dqk, int dv, int cap, int is_ring,
-                            int window, int max_seqlen_k, int rope_dim, float rope_base,
-                            float softmax_scale, void* workspace, size_t workspace_bytes,
-                            void* stream) {
+namespace {
+
+// hattn_decode() and hattn_decode_append(): k_new / v_new null for the former.
+hattn_status_t decode_step(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                           const void* v_cache, const int* seqlens_k, const float* sink, void* out,
+                           float* lse, int B, int T, int hq, int hkv, int dqk, int dv, int cap,
+                           int is_ring, int window, int max_seqlen_k, int rope_dim,
+                           float rope_base, float softmax_scale, void* workspace,
+                           size_t workspace_bytes, void* stream) {
   hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
   if (st != HATTN_OK) return st;
   if (B < 0 || T <= 0 || cap <= 0 || window < 0 || max_seqlen_k < T ||
@@ -224,6 +227,9 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) || (reinterpret_cast<uintptr_t>(sink) & 3u) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return HATTN_ERR_INVALID_ARG;
+  const bool append = k_new != nullptr || v_new != nullptr;
+  if (append && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
     return HATTN_ERR_INVALID_ARG;
   DecodeArgs a;
   a.q = q;
@@ -244,6 +250,8 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   make_rope_freqs(rope_base, &a.freqs);
   a.nsplit = decode_num_splits(max_seqlen_k, T, window, is_ring, cap, &a.chunk);
+  a.k_new = k_new;
+  a.v_new = v_new;
   const size_t need = decode_workspace_bytes(B, T, hq, a.nsplit);
   a.part_o = nullptr;
   a.part_lse = nullptr;
@@ -257,6 +265,32 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
   if (!device_ctl(&a.ctl)) return HATTN_ERR_CUDA;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return HATTN_ERR_CUDA;
   return HATTN_OK;
+}
+
+}  // namespace
+
+hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int* seqlens_k, const float* sink, void* out, float* lse, int B,
+                            int T, int hq, int hkv, int dqk, int dv, int cap, int is_ring,
+                            int window, int max_seqlen_k, int rope_dim, float rope_base,
+                            float softmax_scale, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return decode_step(q, nullptr, nullptr, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq,
+                     hkv, dqk, dv, cap, is_ring, window, max_seqlen_k, rope_dim, rope_base,
+                     softmax_scale, workspace, workspace_bytes, stream);
+}
+
+hattn_status_t hattn_decode_append(const void* q, const void* k_new, const void* v_new,
+                                   void* k_cache, void* v_cache, const int* seqlens_k,
+                                   const float* sink, void* out, float* lse, int B, int T, int hq,
+                                   int hkv, int dqk, int dv, int cap, int is_ring, int window,
+                                   int max_seqlen_k, int rope_dim, float rope_base,
+                                   float softmax_scale, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  if (B > 0 && (!k_new || !v_new)) return HATTN_ERR_INVALID_ARG;
+  return decode_step(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv,
+                     dqk, dv, cap, is_ring, window, max_seqlen_k, rope_dim, rope_base,
+                     softmax_scale, workspace, workspace_bytes, stream);
 }
 
 hattn_status_t hattn_check_device_status(void* stream) {

@@ -42,10 +42,12 @@ int num_sms();
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
                                     cudaStream_t s);
+// Token t of sequence b goes to position start_pos[b] + t, or, with
+// from_len, to seqlens[b] - T + t (start_pos then holds seqlens).
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* start_pos,
                              void* k_cache, void* v_cache, int B, int T, int hkv, int cap,
                              int is_ring, const RopeFreqs& f, const DeviceCtl& ctl,
-                             cudaStream_t s);
+                             cudaStream_t s, bool from_len = false);
 
 // ---- prefill (prefill_tc.cu) ------------------------------------------------
 struct PrefillArgs {
@@ -83,6 +85,11 @@ struct DecodeArgs {
   float* part_lse;  // [B, hq, T, nsplit] fp32, log2 domain
   int nsplit;
   int chunk;        // keys per split
+  // Append fused into the step (hattn_decode_append): the T new tokens' K
+  // (un-rotated) and V, written into the caches before they are read.
+  // nullptr: the caches already hold them.
+  const void* k_new = nullptr;  // bf16 [B, T, hkv, dqk]
+  const void* v_new = nullptr;  // bf16 [B, T, hkv, dv]
   DeviceCtl ctl;
 };
 int decode_num_splits(int max_seqlen_k, int T, int window, int is_ring, int cap, int* chunk);

@@ -127,14 +127,15 @@ __global__ void __launch_bounds__(256) rope_keys_packed_kernel(
 __global__ void __launch_bounds__(256) kv_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int* __restrict__ start_pos, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-    int B, int T, int hkv, int cap, int is_ring, const RopeFreqs f, const DeviceCtl ctl) {
+    int B, int T, int hkv, int cap, int is_ring, const RopeFreqs f, const DeviceCtl ctl,
+    int from_len) {
   const int lane = threadIdx.x & 31;
   const long row = long(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);  // (b, t, g)
   if (row >= long(B) * T * hkv) return;
   const int g = int(row % hkv);
   const int t = int((row / hkv) % T);
   const int b = int(row / (long(hkv) * T));
-  const int pos = __ldg(start_pos + b) + t;
+  const int pos = __ldg(start_pos + b) + t - (from_len ? T : 0);
   if (pos < 0 || (!is_ring && pos >= cap)) {
     if (lane == 0) record_status(ctl, HATTN_ERR_INVALID_ARG);
     return;  // whole warp leaves together: no shuffle is pending
@@ -164,14 +165,14 @@ cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_se
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* start_pos,
                              void* k_cache, void* v_cache, int B, int T, int hkv, int cap,
                              int is_ring, const RopeFreqs& f, const DeviceCtl& ctl,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool from_len) {
   const long rows = long(B) * T * hkv;
   if (rows == 0) return cudaSuccess;
   const long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   kv_append_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), start_pos,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), B, T, hkv, cap, is_ring, f,
-      ctl);
+      ctl, from_len ? 1 : 0);
   return cudaGetLastError();
 }
 

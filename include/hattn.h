@@ -183,6 +183,35 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
 #define HATTN_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /*
+ * One whole decode / MTP-verify step of a layer: the append of the T new
+ * tokens (hattn_rope_kv_append() at positions seqlens_k[b] - T + t) and the
+ * attention of hattn_decode() over the cache that then holds them, with the
+ * same results as those two calls in that order (cache contents included).
+ * MiMo-V2-Flash paper review, section 3.1 (hybrid layers, fixed window
+ * cache); plmsmile notes, MiMo-V2-Flash "local window" (the window layer's
+ * cache is a fixed ring).
+ *
+ *   k_new, v_new  bf16 [B, T, hkv, dqk] / [B, T, hkv, dv]: the new tokens'
+ *                 un-rotated keys and their values
+ *   k_cache, v_cache  written in the T new tokens' slots, then read
+ *   every other argument as for hattn_decode()
+ *
+ * For a ring of at most 144 slots with at most 32 query rows per KV head
+ * (G * T <= 32, G in {1, 2, 4, 8}) the append runs inside the attention
+ * kernel: one launch per step.  Otherwise the append kernel runs first, on
+ * the same stream.  Errors as for the two calls; a sequence whose length
+ * fails the checks is neither appended nor attended (its output rows are
+ * not written) and HATTN_ERR_INVALID_ARG is recorded.
+ */
+hattn_status_t hattn_decode_append(const void* q, const void* k_new, const void* v_new,
+                                   void* k_cache, void* v_cache, const int* seqlens_k,
+                                   const float* sink, void* out, float* lse, int B, int T, int hq,
+                                   int hkv, int dqk, int dv, int cap, int is_ring, int window,
+                                   int max_seqlen_k, int rope_dim, float rope_base,
+                                   float softmax_scale, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
  * hattn_decode() for callers that cannot allocate device memory.  The paper
  * has no counterpart to this entry point; it exists for callers that cannot
  * call cudaMalloc -- code running inside a host framework that owns all

@@ -217,6 +217,70 @@ def test_decode_unwritten_slots_hold_nan(cap, window, T, lens):
     _decode_compare(d, cap, is_ring, f"NaN-filled cache cap={cap}", init=float("nan"))
 
 
+def _append_step(d, cap, is_ring, init=0.0):
+    """Caches holding each sequence's history before its T new tokens, and
+    those tokens' un-rotated K / V as [B, T, hkv, d]."""
+    dev = torch.device("cuda")
+    T = d.q.shape[1]
+    upto = [L - T for L in d.seqlens]
+    kc, vc = fill_cache(d, cap, is_ring, upto=upto, init=init)
+    k_new = torch.stack([d.k_hist[b, L - T:L] for b, L in enumerate(d.seqlens)]).to(dev)
+    v_new = torch.stack([d.v_hist[b, L - T:L] for b, L in enumerate(d.seqlens)]).to(dev)
+    sl = torch.tensor(d.seqlens, dtype=torch.int32, device=dev)
+    return kc, vc, k_new.contiguous(), v_new.contiguous(), sl
+
+
+@pytest.mark.parametrize("cap,window,T,G,lens", [
+    (131, 128, 4, 8, [4, 5, 100, 130, 131, 132, 500, 1000]),   # append inside the ring kernel
+    (128, 128, 1, 8, [1, 2, 127, 128, 129, 700]),
+    (130, 128, 3, 4, [3, 64, 129, 130, 131, 4000]),
+    (16, 16, 1, 2, [1, 15, 16, 17, 33]),
+    (300, 128, 4, 8, [4, 131, 299, 300, 301, 1234]),           # append kernel, then the step
+    (0, 0, 4, 16, [4, 100, 2048, 2049, 5000]),                  # linear cache
+])
+def test_decode_append_is_append_then_decode(cap, window, T, G, lens):
+    """hattn_decode_append == hattn_rope_kv_append at seqlens - T followed by
+    hattn_decode: the same cache bytes and the same outputs, bit for bit; and
+    the outputs match the oracle."""
+    is_ring = window > 0
+    cap = cap or max(lens) + 3
+    base = 1e4 if is_ring else 5e6
+    d = synth.decode_case(lens, T, G * 2, 2, window=window, rope_base=base,
+                          seed=1500 + cap + T)
+    dev = torch.device("cuda")
+    kc, vc, k_new, v_new, sl = _append_step(d, cap, is_ring)
+    kc2, vc2 = kc.clone(), vc.clone()
+    q, sink = d.q.to(dev), d.sink.to(dev)
+    kw = dict(max_seqlen_k=max(lens), window=window, is_ring=is_ring, rope_base=base,
+              softmax_scale=d.scale)
+    out, lse = ha.decode_append(q, k_new, v_new, kc, vc, sl, sink, **kw)
+    ha.rope_kv_append(k_new, v_new, sl - T, kc2, vc2, is_ring=is_ring, rope_base=base)
+    out2, lse2 = ha.decode(q, kc2, vc2, sl, sink, **kw)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2), "cache bytes differ"
+    assert torch.equal(out, out2) and torch.equal(lse, lse2), "outputs differ"
+    o_ref, l_ref = oracle.decode(d.q, d.k_hist, d.v_hist, d.seqlens, d.sink, window=window,
+                                 rope_base=base, scale=d.scale)
+    compare(out, lse, o_ref, l_ref, f"decode_append cap={cap} T={T} G={G}")
+
+
+def test_decode_append_unwritten_slots_hold_nan():
+    """The fused append over a ring whose never-written slots hold NaN."""
+    lens, T, cap = [4, 9, 60, 130, 131, 700], 4, 131
+    d = synth.decode_case(lens, T, 16, 2, window=128, rope_base=1e4, seed=1600)
+    dev = torch.device("cuda")
+    kc, vc, k_new, v_new, sl = _append_step(d, cap, True, init=float("nan"))
+    out, lse = ha.decode_append(d.q.to(dev), k_new, v_new, kc, vc, sl, d.sink.to(dev),
+                                max_seqlen_k=max(lens), window=128, is_ring=True, rope_base=1e4,
+                                softmax_scale=d.scale)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    o_ref, l_ref = oracle.decode(d.q, d.k_hist, d.v_hist, d.seqlens, d.sink, window=128,
+                                 rope_base=1e4, scale=d.scale)
+    compare(out, lse, o_ref, l_ref, "decode_append NaN-filled ring")
+
+
 @pytest.mark.parametrize("window,T", [(1, 1), (2, 2), (5, 4), (16, 1)])
 def test_decode_tiny_rings(window, T):
     cap = window + T - 1
