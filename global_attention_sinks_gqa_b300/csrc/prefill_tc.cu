@@ -335,8 +335,10 @@ __device__ __forceinline__ void load_s_row(uint32_t t_s, uint32_t (&s)[BN]) {
 // The whole key band of a unit as one block of BN columns, in two halves of
 // H1 and H2 columns (registers).  Half 1 sets the max m; half 2 is taken
 // against m unless its own max exceeds m by more than 2^8, in which case m
-// moves and half 1 is taken again (rare: the row's weights would otherwise
-// grow past 256 in bf16).  c_lo / c_hi: this row's visible columns;
+// moves and half 1's weights, already in TMEM as bf16 over S, are scaled to
+// the new max (rare: the row's weights would otherwise grow past 256 in
+// bf16; a weight scaled down by more than 2^8 keeps a relative error of
+// 2^-8, i.e. 2^-16 of the row's largest weight).  c_lo / c_hi: this row's visible columns;
 // lo_max / hi_min: the largest c_lo and smallest c_hi over the tile, which
 // decide which edges a half has to mask.  Returns m (log2 units, -inf if no
 // column is visible) and l = sum of 2^(x - m).
@@ -356,21 +358,40 @@ __device__ __forceinline__ void softmax_one(uint32_t t_s, float scale_log2, int 
     l1 = exp_pack_store<H1>(s1, scale_log2, m == -INFINITY ? 0.f : m, t_s);
   }
   bool redo;
-  float l2;
+  float l2, f1 = 1.f;
   {
     uint32_t s2[H2];
     load_s_row<H2>(t_s + H1, s2);
     mask_block<H2>(s2, lower2, upper2, c_lo - H1, c_hi - H1);
     const float m2 = fmaxf(m, row_max<H2>(s2) * scale_log2);
     redo = m2 > m + kRescaleThreshold;
-    if (redo) m = m2;
+    if (redo) {
+      f1 = fast_exp2(m - m2);  // 0 when half 1 saw no key
+      m = m2;
+    }
     l2 = exp_pack_store<H2>(s2, scale_log2, m == -INFINITY ? 0.f : m, t_s + H1 / 2);
   }
   if (__any_sync(0xffffffffu, redo)) {
-    uint32_t s1[H1];
-    load_s_row<H1>(t_s, s1);
-    mask_block<H1>(s1, lower1, upper1, c_lo, c_hi);
-    l1 = exp_pack_store<H1>(s1, scale_log2, m == -INFINITY ? 0.f : m, t_s);
+    // half 1's P (bf16 pairs in TMEM columns 0 .. H1/2 - 1) times f1
+    constexpr int NP = H1 / 2;
+    static_assert(NP % 8 == 0, "P columns in pieces of 8");
+    uint32_t pv[NP];
+    tmem_st_wait();  // half 1's P stores have landed
+#pragma unroll
+    for (int c = 0; c < NP; c += 8) tmem_ld8_nowait(t_s + c, pv + c);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c = 0; c < NP; c += 8) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        tmem_reg_fence(pv[c + e]);
+        const float2 x = unpack_bf16x2(pv[c + e]);
+        pk[e] = pack_bf16x2(x.x * f1, x.y * f1);
+      }
+      tmem_st8(t_s + c, pk);
+    }
+    l1 *= f1;
   }
   l = l1 + l2;
 }

@@ -77,6 +77,33 @@ def test_prefill_sink_stress(window, base, sink_mean, sink_std):
         assert np.abs(o0 - o_ref).max() > 0.1
 
 
+@pytest.mark.parametrize("G", [8, 16])
+def test_prefill_many_short_sequences(G):
+    """More sequences than the kernel caches offsets for, most shorter than
+    one unit of the sliding-window path."""
+    rs = np.random.RandomState(600 + G)
+    lens = [int(x) for x in rs.randint(1, 90, size=150)] + [700]
+    c = synth.prefill_case(lens, 2 * G, 2, window=128, rope_base=1e4, seed=600 + G)
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"150 short sequences G={G}")
+
+
+@pytest.mark.parametrize("G,window", [(8, 128), (16, 128), (8, 64)])
+def test_prefill_window_max_jumps_late_in_band(G, window):
+    """Each key is 0.8 x the query of its token's first head in the group, so
+    that head's rows have their largest logit (~11, against ~2 elsewhere) on
+    the diagonal, past the first half of a one-block band: the softmax moves
+    its max after half 1 has been taken and scales half 1's weights down by
+    far more than 2^8."""
+    lens = [700, 333]
+    c = synth.prefill_case(lens, 2 * G, 2, window=window, rope_base=1e4, seed=650 + G + window)
+    c.k = (0.8 * c.q.float()[:, ::G, :]).to(torch.bfloat16).contiguous()
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"growing keys G={G} W={window}")
+
+
 def test_prefill_repeatable_and_independent_of_lse_pointer():
     c = synth.prefill_case([1000, 500], 64, 8, window=128, rope_base=1e4, seed=500)
     out1, lse1 = gpu_prefill(c)
