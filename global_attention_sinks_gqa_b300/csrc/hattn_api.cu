@@ -118,7 +118,7 @@ const char* hattn_status_string(hattn_status_t s) {
 size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk) {
   if (total_tokens <= 0 || hkv <= 0 || dqk <= 0) return 0;
   const size_t bytes = size_t(total_tokens) * size_t(hkv) * size_t(dqk) * 2;
-  return (bytes + 255) / 256 * 256;
+  return (bytes + 255) / 256 * 256 + 256;  // rotated keys, then the work counter
 }
 
 hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const float* sink,
@@ -147,6 +147,11 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
   PrefillArgs a;
   a.q = q;
   a.k_rot = workspace;
+  {
+    const size_t kb = size_t(total_tokens) * size_t(hkv) * size_t(dqk) * 2;
+    a.unit_ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
+                                                 (kb + 255) / 256 * 256);
+  }
   a.v = v;
   a.sink = sink;
   a.out = out;
@@ -161,8 +166,8 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   make_rope_freqs(rope_base, &a.freqs);
   a.ctl = ctl;
-  if (launch_rope_keys_packed(k, workspace, cu_seqlens, batch, total_tokens, hkv, a.freqs, ctl, s) !=
-      cudaSuccess)
+  if (launch_rope_keys_packed(k, workspace, cu_seqlens, batch, total_tokens, hkv, a.freqs, ctl, s,
+                              a.unit_ctr) != cudaSuccess)
     return HATTN_ERR_CUDA;
   if (max_seqlen == 0) return HATTN_OK;
   if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;

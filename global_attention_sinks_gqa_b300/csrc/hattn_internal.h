@@ -39,9 +39,10 @@ bool make_map(CUtensorMap* m, const void* base, long rows, int heads, int dim, i
 int num_sms();
 
 // ---- rope / append (rope_append.cu) --------------------------------------
+// Also zeroes *unit_ctr (the prefill kernel's work counter) when non-null.
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
-                                    cudaStream_t s);
+                                    cudaStream_t s, unsigned int* unit_ctr = nullptr);
 // Token t of sequence b goes to position start_pos[b] + t, or, with
 // from_len, to seqlens[b] - T + t (start_pos then holds seqlens).
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* start_pos,
@@ -53,6 +54,7 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* st
 struct PrefillArgs {
   const void* q;
   const void* k_rot;
+  unsigned int* unit_ctr;  // work counter (zeroed by the key rotation pass)
   const void* v;
   const float* sink;
   void* out;

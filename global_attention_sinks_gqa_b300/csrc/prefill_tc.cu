@@ -159,14 +159,19 @@ __device__ __forceinline__ void reg_alloc() {
 
 constexpr int kCuCache = 128;  // batches up to 127 sequences keep cu_seqlens in shared memory
 
+constexpr int kUnitQueue = 4;          // units the producer may publish ahead
+constexpr int kUnitReaders = 1 + 8;    // the MMA issuer and the eight softmax warps
+
 template <int NSLOT>
 struct Bars {
   uint64_t q_full[2], q_ready[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+  uint64_t unit_full[kUnitQueue], unit_empty[kUnitQueue];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int unit[kUnitQueue];  // published unit indices, -1: no more
   int cu[kCuCache];
 };
 
@@ -428,6 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
     }
+    for (int i = 0; i < kUnitQueue; ++i) {
+      mbar_init(&bars->unit_full[i], 1);
+      mbar_init(&bars->unit_empty[i], kUnitReaders);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -450,6 +459,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   uint8_t* ring = smem + C::kOffRing;
   const int* cu = cu_cached ? bars->cu : a.cu_seqlens;
+  // Units are handed out by a counter in global memory, so SMs that run
+  // faster take more of them; the producer draws each unit and publishes its
+  // index in a small queue that the MMA issuer and the softmax warps read in
+  // the same order (-1: no more units).  n: queue entries read so far.
+  auto read_unit = [&](uint32_t& n, bool whole_warp) -> int {
+    const uint32_t q = n % kUnitQueue, ph = (n / kUnitQueue) & 1u;
+    const bool ok = whole_warp ? warp_wait(&bars->unit_full[q], ph, a.ctl, abort)
+                               : mbar_wait(&bars->unit_full[q], ph, a.ctl, abort);
+    if (!ok) return -1;
+    const int u = bars->unit[q];
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || lane == 0) mbar_arrive(&bars->unit_empty[q]);
+    ++n;
+    return u;
+  };
 
   if (warp < 4) {
     reg_dealloc<kRegsLow>();  // one instruction for all of warpgroup 0
@@ -468,9 +492,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pos;
         return true;
       };
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      uint32_t pn = 0;  // queue entries published
+      while (ok) {
+        // draw the next unit that holds a query, publish it (or the end)
+        const uint32_t q = pn % kUnitQueue;
+        if (pn >= uint32_t(kUnitQueue) &&
+            !mbar_wait(&bars->unit_empty[q], ((pn / kUnitQueue) & 1u) ^ 1u, a.ctl, abort))
+          break;
         UnitInfo ui;
-        if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
+        int u;
+        do {
+          u = int(atomicAdd(a.unit_ctr, 1u));
+        } while (u < nunits && !unit_info<G, BN, WIN>(u, a, cu, nut, ui));
+        if (u >= nunits) u = -1;
+        bars->unit[q] = u;
+        mbar_arrive(&bars->unit_full[q]);
+        ++pn;
+        if (u < 0) break;
         const int row0 = ui.tok0 + ui.kstart;
         // K_0 first (its slots free up while the previous unit finishes), then
         // the two Q tiles, then V_0, K_1, V_1, ...
@@ -573,9 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one key block per unit: S_t = Q_t K^T once O_t (over S_t's upper
         // columns) has been read by the previous unit's epilogue, then
         // O_t = P_t V
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        uint32_t rn = 0;
+        while (ok) {
+          const int u = read_unit(rn, false);
+          if (u < 0) break;
           UnitInfo ui;
-          if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
+          unit_info<G, BN, WIN>(u, a, cu, nut, ui);
           const uint32_t k0 = pos;
           pos += 3;
           if (!wait_slots(k0, 3)) break;
@@ -605,10 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           release_slots(vp, 2);
           ++uc;
         }
-      } else
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      } else {
+      uint32_t rn = 0;
+      while (ok) {
+        const int u = read_unit(rn, false);
+        if (u < 0) break;
         UnitInfo ui;
-        if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
+        unit_info<G, BN, WIN>(u, a, cu, nut, ui);
         const uint32_t k0 = pos;
         pos += 3;
         if (!wait_slots(k0, 3)) break;
@@ -650,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++uc;
       }
+      }
       // every MMA issued must be complete before TMEM is released
       umma_commit(&bars->drain);
       mbar_wait_drain(&bars->drain, 0, a.ctl);
@@ -685,7 +730,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float l_tot = pl * fo + exp2f(psink - msub);
       const float inv = fo / l_tot;
       const uint64_t inv2 = f2_pack(inv, inv);
-      uint8_t* orow_ptr = static_cast<uint8_t*>(a.out) + porow * 256;
+      // O leaves TMEM first (scaled, packed to bf16 in registers), so O_t's
+      // columns go back to the MMA before the stores, whose drain then
+      // overlaps the next unit's QK^T
+      uint32_t pk[64];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {  // 64 columns in flight per wait
         uint32_t v[64];
@@ -694,36 +742,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 64; ++e) tmem_reg_fence(v[e]);
-        uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float2 y = f2_unpack(
               f2_mul(f2_pack(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), inv2));
-          pk[e] = pack_bf16x2(y.x, y.y);
-        }
-        if (pvalid) {
-          uint8_t* dst = orow_ptr + half * 128;
-          if (out32) {  // 32-byte stores: one full sector each
-#pragma unroll
-            for (int e = 0; e < 4; ++e) st_global_v8(dst + 32 * e, pk + 8 * e);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              reinterpret_cast<uint4*>(dst)[e] =
-                  make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-          }
+          pk[32 * half + e] = pack_bf16x2(y.x, y.y);
         }
       }
-      if (pvalid && a.lse != nullptr) a.lse[porow] = (msub + log2f(l_tot)) * kLn2;
       tc_fence_before();
       mbar_arrive(&bars->o_free[t]);
+      if (pvalid) {
+        uint8_t* dst = static_cast<uint8_t*>(a.out) + porow * 256;
+        if (out32) {  // 32-byte stores: one full sector each
+#pragma unroll
+          for (int e = 0; e < 8; ++e) st_global_v8(dst + 32 * e, pk + 8 * e);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            reinterpret_cast<uint4*>(dst)[e] =
+                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+        if (a.lse != nullptr) a.lse[porow] = (msub + log2f(l_tot)) * kLn2;
+      }
       return true;
     };
 
     bool ok = true;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    uint32_t rn = 0;
+    while (true) {
+      const int u = read_unit(rn, true);
+      if (u < 0) {
+        ok = !*abort;
+        break;
+      }
       UnitInfo ui;
-      if (!unit_info<G, BN, WIN>(u, a, cu, nut, ui)) continue;
+      unit_info<G, BN, WIN>(u, a, cu, nut, ui);
       if (!warp_wait(&bars->q_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
       const int qmin = ui.t0 + t * TQ;           // first token of this tile
       const int qpos = qmin + tl;

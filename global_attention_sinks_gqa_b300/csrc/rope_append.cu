@@ -79,8 +79,10 @@ constexpr int kTokWarps = 8;
 
 __global__ void __launch_bounds__(256) rope_keys_packed_kernel(
     const uint4* __restrict__ k, uint4* __restrict__ k_rot, const int* __restrict__ cu_seqlens,
-    int batch, long total, int hkv, const RopeFreqs f, const DeviceCtl ctl) {
+    int batch, long total, int hkv, const RopeFreqs f, const DeviceCtl ctl,
+    unsigned int* __restrict__ unit_ctr) {
   __shared__ float2 cs_tab[kTokWarps][32];
+  if (unit_ctr != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *unit_ctr = 0u;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const long nchunks = long(hkv) * 24;
   bool overflow = false;
@@ -151,14 +153,14 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
 
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, unsigned int* unit_ctr) {
   if (total == 0) return cudaSuccess;
   long blocks = (total + kTokWarps - 1) / kTokWarps;
   const long cap_blocks = long(num_sms()) * 8;  // grid-stride beyond 8 blocks per SM
   if (blocks > cap_blocks) blocks = cap_blocks;
   rope_keys_packed_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
       static_cast<const uint4*>(k), static_cast<uint4*>(k_rot), cu_seqlens, batch, total, hkv, f,
-      ctl);
+      ctl, unit_ctr);
   return cudaGetLastError();
 }
 

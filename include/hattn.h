@@ -75,7 +75,9 @@ const char* hattn_status_string(hattn_status_t status);
 
 /*
  * Bytes of workspace hattn_prefill() needs: the rotated keys,
- * total_tokens * hkv * dqk 16-bit values, rounded up to 256 bytes.
+ * total_tokens * hkv * dqk 16-bit values, rounded up to 256 bytes, then 256
+ * bytes for the attention kernel's work counter (both rewritten by every
+ * call: a workspace serves one call at a time).
  */
 size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk);
 

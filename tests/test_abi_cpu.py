@@ -42,8 +42,9 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    assert ha.hattn_prefill_workspace_size(32768, 8, 192) == 32768 * 8 * 192 * 2
-    assert ha.hattn_prefill_workspace_size(3, 1, 192) == 1280  # 1152 rounded to 256
+    # rotated keys rounded to 256 bytes, then 256 bytes of work counter
+    assert ha.hattn_prefill_workspace_size(32768, 8, 192) == 32768 * 8 * 192 * 2 + 256
+    assert ha.hattn_prefill_workspace_size(3, 1, 192) == 1280 + 256  # 1152 rounded to 256
     # a ring window fits one chunk: no workspace
     assert ha.hattn_decode_workspace_size(64, 4, 64, 8, 128, 65536, 128, 131, 1) == 0
     n = ha.hattn_decode_workspace_size(64, 4, 64, 4, 128, 65536, 0, 65536, 0)
