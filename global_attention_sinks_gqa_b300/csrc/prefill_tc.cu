@@ -510,9 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pn;
         if (u < 0) break;
         const int row0 = ui.tok0 + ui.kstart;
-        // K_0 first (its slots free up while the previous unit finishes), then
-        // the two Q tiles, then V_0, K_1, V_1, ...
-        for (int i = 0; i < 3 && ok; ++i) ok = load_box(&mapK, 64 * i, ui.g, row0);
+        // Several blocks: K_0 first (its slots free up while the previous
+        // unit finishes), then the two Q tiles, then V_0, K_1, V_1, ...  One
+        // block: the Q tiles first -- a tile's buffer frees with its S MMA of
+        // the previous unit and its RoPE heads the tile's next chain -- then
+        // K_0, V_0.
+        if constexpr (!ONE)
+          for (int i = 0; i < 3 && ok; ++i) ok = load_box(&mapK, 64 * i, ui.g, row0);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -528,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ui.tok0 + ui.t0 + t * TQ);
           ++qf;
         }
+        if constexpr (ONE)
+          for (int i = 0; i < 3 && ok; ++i) ok = load_box(&mapK, 64 * i, ui.g, row0);
         for (int j = 0; j < ui.nblk && ok; ++j) {
           for (int i = 0; i < 2 && ok; ++i) ok = load_box(&mapV, 64 * i, ui.g, row0 + j * BN);
           if (j + 1 < ui.nblk)
