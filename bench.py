@@ -258,7 +258,8 @@ class Workload:
         assert st == 0, ha.status_string(st)
         # a ring of <= 144 slots with <= 32 rows per KV head runs the append
         # inside the attention kernel; otherwise the append kernel goes first
-        fused = dd["ring"] and dd["cap"] <= 144 and (p["hq"] // p["hkv"]) * self.T <= 32
+        fused = (dd["ring"] and dd["cap"] <= 144 and self.T <= 4
+                 and (p["hq"] // p["hkv"]) * self.T <= 32)
         return (1 if fused else 2) + (1 if dd["ws_n"] else 0)
 
     def flops(self):

@@ -15,8 +15,8 @@
 // into chunks of `chunk` keys; a ring's slots are split the same way (the key
 // position of slot s is the one position of the last `cap` that is congruent
 // to s).  The kernel is persistent: one CTA per SM walks the items
-// round-robin.  The G*T <= 64 rows sit in a 128-row tile whose other rows are
-// zero, so QK^T and PV are plain M=128 tensor-core products; the step is
+// round-robin.  The G*T <= 128 rows sit in a 128-row tile whose other rows
+// are zero, so QK^T and PV are plain M=128 tensor-core products; the step is
 // bound by streaming the cache, not by the multiply.
 //
 // CTA roles (192 threads):
@@ -1578,8 +1578,9 @@ size_t decode_workspace_bytes(int B, int T, int hq, int nsplit) {
 cudaError_t launch_decode(const DecodeArgs& a_in, cudaStream_t s) {
   DecodeArgs a = a_in;
   const int G = a.hq / a.hkv;
-  const bool ring_tc = a.is_ring && a.cap <= kRingTcMaxCap && a.nsplit == 1 && G * a.T <= 32 &&
-                       (G == 1 || G == 2 || G == 4 || G == 8);
+  // (its per-worker tables and its share of the append assume T <= 4)
+  const bool ring_tc = a.is_ring && a.cap <= kRingTcMaxCap && a.nsplit == 1 && a.T <= 4 &&
+                       G * a.T <= 32 && (G == 1 || G == 2 || G == 4 || G == 8);
   if (a.k_new && !ring_tc) {
     // the append as its own launch ahead of the step
     cudaError_t e = launch_kv_append(a.k_new, a.v_new, a.seqlens, const_cast<void*>(a.k_cache),
@@ -1600,7 +1601,7 @@ cudaError_t launch_decode(const DecodeArgs& a_in, cudaStream_t s) {
     }
   }
   // a ring small enough to sit in shared memory whole: one CTA per item
-  if (a.is_ring && a.cap <= kRingMaxCap && a.nsplit == 1) {
+  if (a.is_ring && a.cap <= kRingMaxCap && a.nsplit == 1 && G * a.T <= 64) {
     const int rows = G * a.T;
     if (rows <= 16) return launch_ring<1>(a, s);
     if (rows <= 32) return launch_ring<2>(a, s);

@@ -222,7 +222,7 @@ hattn_status_t decode_step(const void* q, const void* k_new, const void* v_new, 
   if (B < 0 || T <= 0 || cap <= 0 || window < 0 || max_seqlen_k < T ||
       (is_ring != 0 && is_ring != 1))
     return HATTN_ERR_INVALID_ARG;
-  if (T > 4 || (hq / hkv) * T > 64) return HATTN_ERR_UNSUPPORTED;
+  if (T > 8 || (hq / hkv) * T > 128) return HATTN_ERR_UNSUPPORTED;
   if (is_ring && window == 0) return HATTN_ERR_INVALID_ARG;  // a ring only holds a window
   if (is_ring && cap < window + T - 1) return HATTN_ERR_RING_TOO_SMALL;
   if (!is_ring && max_seqlen_k > cap) return HATTN_ERR_INVALID_ARG;

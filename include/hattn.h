@@ -161,7 +161,8 @@ size_t hattn_decode_workspace_size(int B, int T, int hq, int hkv, int dv, int ma
  *   sink       fp32 [hq]
  *   out        bf16 [B, T, hq, dv]     written
  *   lse        fp32 [B, T, hq]         written (may be NULL)
- *   T          1..4 query tokens per sequence
+ *   T          1..8 query tokens per sequence, with (hq / hkv) * T <= 128
+ *              (else HATTN_ERR_UNSUPPORTED)
  *   is_ring    1: key j lives in slot j % cap and cap >= window + T - 1 is
  *              required (else HATTN_ERR_RING_TOO_SMALL); needs window > 0.
  *              0: key j lives in slot j.
@@ -199,7 +200,7 @@ hattn_status_t hattn_decode(const void* q, const void* k_cache, const void* v_ca
  *   every other argument as for hattn_decode()
  *
  * For a ring of at most 144 slots with at most 32 query rows per KV head
- * (G * T <= 32, G in {1, 2, 4, 8}) the append runs inside the attention
+ * (T <= 4, G * T <= 32, G in {1, 2, 4, 8}) the append runs inside the attention
  * kernel: one launch per step.  Otherwise the append kernel runs first, on
  * the same stream.  Errors as for the two calls; a sequence whose length
  * fails the checks is neither appended nor attended (its output rows are

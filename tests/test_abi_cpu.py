@@ -102,7 +102,7 @@ def _decode(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(cap=130), ha.HATTN_ERR_RING_TOO_SMALL),          # needs W + T - 1 = 131
     (dict(cap=127, T=1), ha.HATTN_ERR_RING_TOO_SMALL),
-    (dict(T=5), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(T=9, cap=136), ha.HATTN_ERR_UNSUPPORTED),          # up to 8 tokens per step
     (dict(T=0), ha.HATTN_ERR_INVALID_ARG),
     (dict(is_ring=1, window=0), ha.HATTN_ERR_INVALID_ARG),
     (dict(is_ring=0, window=0, hkv=4, cap=1000, max_seqlen_k=2000), ha.HATTN_ERR_INVALID_ARG),

@@ -197,7 +197,7 @@ def _decode_compare(d, cap, is_ring, what, init=0.0):
     return compare(out, lse, o_ref, l_ref, what)
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 4])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 6, 8])
 @pytest.mark.parametrize("G", [1, 8, 16])
 def test_decode_swa_ring(T, G):
     lens = [T, T + 1, 100, 130, 131, 132, 500, 1000]
@@ -205,7 +205,7 @@ def test_decode_swa_ring(T, G):
     _decode_compare(d, 128 + T - 1, True, f"swa ring T={T} G={G}")
 
 
-@pytest.mark.parametrize("T", [1, 4])
+@pytest.mark.parametrize("T", [1, 4, 8])
 @pytest.mark.parametrize("G", [4, 16])
 def test_decode_ga_linear_multi_chunk(T, G):
     lens = [T, 64, 1023, 1024, 1025, 2048, 2049, 5000]  # 1 to 3 chunks of 2048
@@ -262,6 +262,8 @@ def _append_step(d, cap, is_ring, init=0.0):
     (128, 128, 1, 8, [1, 2, 127, 128, 129, 700]),
     (130, 128, 3, 4, [3, 64, 129, 130, 131, 4000]),
     (16, 16, 1, 2, [1, 15, 16, 17, 33]),
+    (135, 128, 8, 4, [8, 9, 134, 135, 136, 900]),              # 8 tokens, 32 rows: ring kernel
+    (135, 128, 8, 16, [8, 9, 134, 135, 136, 900]),             # 128 rows: the general kernel
     (300, 128, 4, 8, [4, 131, 299, 300, 301, 1234]),           # append kernel, then the step
     (0, 0, 4, 16, [4, 100, 2048, 2049, 5000]),                  # linear cache
 ])
