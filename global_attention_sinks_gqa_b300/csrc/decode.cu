@@ -69,12 +69,17 @@ constexpr int kChunkLong = 4096;       // and beyond
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kOffStage % 1024 == 0 && kBox % 1024 == 0, "swizzle atoms must be 1024-byte aligned");
 
+constexpr int kItemQueue = 4;        // items the producer may publish ahead
+constexpr int kItemReaders = 1 + 4;  // the MMA issuer and the four row warps
+
 struct Bars {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_ready[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done, o_free, drain;
+  uint64_t item_full[kItemQueue], item_empty[kItemQueue];
   uint32_t tmem_base;
   int abort;
+  int item[kItemQueue];  // published virtual item indices, -1: no more
 };
 
 // Slots of the cache a work item covers.  Linear cache: the visible positions
@@ -183,6 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
+    for (int i = 0; i < kItemQueue; ++i) {
+      mbar_init(&bars->item_full[i], 1);
+      mbar_init(&bars->item_empty[i], kItemReaders);
+    }
     bars->abort = 0;
   }
   if (threadIdx.x == 0) mbar_fence_init();
@@ -199,15 +208,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Items are drawn from a work counter in the workspace when there is one
+  // (split caches: SMs that run faster take more items), else round-robin;
+  // the producer publishes each item in a small queue that the MMA issuer and
+  // the row warps read in the same order (-1: no more).  n: entries read.
+  auto read_item = [&](uint32_t& n, bool whole_warp) -> int {
+    const uint32_t q = n % kItemQueue, ph = (n / kItemQueue) & 1u;
+    const bool ok = whole_warp ? warp_wait(&bars->item_full[q], ph, a.ctl, abort)
+                               : mbar_wait(&bars->item_full[q], ph, a.ctl, abort);
+    if (!ok) return -1;
+    const int v = bars->item[q];
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || lane == 0) mbar_arrive(&bars->item_empty[q]);
+    ++n;
+    return v;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t pos = 0;
       bool ok = true;
-      for (int v = blockIdx.x; v < nvirt && ok; v += gridDim.x) {
+      uint32_t pn = 0;  // queue entries published
+      int next_static = blockIdx.x;
+      while (ok) {
+        const uint32_t q = pn % kItemQueue;
+        if (pn >= uint32_t(kItemQueue) &&
+            !mbar_wait(&bars->item_empty[q], ((pn / kItemQueue) & 1u) ^ 1u, a.ctl, abort))
+          break;
         Item it;
-        if (item_info(v, a, it) != 1) continue;
+        int v;
+        while (true) {
+          if (a.item_ctr != nullptr) {
+            v = int(atomicAdd(a.item_ctr, 1u));
+          } else {
+            v = next_static;
+            next_static += gridDim.x;
+          }
+          if (v >= nvirt) break;
+          const int st_item = item_info(v, a, it);
+          if (st_item == 1) break;
+          if (st_item < 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+        }
+        if (v >= nvirt) v = -1;
+        bars->item[q] = v;
+        mbar_arrive(&bars->item_full[q]);
+        ++pn;
+        if (v < 0) break;
         const int plane = it.b * a.hkv + it.kvh;
         const int nb = (it.s_end - it.s_beg + kBK - 1) / kBK;
         for (int blk = 0; blk < nb; ++blk, ++pos) {
@@ -273,9 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars->empty[st]);  // K and V of this block are consumed
         return true;
       };
-      for (int v = blockIdx.x; v < nvirt && ok; v += gridDim.x) {
+      uint32_t rn = 0;
+      while (ok) {
+        const int v = read_item(rn, false);
+        if (v < 0) break;
         Item it;
-        if (item_info(v, a, it) != 1) continue;
+        item_info(v, a, it);
         const uint32_t qb = qc & 1u;
         if (!mbar_wait(&bars->q_ready[qb], (qc >> 1) & 1u, a.ctl, abort)) break;
         ++qc;
@@ -375,13 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    for (int v = blockIdx.x; v < nvirt; v += gridDim.x) {
-      Item it;
-      const int st_item = item_info(v, a, it);
-      if (st_item != 1) {
-        if (st_item < 0 && warp == 2 && lane == 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
-        continue;
+    uint32_t rn = 0;
+    while (true) {
+      const int v = read_item(rn, true);
+      if (v < 0) {
+        ok = ok && !*abort;
+        break;
       }
+      Item it;
+      item_info(v, a, it);
       // ---- Q: this row from global memory, RoPE on dims 0..63 in registers
       // (pairs (i, i + 32); the G lanes holding one token's heads each
       // evaluate 32/G of the 32 angles and exchange them by shuffles), into
@@ -1541,6 +1593,10 @@ cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const long nvirt = long(a.nsplit) * a.B * a.hkv;
   const int grid = int(nvirt < num_sms() ? nvirt : num_sms());
+  if (a.item_ctr != nullptr) {
+    cudaError_t e = cudaMemsetAsync(a.item_ctr, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+  }
   kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, a, int(nvirt));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.nsplit == 1) return e;
@@ -1572,7 +1628,8 @@ size_t decode_workspace_bytes(int B, int T, int hq, int nsplit) {
   const size_t rows = size_t(B) * hq * T * nsplit;
   const size_t o_bytes = rows * kDv * sizeof(float);
   const size_t l_bytes = rows * sizeof(float);
-  return ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
+  // partial O, partial lse, then the kernel's work counter
+  return ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256 + 256;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a_in, cudaStream_t s) {

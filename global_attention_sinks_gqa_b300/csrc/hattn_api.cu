@@ -263,9 +263,12 @@ hattn_status_t decode_step(const void* q, const void* k_new, const void* v_new, 
   if (need) {
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return HATTN_ERR_WORKSPACE;
     const size_t rows = size_t(B) * hq * T * a.nsplit;
+    const size_t o_bytes = (rows * kDv * sizeof(float) + 255) / 256 * 256;
+    const size_t l_bytes = (rows * sizeof(float) + 255) / 256 * 256;
     a.part_o = static_cast<float*>(workspace);
-    a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                          (rows * kDv * sizeof(float) + 255) / 256 * 256);
+    a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + o_bytes);
+    a.item_ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + o_bytes +
+                                                 l_bytes);
   }
   if (!device_ctl(&a.ctl)) return HATTN_ERR_CUDA;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return HATTN_ERR_CUDA;

@@ -90,6 +90,7 @@ struct DecodeArgs {
   // Append fused into the step (hattn_decode_append): the T new tokens' K
   // (un-rotated) and V, written into the caches before they are read.
   // nullptr: the caches already hold them.
+  unsigned int* item_ctr = nullptr;  // work counter in the workspace (nsplit > 1)
   const void* k_new = nullptr;  // bf16 [B, T, hkv, dqk]
   const void* v_new = nullptr;  // bf16 [B, T, hkv, dv]
   DeviceCtl ctl;

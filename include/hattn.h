@@ -142,6 +142,9 @@ hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const 
  * as the hattn_decode() call (0 when one pass per KV head suffices: a
  * window or ring of at most 1024 keys).  A linear cache is cut into chunks
  * of 2048 keys (4096 beyond 16K keys); a ring into chunks of its cap slots.
+ * The workspace holds the chunks' partial O and lse and 256 bytes for the
+ * kernel's work counter (zeroed by every call: a workspace serves one call
+ * at a time).
  */
 size_t hattn_decode_workspace_size(int B, int T, int hq, int hkv, int dv, int max_seqlen_k,
                                    int window, int cap, int is_ring);

@@ -47,12 +47,13 @@ def test_workspace_sizes(lib):
     assert ha.hattn_prefill_workspace_size(3, 1, 192) == 1280 + 256  # 1152 rounded to 256
     # a ring window fits one chunk: no workspace
     assert ha.hattn_decode_workspace_size(64, 4, 64, 8, 128, 65536, 128, 131, 1) == 0
+    # partial O and lse (each rounded to 256 bytes), then 256 bytes of work counter
     n = ha.hattn_decode_workspace_size(64, 4, 64, 4, 128, 65536, 0, 65536, 0)
     rows = 64 * 64 * 4 * 16  # 16 chunks of 4096 keys (caches beyond 16K keys)
-    assert n == rows * 128 * 4 + rows * 4
+    assert n == rows * 128 * 4 + rows * 4 + 256
     n = ha.hattn_decode_workspace_size(8, 4, 64, 4, 128, 10000, 0, 10000, 0)
     rows = 8 * 64 * 4 * 5  # 5 chunks of 2048 keys
-    assert n == rows * 128 * 4 + rows * 4
+    assert n == rows * 128 * 4 + rows * 4 + 256
     # a ring is cut by its capacity, not by the window
     assert ha.hattn_decode_workspace_size(2, 1, 16, 1, 128, 9000, 1000, 3000, 1) > 0
     assert ha.hattn_decode_workspace_size(2, 1, 16, 1, 128, 9000, 1000, 1000, 1) == 0
