@@ -585,6 +585,75 @@ def run_hybrid_block(args):
             "parts": parts, "clocks": clk.summary()}
 
 
+def run_prefix_prefill(args):
+    """Prefill over a cached prefix: a global layer (64q/4kv, base 5e6) whose
+    cache already holds 28672 tokens receives 4096 new ones (append + attention,
+    one hattn_prefill_cached call per step)."""
+    import global_attention_sinks_gqa_b300 as ha
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    P, S = 28672, 4096
+    p = synth.CONFIGS["ga_prefill_32k"]
+    hq, hkv, base = p["hq"], p["hkv"], p["rope_base"]
+    g = synth._gen(7, dev)
+    q = synth.randn_bf16((S, hq, D_QK), g, dev)
+    k_new = synth.randn_bf16((S, hkv, D_QK), g, dev)
+    v_new = synth.randn_bf16((S, hkv, D_V), g, dev)
+    sink = synth.randn_f32((hq,), g, dev)
+    cap = P + S + 256
+    kc = torch.empty((1, hkv, cap, D_QK), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty((1, hkv, cap, D_V), dtype=torch.bfloat16, device=dev)
+    for s0 in range(0, P, 4096):  # the prefix, written by the append kernel
+        kp = synth.randn_bf16((1, 4096, hkv, D_QK), g, dev)
+        vp = synth.randn_bf16((1, 4096, hkv, D_V), g, dev)
+        ha.rope_kv_append(kp, vp, torch.tensor([s0], dtype=torch.int32, device=dev), kc, vc,
+                          is_ring=False, rope_base=base)
+    cu = torch.tensor([0, S], dtype=torch.int32, device=dev)
+    pre = torch.tensor([P], dtype=torch.int32, device=dev)
+    out = torch.empty((S, hq, D_V), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((S, hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    sptr = torch.cuda.current_stream(dev).cuda_stream
+
+    def step():
+        st = ha.hattn_prefill_cached(q, k_new, v_new, kc, vc, cu, pre, sink, out, lse, 1, S, S,
+                                     P, cap, hq, hkv, D_QK, D_V, R, base, 0,
+                                     1.0 / math.sqrt(D_QK), ws, ws.numel(), sptr)
+        assert st == 0, ha.status_string(st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        start.record()
+        for _ in range(args.steps):
+            step()
+        stop.record()
+        torch.cuda.synchronize()
+    ha.check_device_status()
+    ms = start.elapsed_time(stop) / args.steps
+    hbm, tf_burst, tf_sust, src = measured_peaks()
+    pairs = S * P + S * (S + 1) // 2
+    flops = PAIR_FLOPS * hq * pairs
+    byts = (S * (hq * D_QK * 2 + hkv * (D_QK + D_V) * 2 * 2 + hq * D_V * 2 + hq * 4)
+            + P * hkv * (D_QK + D_V) * 2 + hq * 4)
+    t = ms / 1e3
+    return {"metric": METRIC, "value": round(flops / t / 1e12, 3), "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks)",
+            "config": {"workload": "prefix_prefill: global layer (64q/4kv, base 5e6), 4096 new "
+                                   "tokens over a cached prefix of 28672"},
+            "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 2),
+                         "peak": tf_sust, "unit": "TFLOP/s",
+                         "frac": round(flops / t / 1e12 / tf_sust, 4), "traffic": None,
+                         "peak_source": f"{src} bf16_tflops_sustained"},
+            "algorithmic": {"flops": flops, "bytes": byts}, "clocks": clk.summary()}
+
+
 def run_profile_case(args):
     """One call of one part of the step at a chosen size, for an ncu capture:
     a warm-up call, then the profiled call inside the NVTX range "profile"."""
@@ -648,14 +717,19 @@ def main():
                     help="swa_prefill | ga_prefill | decode_swa | decode_ga: one call, for ncu")
     ap.add_argument("--seq", type=int, default=0, help="prefill length for --profile-case")
     ap.add_argument("--batch", type=int, default=0, help="decode batch for --profile-case")
-    ap.add_argument("--workload", default="step", choices=["step", "hybrid_block_256k"],
-                    help="step: the default bench step; hybrid_block_256k: config 5 alone")
+    ap.add_argument("--workload", default="step",
+                    choices=["step", "hybrid_block_256k", "prefix_prefill"],
+                    help="step: the default bench step; hybrid_block_256k: config 5 alone; "
+                         "prefix_prefill: 4096 new tokens over a cached 28672-token prefix")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
         return
     if args.workload == "hybrid_block_256k":
         print(json.dumps(run_hybrid_block(args)))
+        return
+    if args.workload == "prefix_prefill":
+        print(json.dumps(run_prefix_prefill(args)))
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -42,6 +42,8 @@ SIGNATURES = {
     "hattn_prefill_workspace_size": (_Z, [_L, _I, _I]),
     "hattn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _L, _I, _I, _I, _I, _I, _I, _F, _I, _F,
                            _P, _Z, _P]),
+    "hattn_prefill_cached": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _I,
+                                  _I, _I, _I, _I, _F, _I, _F, _P, _Z, _P]),
     "hattn_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "hattn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "hattn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -120,6 +122,18 @@ def hattn_prefill(q, k, v, sink, out, lse, batch, cu_seqlens, total_tokens, max_
         int(total_tokens), int(max_seqlen), int(hq), int(hkv), int(dqk), int(dv), int(rope_dim),
         float(rope_base), int(window), float(softmax_scale), _ptr(workspace), int(workspace_bytes),
         _stream(stream))
+
+
+def hattn_prefill_cached(q, k_new, v_new, k_cache, v_cache, cu_seqlens, prefix_lens, sink, out,
+                         lse, batch, total_tokens, max_seqlen, max_prefix, cap, hq, hkv, dqk, dv,
+                         rope_dim, rope_base, window, softmax_scale, workspace, workspace_bytes,
+                         stream=None) -> int:
+    return load_library().hattn_prefill_cached(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens),
+        _ptr(prefix_lens), _ptr(sink), _ptr(out), _ptr(lse), int(batch), int(total_tokens),
+        int(max_seqlen), int(max_prefix), int(cap), int(hq), int(hkv), int(dqk), int(dv),
+        int(rope_dim), float(rope_base), int(window), float(softmax_scale), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
 
 
 def hattn_rope_kv_append(k_new, v_new, start_pos, k_cache, v_cache, B, T, hkv, dqk, dv, cap,
@@ -204,6 +218,31 @@ def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_bas
     _check(hattn_prefill(q, k, v, sink, out, lse, cu_seqlens.numel() - 1, cu_seqlens, total,
                          max_seqlen, hq, hkv, dqk, dv, ROPE_DIM, rope_base, window, softmax_scale,
                          workspace, workspace.numel()), "hattn_prefill")
+    return out, lse
+
+
+def prefill_cached(q, k_new, v_new, k_cache, v_cache, cu_seqlens, prefix_lens, sink, *,
+                   max_seqlen: int, max_prefix: int, window: int, rope_base: float,
+                   softmax_scale: float | None = None, out=None, lse=None, workspace=None,
+                   with_lse: bool = True):
+    """Prefill of new tokens that continue cached prefixes (linear caches); the new
+    keys / values are appended to the caches.  Returns (out, lse)."""
+    total, hq, dqk = q.shape
+    hkv, dv = k_new.shape[1], v_new.shape[2]
+    cap = k_cache.shape[2]
+    if softmax_scale is None:
+        softmax_scale = dqk ** -0.5
+    if out is None:
+        out = torch.empty((total, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((total, hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=q.device)
+    _check(hattn_prefill_cached(q, k_new, v_new, k_cache, v_cache, cu_seqlens, prefix_lens, sink,
+                                out, lse, cu_seqlens.numel() - 1, total, max_seqlen, max_prefix,
+                                cap, hq, hkv, dqk, dv, ROPE_DIM, rope_base, window,
+                                softmax_scale, workspace, workspace.numel()),
+           "hattn_prefill_cached")
     return out, lse
 
 

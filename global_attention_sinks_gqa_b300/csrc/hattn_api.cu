@@ -174,6 +174,64 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
   return HATTN_OK;
 }
 
+hattn_status_t hattn_prefill_cached(const void* q, const void* k_new, const void* v_new,
+                                    void* k_cache, void* v_cache, const int* cu_seqlens,
+                                    const int* prefix_lens, const float* sink, void* out,
+                                    float* lse, int batch, long total_tokens, int max_seqlen,
+                                    int max_prefix, int cap, int hq, int hkv, int dqk, int dv,
+                                    int rope_dim, float rope_base, int window,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
+  if (st != HATTN_OK) return st;
+  if (batch <= 0 || total_tokens < 0 || max_seqlen < 0 || max_prefix < 0 || window < 0 ||
+      cap <= 0)
+    return HATTN_ERR_INVALID_ARG;
+  if (total_tokens > 2147483647L || max_seqlen > total_tokens) return HATTN_ERR_INVALID_ARG;
+  if (!finite_positive(rope_base) || !finite_positive(softmax_scale)) return HATTN_ERR_INVALID_ARG;
+  if (total_tokens == 0) return HATTN_OK;
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !cu_seqlens || !prefix_lens || !sink ||
+      !out)
+    return HATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+    return HATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(sink) & 3u || reinterpret_cast<uintptr_t>(lse) & 3u ||
+      reinterpret_cast<uintptr_t>(cu_seqlens) & 3u || reinterpret_cast<uintptr_t>(prefix_lens) & 3u)
+    return HATTN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < 256) return HATTN_ERR_WORKSPACE;
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrefillArgs a;
+  a.q = q;
+  a.k_rot = k_cache;
+  a.unit_ctr = static_cast<unsigned int*>(workspace);
+  a.v = v_cache;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.cu_seqlens = cu_seqlens;
+  a.batch = batch;
+  a.total = total_tokens;
+  a.max_seqlen = max_seqlen;
+  a.hq = hq;
+  a.hkv = hkv;
+  // a window covering every key of every sequence is global
+  a.window = long(window) >= long(max_prefix) + max_seqlen ? 0 : window;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  make_rope_freqs(rope_base, &a.freqs);
+  a.ctl = ctl;
+  a.prefix = prefix_lens;
+  a.cap = cap;
+  if (launch_kv_append_packed(k_new, v_new, cu_seqlens, prefix_lens, k_cache, v_cache, batch,
+                              total_tokens, hkv, cap, a.freqs, ctl, a.unit_ctr, s) != cudaSuccess)
+    return HATTN_ERR_CUDA;
+  if (max_seqlen == 0) return HATTN_OK;
+  if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;
+  return HATTN_OK;
+}
+
 hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const int* start_pos,
                                     void* k_cache, void* v_cache, int B, int T, int hkv, int dqk,
                                     int dv, int cap, int is_ring, int rope_dim, float rope_base,

@@ -50,6 +50,14 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* st
                              int is_ring, const RopeFreqs& f, const DeviceCtl& ctl,
                              cudaStream_t s, bool from_len = false);
 
+// Packed new tokens of sequence b to slots prefix[b] + t of a linear cache;
+// also zeroes V slots [end, end + 256) past each sequence's new end and
+// *unit_ctr (see rope_append.cu).
+cudaError_t launch_kv_append_packed(const void* k_new, const void* v_new, const int* cu_seqlens,
+                                    const int* prefix, void* k_cache, void* v_cache, int batch,
+                                    long total, int hkv, int cap, const RopeFreqs& f,
+                                    const DeviceCtl& ctl, unsigned int* unit_ctr, cudaStream_t s);
+
 // ---- prefill (prefill_tc.cu) ------------------------------------------------
 struct PrefillArgs {
   const void* q;
@@ -68,6 +76,11 @@ struct PrefillArgs {
   float scale_log2;  // softmax_scale * log2(e)
   RopeFreqs freqs;
   DeviceCtl ctl;
+  // Prefill over a cached prefix (hattn_prefill_cached): sequence b's new
+  // tokens sit at positions prefix[b]..; keys and values are read from the
+  // caches [batch, hkv, cap, d] (k_rot, v point at them), slot = position.
+  const int* prefix = nullptr;
+  int cap = 0;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 

@@ -175,8 +175,11 @@ struct Bars {
   int cu[kCuCache];
 };
 
+// t0: index of the unit's first query among its sequence's new tokens; P:
+// positions before them (the cached prefix; 0 for a plain prefill); key and
+// query positions (kstart, masks, RoPE) count from the sequence's start.
 struct UnitInfo {
-  int b, g, t0, L, tok0, kstart, nblk;
+  int b, g, t0, L, tok0, kstart, nblk, P;
 };
 
 // Unit u of the persistent loop.  Global units run latest (longest) first so
@@ -195,8 +198,9 @@ __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, const int
   ui.L = cu[ui.b + 1] - ui.tok0;
   ui.t0 = qt * UT;
   if (ui.t0 >= ui.L) return false;
-  const int qend = min(ui.t0 + UT, ui.L);  // one past the last valid query
-  ui.kstart = WIN ? max(0, ui.t0 - a.window + 1) : 0;
+  ui.P = a.prefix != nullptr ? __ldg(a.prefix + ui.b) : 0;
+  const int qend = ui.P + min(ui.t0 + UT, ui.L);  // one past the last valid query position
+  ui.kstart = WIN ? max(0, ui.P + ui.t0 - a.window + 1) : 0;
   ui.nblk = (qend - ui.kstart + BN - 1) / BN;
   return true;
 }
@@ -483,6 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pos = 0;            // ring positions filled so far
       uint32_t qfills0 = 0, qfills1 = 0;  // Q loads issued into the tile A / B buffer
       bool ok = true;
+      // K / V box of key position kpos of unit ui: packed keys [total, hkv, d]
+      // (coordinates: KV head, token) or a cache [B, hkv, cap, d] (slot, plane)
+      auto kv_c1 = [&](const UnitInfo& ui, int kpos) {
+        return a.prefix != nullptr ? kpos : ui.g;
+      };
+      auto kv_c2 = [&](const UnitInfo& ui, int kpos) {
+        return a.prefix != nullptr ? ui.b * a.hkv + ui.g : ui.tok0 + kpos;
+      };
       auto load_box = [&](const CUtensorMap* map, int dim0, int g, int row) -> bool {
         const uint32_t slot = pos % NSLOT;
         const uint32_t ph = (pos / NSLOT) & 1u;
@@ -509,14 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars->unit_full[q]);
         ++pn;
         if (u < 0) break;
-        const int row0 = ui.tok0 + ui.kstart;
+        const int k0pos = ui.kstart;
         // Several blocks: K_0 first (its slots free up while the previous
         // unit finishes), then the two Q tiles, then V_0, K_1, V_1, ...  One
         // block: the Q tiles first -- a tile's buffer frees with its S MMA of
         // the previous unit and its RoPE heads the tile's next chain -- then
         // K_0, V_0.
         if constexpr (!ONE)
-          for (int i = 0; i < 3 && ok; ++i) ok = load_box(&mapK, 64 * i, ui.g, row0);
+          for (int i = 0; i < 3 && ok; ++i)
+            ok = load_box(&mapK, 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -533,12 +546,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++qf;
         }
         if constexpr (ONE)
-          for (int i = 0; i < 3 && ok; ++i) ok = load_box(&mapK, 64 * i, ui.g, row0);
+          for (int i = 0; i < 3 && ok; ++i)
+            ok = load_box(&mapK, 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
         for (int j = 0; j < ui.nblk && ok; ++j) {
-          for (int i = 0; i < 2 && ok; ++i) ok = load_box(&mapV, 64 * i, ui.g, row0 + j * BN);
+          const int vpos = k0pos + j * BN;
+          for (int i = 0; i < 2 && ok; ++i)
+            ok = load_box(&mapV, 64 * i, kv_c1(ui, vpos), kv_c2(ui, vpos));
           if (j + 1 < ui.nblk)
             for (int i = 0; i < 3 && ok; ++i)
-              ok = load_box(&mapK, 64 * i, ui.g, row0 + (j + 1) * BN);
+              ok = load_box(&mapK, 64 * i, kv_c1(ui, vpos + BN), kv_c2(ui, vpos + BN));
         }
       }
       // never leave with copies in flight into this CTA's shared memory
@@ -784,8 +800,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       UnitInfo ui;
       unit_info<G, BN, WIN>(u, a, cu, nut, ui);
       if (!warp_wait(&bars->q_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
-      const int qmin = ui.t0 + t * TQ;           // first token of this tile
+      const int qmin = ui.P + ui.t0 + t * TQ;    // position of the tile's first token
       const int qpos = qmin + tl;
+      const int qidx = qpos - ui.P;              // this row's index among the new tokens
       // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
       // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
       // The G lanes holding one token's heads each evaluate 32/G of the 32
@@ -862,8 +879,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       pm = m;
       pl = l;
       psink = sink_l2;
-      pvalid = qpos < ui.L;
-      porow = long(ui.tok0 + qpos) * a.hq + h;
+      pvalid = qidx < ui.L;
+      porow = long(ui.tok0 + qidx) * a.hq + h;
       puc = uc;
       ++uc;
     }
@@ -881,9 +898,12 @@ template <int G, int BN, bool WIN, bool ONE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   using C = Cfg<G, BN, ONE>;
   CUtensorMap mq, mk, mv;
+  const bool cached = a.prefix != nullptr;
   if (!make_map(&mq, a.q, a.total, a.hq, kDqk, G, C::TQ) ||
-      !make_map(&mk, a.k_rot, a.total, a.hkv, kDqk, 1, BN) ||
-      !make_map(&mv, a.v, a.total, a.hkv, kDv, 1, BN))
+      !(cached ? make_map(&mk, a.k_rot, long(a.batch) * a.hkv, a.cap, kDqk, BN, 1)
+               : make_map(&mk, a.k_rot, a.total, a.hkv, kDqk, 1, BN)) ||
+      !(cached ? make_map(&mv, a.v, long(a.batch) * a.hkv, a.cap, kDv, BN, 1)
+               : make_map(&mv, a.v, a.total, a.hkv, kDv, 1, BN)))
     return cudaErrorInvalidValue;
   auto kern = prefill_kernel<G, BN, WIN, ONE>;
   static bool attr_set = false;

@@ -149,7 +149,67 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
   if (lane < 16) v_cache[crow * 16 + lane] = __ldg(v_new + row * 16 + lane);
 }
 
+// Append of packed new tokens for a prefill over a cached prefix: row (token
+// n of sequence b, KV head g) goes to slot prefix[b] + (n - cu[b]) of a linear
+// cache, rotated like kv_append_kernel.  Rows past total * hkv zero, one warp
+// per (sequence, KV head), the V slots [end, end + 256) past the sequence's
+// new end: the attention kernel reads whole key blocks, and a stale value
+// there must not turn a zero weight into NaN.  Block 0 also zeroes the
+// attention kernel's work counter.
+__global__ void __launch_bounds__(256) kv_append_packed_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+    const int* __restrict__ cu_seqlens, const int* __restrict__ prefix,
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int batch, long total, int hkv,
+    int cap, const RopeFreqs f, const DeviceCtl ctl, unsigned int* __restrict__ unit_ctr) {
+  if (unit_ctr != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *unit_ctr = 0u;
+  const int lane = threadIdx.x & 31;
+  const long row = long(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
+  const long nrows = total * hkv;
+  if (row < nrows) {
+    const long n = row / hkv;
+    const int g = int(row - n * hkv);
+    int lo = 0, hi = batch;  // largest b with cu[b] <= n
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(cu_seqlens + mid) <= n) lo = mid; else hi = mid - 1;
+    }
+    const int pos = __ldg(prefix + lo) + int(n - __ldg(cu_seqlens + lo));
+    if (pos < 0 || pos >= cap) {
+      if (lane == 0) record_status(ctl, HATTN_ERR_INVALID_ARG);
+      return;  // whole warp leaves together: no shuffle is pending
+    }
+    const long crow = (long(lo) * hkv + g) * cap + pos;
+    if (rope_key_row(k_new + row * 24, k_cache + crow * 24, pos, lane, f))
+      record_status(ctl, HATTN_ERR_INVALID_ARG);
+    if (lane < 16) v_cache[crow * 16 + lane] = __ldg(v_new + row * 16 + lane);
+    return;
+  }
+  const long z = row - nrows;
+  if (z >= long(batch) * hkv) return;
+  const int b = int(z / hkv), g = int(z - long(b) * hkv);
+  const int end = max(0, __ldg(prefix + b) + __ldg(cu_seqlens + b + 1) - __ldg(cu_seqlens + b));
+  const int stop = min(cap, end + 256);
+  uint4* plane = v_cache + (long(b) * hkv + g) * cap * 16;
+  for (int slot = end + (lane >> 4); slot < stop; slot += 2)
+    plane[long(slot) * 16 + (lane & 15)] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
+
+cudaError_t launch_kv_append_packed(const void* k_new, const void* v_new, const int* cu_seqlens,
+                                    const int* prefix, void* k_cache, void* v_cache, int batch,
+                                    long total, int hkv, int cap, const RopeFreqs& f,
+                                    const DeviceCtl& ctl, unsigned int* unit_ctr,
+                                    cudaStream_t s) {
+  const long rows = total * hkv + long(batch) * hkv;
+  if (rows == 0) return cudaSuccess;
+  const long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  kv_append_packed_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cu_seqlens, prefix,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), batch, total, hkv, cap, f, ctl,
+      unit_ctr);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,

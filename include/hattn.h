@@ -137,6 +137,41 @@ hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const 
                                     void* stream);
 
 /*
+ * Prefill over a cached prefix (prefix-cache reuse, chunked prefill): the new
+ * tokens of each sequence continue a history already held in a linear cache.
+ * Their keys (rotated) and values are appended to the caches, then each new
+ * token attends causally (within the window, if any) over the whole cache.
+ * Same results as hattn_rope_kv_append() of the new tokens at positions
+ * prefix_lens[b] + t followed by attention over all prefix_lens[b] + L_b
+ * keys.  MiMo-V2-Flash paper review, section 5.6 (prefix cache and rollout);
+ * plmsmile notes, MiMo-V2-Flash (partial rollouts re-prefilled).
+ *
+ *   q           bf16 [total_tokens, hq, dqk]  the new tokens' queries, un-rotated, packed
+ *   k_new, v_new  bf16 [total_tokens, hkv, dqk] / [total_tokens, hkv, dv], packed
+ *   k_cache, v_cache  [batch, hkv, cap, dqk|dv] linear (slot = position): slots
+ *               [0, prefix_lens[b]) hold the prefix as hattn_rope_kv_append()
+ *               writes it; the new tokens are written at [prefix, prefix + L_b),
+ *               and V slots [prefix + L_b, prefix + L_b + 256) are zeroed (they
+ *               hold no token yet)
+ *   cu_seqlens  int32 [batch + 1] DEVICE, as for hattn_prefill(): the new tokens
+ *   prefix_lens int32 [batch] DEVICE: tokens already in the caches, >= 0
+ *   out, lse    as for hattn_prefill(), one row per new token
+ *   max_seqlen  upper bound of the new tokens per sequence; max_prefix upper
+ *               bound of prefix_lens; prefix_lens[b] + L_b <= cap
+ *   workspace   DEVICE scratch of >= 256 bytes (the kernel's work counter)
+ *   other arguments as for hattn_prefill().
+ * A position outside [0, cap) is skipped and recorded as HATTN_ERR_INVALID_ARG.
+ */
+hattn_status_t hattn_prefill_cached(const void* q, const void* k_new, const void* v_new,
+                                    void* k_cache, void* v_cache, const int* cu_seqlens,
+                                    const int* prefix_lens, const float* sink, void* out,
+                                    float* lse, int batch, long total_tokens, int max_seqlen,
+                                    int max_prefix, int cap, int hq, int hkv, int dqk, int dv,
+                                    int rope_dim, float rope_base, int window,
+                                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
  * Bytes of workspace hattn_decode() needs for a batch whose longest
  * sequence holds max_seqlen_k tokens, with the same cap, is_ring and window
  * as the hattn_decode() call (0 when one pass per KV head suffices: a

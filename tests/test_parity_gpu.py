@@ -411,3 +411,91 @@ def test_hybrid_block_256k_sampled():
         compare(out[idx], lse[idx], o_ref, l_ref, f"hybrid layer {li} ({kind})")
         del c, out, lse, cpu
         torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ prefill over a cached prefix
+def _prefill_cached_case(prefixes, news, G, window, base, seed, init=0.0):
+    """Sequences whose first prefixes[b] tokens sit in a linear cache and whose
+    next news[b] tokens are new; returns the CUDA path's (out, lse) for the new
+    tokens, the oracle's over each whole history, and the caches."""
+    dev = torch.device("cuda")
+    hq, hkv = 2 * G, 2
+    Ls = [p + n for p, n in zip(prefixes, news)]
+    d = synth.decode_case(Ls, 1, hq, hkv, window=window, rope_base=base, seed=seed)
+    g = synth._gen(seed + 1, "cpu")
+    q_new = [synth.randn_bf16((n, hq, synth.D_QK), g, "cpu") for n in news]
+    B, cap = len(Ls), max(Ls) + 300
+    kc = torch.full((B, hkv, cap, synth.D_QK), init, dtype=torch.bfloat16, device=dev)
+    vc = torch.full((B, hkv, cap, synth.D_V), init, dtype=torch.bfloat16, device=dev)
+    for b, P in enumerate(prefixes):
+        if P:
+            ha.rope_kv_append(d.k_hist[b:b + 1, :P].contiguous().to(dev),
+                              d.v_hist[b:b + 1, :P].contiguous().to(dev),
+                              torch.zeros(1, dtype=torch.int32, device=dev), kc[b:b + 1],
+                              vc[b:b + 1], is_ring=False, rope_base=base)
+    k_new = torch.cat([d.k_hist[b, P:P + n] for b, (P, n) in enumerate(zip(prefixes, news))])
+    v_new = torch.cat([d.v_hist[b, P:P + n] for b, (P, n) in enumerate(zip(prefixes, news))])
+    cu = torch.tensor([0] + list(np.cumsum(news)), dtype=torch.int32, device=dev)
+    pre = torch.tensor(prefixes, dtype=torch.int32, device=dev)
+    out, lse = ha.prefill_cached(torch.cat(q_new).to(dev), k_new.to(dev), v_new.to(dev), kc, vc,
+                                 cu, pre, d.sink.to(dev), max_seqlen=max(news),
+                                 max_prefix=max(prefixes), window=window, rope_base=base,
+                                 softmax_scale=d.scale)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    o_ref, l_ref = [], []
+    for b, (P, n) in enumerate(zip(prefixes, news)):
+        if n == 0:
+            continue
+        o, l = oracle.decode(q_new[b][None], d.k_hist[b:b + 1], d.v_hist[b:b + 1], [P + n],
+                             d.sink, window=window, rope_base=base, scale=d.scale)
+        o_ref.append(o[0])
+        l_ref.append(l[0])
+    return out, lse, np.concatenate(o_ref), np.concatenate(l_ref), (kc, vc, d, k_new, v_new)
+
+
+@pytest.mark.parametrize("prefixes,news,G,window,base", [
+    ([0, 100, 3000], [50, 300, 257], 16, 0, 5e6),       # global layer, ragged
+    ([0, 1, 500], [700, 129, 64], 8, 128, 1e4),         # window over the cache (one block)
+    ([2000, 0], [300, 1500], 4, 1000, 1e4),             # wide window (several blocks)
+    ([4095, 17], [1, 2], 16, 0, 5e6),                   # one or two new tokens
+])
+def test_prefill_cached_prefix(prefixes, news, G, window, base):
+    out, lse, o_ref, l_ref, _ = _prefill_cached_case(prefixes, news, G, window, base,
+                                                     seed=1700 + G + window)
+    compare(out, lse, o_ref, l_ref, f"cached prefix {prefixes} + {news} W={window}")
+
+
+def test_prefill_cached_prefix_over_nan_slots():
+    """Slots past the history hold NaN before the call: the appended keys and
+    the zeroed value slots past them keep the output finite and exact."""
+    out, lse, o_ref, l_ref, _ = _prefill_cached_case([37, 1200], [90, 333], 16, 0, 5e6,
+                                                     seed=1800, init=float("nan"))
+    compare(out, lse, o_ref, l_ref, "cached prefix over NaN slots")
+
+
+def test_prefill_cached_appends_like_rope_kv_append():
+    """The new tokens land in the caches exactly as hattn_rope_kv_append writes them."""
+    prefixes, news = [10, 300], [40, 77]
+    _, _, _, _, (kc, vc, d, k_new, v_new) = _prefill_cached_case(prefixes, news, 8, 128, 1e4,
+                                                                 seed=1900)
+    dev = torch.device("cuda")
+    kc2, vc2 = torch.zeros_like(kc), torch.zeros_like(vc)
+    off = 0
+    for b, (P, n) in enumerate(zip(prefixes, news)):
+        ha.rope_kv_append(k_new[off:off + n][None].to(dev), v_new[off:off + n][None].to(dev),
+                          torch.tensor([P], dtype=torch.int32, device=dev), kc2[b:b + 1],
+                          vc2[b:b + 1], is_ring=False, rope_base=1e4)
+        assert torch.equal(kc[b, :, P:P + n], kc2[b, :, P:P + n])
+        assert torch.equal(vc[b, :, P:P + n], vc2[b, :, P:P + n])
+        assert (vc[b, :, P + n:P + n + 256] == 0).all()   # the zeroed tail
+        off += n
+    torch.cuda.synchronize()
+
+
+def test_prefill_cached_without_prefix_matches_prefill():
+    """Empty prefixes: the same attention as hattn_prefill of the new tokens."""
+    news, G = [300, 129, 64], 8
+    out, lse, o_ref, l_ref, (kc, vc, d, k_new, v_new) = _prefill_cached_case(
+        [0, 0, 0], news, G, 128, 1e4, seed=2000)
+    compare(out, lse, o_ref, l_ref, "cached prefix, none cached")
