@@ -50,6 +50,8 @@ SIGNATURES = {
                           _F, _F, _P, _Z, _P]),
     "hattn_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                  _I, _I, _I, _I, _F, _F, _P, _Z, _P]),
+    "hattn_decode_append_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I,
+                                       _I, _I, _I, _I, _I, _I, _I, _F, _F, _P, _Z, _P]),
     "hattn_decode_static_scratch": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                          _I, _I, _I, _I, _F, _F, _P]),
     "hattn_check_device_status": (_I, [_P]),
@@ -168,6 +170,18 @@ def hattn_decode_append(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, out,
         _ptr(sink), _ptr(out), _ptr(lse), int(B), int(T), int(hq), int(hkv), int(dqk), int(dv),
         int(cap), int(is_ring), int(window), int(max_seqlen_k), int(rope_dim), float(rope_base),
         float(softmax_scale), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def hattn_decode_append_paged(q, k_new, v_new, k_pages, v_pages, block_table, table_stride,
+                              num_pages, page, seqlens_k, sink, out, lse, B, T, hq, hkv, dqk, dv,
+                              window, max_seqlen_k, rope_dim, rope_base, softmax_scale,
+                              workspace, workspace_bytes, stream=None) -> int:
+    return load_library().hattn_decode_append_paged(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+        int(table_stride), int(num_pages), int(page), _ptr(seqlens_k), _ptr(sink), _ptr(out),
+        _ptr(lse), int(B), int(T), int(hq), int(hkv), int(dqk), int(dv), int(window),
+        int(max_seqlen_k), int(rope_dim), float(rope_base), float(softmax_scale), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
 
 
 def hattn_decode_static_scratch(q, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv,
@@ -302,6 +316,34 @@ def decode_append(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, *, max_seq
                                ROPE_DIM, rope_base, softmax_scale, workspace,
                                workspace.numel() if workspace is not None else 0),
            "hattn_decode_append")
+    return out, lse
+
+
+def decode_append_paged(q, k_new, v_new, k_pages, v_pages, block_table, seqlens_k, sink, *,
+                        max_seqlen_k: int, window: int, rope_base: float,
+                        softmax_scale: float | None = None, out=None, lse=None, workspace=None,
+                        with_lse: bool = True):
+    """decode_append over paged caches k_pages / v_pages [num_pages, hkv, page, d] and
+    block_table [B, table_stride] (int32); returns (out, lse)."""
+    B, T, hq, dqk = q.shape
+    num_pages, hkv, page, _ = k_pages.shape
+    dv = v_pages.shape[3]
+    stride = block_table.shape[1]
+    if softmax_scale is None:
+        softmax_scale = dqk ** -0.5
+    if out is None:
+        out = torch.empty((B, T, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((B, T, hq), dtype=torch.float32, device=q.device)
+    need = hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window, stride * page, 0)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(hattn_decode_append_paged(q, k_new, v_new, k_pages, v_pages, block_table, stride,
+                                     num_pages, page, seqlens_k, sink, out, lse, B, T, hq, hkv,
+                                     dqk, dv, window, max_seqlen_k, ROPE_DIM, rope_base,
+                                     softmax_scale, workspace,
+                                     workspace.numel() if workspace is not None else 0),
+           "hattn_decode_append_paged")
     return out, lse
 
 

@@ -96,6 +96,9 @@ __device__ __forceinline__ bool slot_range(int L, const DecodeArgs& a, int& lo, 
     hi = min(L, a.cap);
   } else {
     lo = a.window > 0 ? max(0, L - a.T - a.window + 1) : 0;
+    // paged: blocks of 64 slots start on a multiple of 64, so a block never
+    // straddles two pages (the extra leading slots are outside the window)
+    if (a.pg.table != nullptr) lo &= ~63;
     hi = L;
   }
   return hi > lo;
@@ -265,11 +268,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
           uint8_t* dst = smem + kOffStage + st * kStageBytes;
-          const int row = it.s_beg + blk * kBK;
+          int row = it.s_beg + blk * kBK, pl = plane;
+          if (a.pg.table != nullptr) {  // paged: blocks never straddle a page
+            const int lp = row / a.pg.page;
+            const int phys = __ldg(a.pg.table + long(it.b) * a.pg.stride + lp);
+            if (phys < 0 || phys >= a.pg.num_pages) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+            row -= lp * a.pg.page;
+            pl = phys * a.hkv + it.kvh;  // out of range reads as zeros
+          }
           for (int i = 0; i < 3; ++i)
-            tma_load_3d(dst + i * kBox, &mapK, &bars->full[st], 64 * i, row, plane);
+            tma_load_3d(dst + i * kBox, &mapK, &bars->full[st], 64 * i, row, pl);
           for (int i = 0; i < 2; ++i)
-            tma_load_3d(dst + (3 + i) * kBox, &mapV, &bars->full[st], 64 * i, row, plane);
+            tma_load_3d(dst + (3 + i) * kBox, &mapV, &bars->full[st], 64 * i, row, pl);
         }
       }
       // never leave with copies in flight into this CTA's shared memory
@@ -1587,9 +1597,12 @@ cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {
     attr_set[gi] = true;
   }
   CUtensorMap mq, mk, mv;
+  const bool paged = a.pg.table != nullptr;
+  const long planes = paged ? long(a.pg.num_pages) * a.hkv : long(a.B) * a.hkv;
+  const int slots = paged ? a.pg.page : a.cap;
   if (!make_map(&mq, a.q, long(a.B) * a.T, a.hq, kDqk, G, a.T) ||
-      !make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, kBK, 1) ||
-      !make_map(&mv, a.v_cache, long(a.B) * a.hkv, a.cap, kDv, kBK, 1))
+      !make_map(&mk, a.k_cache, planes, slots, kDqk, kBK, 1) ||
+      !make_map(&mv, a.v_cache, planes, slots, kDv, kBK, 1))
     return cudaErrorInvalidValue;
   const long nvirt = long(a.nsplit) * a.B * a.hkv;
   const int grid = int(nvirt < num_sms() ? nvirt : num_sms());
@@ -1642,7 +1655,7 @@ cudaError_t launch_decode(const DecodeArgs& a_in, cudaStream_t s) {
     // the append as its own launch ahead of the step
     cudaError_t e = launch_kv_append(a.k_new, a.v_new, a.seqlens, const_cast<void*>(a.k_cache),
                                      const_cast<void*>(a.v_cache), a.B, a.T, a.hkv, a.cap,
-                                     a.is_ring, a.freqs, a.ctl, s, true);
+                                     a.is_ring, a.freqs, a.ctl, s, true, a.pg);
     if (e != cudaSuccess) return e;
     a.k_new = nullptr;
     a.v_new = nullptr;

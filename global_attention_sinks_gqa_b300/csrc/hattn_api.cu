@@ -274,7 +274,7 @@ hattn_status_t decode_step(const void* q, const void* k_new, const void* v_new, 
                            float* lse, int B, int T, int hq, int hkv, int dqk, int dv, int cap,
                            int is_ring, int window, int max_seqlen_k, int rope_dim,
                            float rope_base, float softmax_scale, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+                           size_t workspace_bytes, void* stream, const Paging& pg = Paging()) {
   hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
   if (st != HATTN_OK) return st;
   if (B < 0 || T <= 0 || cap <= 0 || window < 0 || max_seqlen_k < T ||
@@ -315,6 +315,7 @@ hattn_status_t decode_step(const void* q, const void* k_new, const void* v_new, 
   a.nsplit = decode_num_splits(max_seqlen_k, T, window, is_ring, cap, &a.chunk);
   a.k_new = k_new;
   a.v_new = v_new;
+  a.pg = pg;
   const size_t need = decode_workspace_bytes(B, T, hq, a.nsplit);
   a.part_o = nullptr;
   a.part_lse = nullptr;
@@ -357,6 +358,29 @@ hattn_status_t hattn_decode_append(const void* q, const void* k_new, const void*
   return decode_step(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv,
                      dqk, dv, cap, is_ring, window, max_seqlen_k, rope_dim, rope_base,
                      softmax_scale, workspace, workspace_bytes, stream);
+}
+
+hattn_status_t hattn_decode_append_paged(const void* q, const void* k_new, const void* v_new,
+                                         void* k_pages, void* v_pages, const int* block_table,
+                                         int table_stride, int num_pages, int page,
+                                         const int* seqlens_k, const float* sink, void* out,
+                                         float* lse, int B, int T, int hq, int hkv, int dqk,
+                                         int dv, int window, int max_seqlen_k, int rope_dim,
+                                         float rope_base, float softmax_scale, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (page <= 0 || page % 64 != 0 || table_stride <= 0 || num_pages <= 0)
+    return HATTN_ERR_INVALID_ARG;
+  if (long(table_stride) * page > 2147483647L) return HATTN_ERR_INVALID_ARG;
+  if (B > 0 && (!k_new || !v_new || !block_table)) return HATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(block_table) & 3u) return HATTN_ERR_INVALID_ARG;
+  Paging pg;
+  pg.table = block_table;
+  pg.stride = table_stride;
+  pg.page = page;
+  pg.num_pages = num_pages;
+  return decode_step(q, k_new, v_new, k_pages, v_pages, seqlens_k, sink, out, lse, B, T, hq, hkv,
+                     dqk, dv, table_stride * page, 0, window, max_seqlen_k, rope_dim, rope_base,
+                     softmax_scale, workspace, workspace_bytes, stream, pg);
 }
 
 hattn_status_t hattn_check_device_status(void* stream) {

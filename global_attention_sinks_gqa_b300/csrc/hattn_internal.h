@@ -43,12 +43,20 @@ int num_sms();
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
                                     cudaStream_t s, unsigned int* unit_ctr = nullptr);
+// A paged cache: position p of sequence b lives in page
+// table[b * stride + p / page], slot p % page; pages are [num_pages, hkv,
+// page, d].  table == nullptr: a contiguous cache [B, hkv, cap, d].
+struct Paging {
+  const int* table = nullptr;
+  int stride = 0, page = 0, num_pages = 0;
+};
+
 // Token t of sequence b goes to position start_pos[b] + t, or, with
 // from_len, to seqlens[b] - T + t (start_pos then holds seqlens).
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* start_pos,
                              void* k_cache, void* v_cache, int B, int T, int hkv, int cap,
                              int is_ring, const RopeFreqs& f, const DeviceCtl& ctl,
-                             cudaStream_t s, bool from_len = false);
+                             cudaStream_t s, bool from_len = false, Paging pg = Paging());
 
 // Packed new tokens of sequence b to slots prefix[b] + t of a linear cache;
 // also zeroes V slots [end, end + 256) past each sequence's new end and
@@ -104,6 +112,7 @@ struct DecodeArgs {
   // (un-rotated) and V, written into the caches before they are read.
   // nullptr: the caches already hold them.
   unsigned int* item_ctr = nullptr;  // work counter in the workspace (nsplit > 1)
+  Paging pg;                         // paged caches (linear positions, cap = stride * page)
   const void* k_new = nullptr;  // bf16 [B, T, hkv, dqk]
   const void* v_new = nullptr;  // bf16 [B, T, hkv, dv]
   DeviceCtl ctl;

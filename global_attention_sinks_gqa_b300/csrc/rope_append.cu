@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int* __restrict__ start_pos, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
     int B, int T, int hkv, int cap, int is_ring, const RopeFreqs f, const DeviceCtl ctl,
-    int from_len) {
+    int from_len, const Paging pg) {
   const int lane = threadIdx.x & 31;
   const long row = long(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);  // (b, t, g)
   if (row >= long(B) * T * hkv) return;
@@ -142,8 +142,19 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     if (lane == 0) record_status(ctl, HATTN_ERR_INVALID_ARG);
     return;  // whole warp leaves together: no shuffle is pending
   }
-  const long slot = is_ring ? (pos % cap) : pos;
-  const long crow = (long(b) * hkv + g) * cap + slot;
+  long crow;
+  if (pg.table != nullptr) {  // paged: the page of this position, its slot there
+    const int lp = pos / pg.page;
+    const int phys = __ldg(pg.table + long(b) * pg.stride + lp);
+    if (phys < 0 || phys >= pg.num_pages) {
+      if (lane == 0) record_status(ctl, HATTN_ERR_INVALID_ARG);
+      return;
+    }
+    crow = (long(phys) * hkv + g) * pg.page + (pos - lp * pg.page);
+  } else {
+    const long slot = is_ring ? (pos % cap) : pos;
+    crow = (long(b) * hkv + g) * cap + slot;
+  }
   if (rope_key_row(k_new + row * 24, k_cache + crow * 24, pos, lane, f))
     record_status(ctl, HATTN_ERR_INVALID_ARG);
   if (lane < 16) v_cache[crow * 16 + lane] = __ldg(v_new + row * 16 + lane);
@@ -227,14 +238,14 @@ cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_se
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* start_pos,
                              void* k_cache, void* v_cache, int B, int T, int hkv, int cap,
                              int is_ring, const RopeFreqs& f, const DeviceCtl& ctl,
-                             cudaStream_t s, bool from_len) {
+                             cudaStream_t s, bool from_len, Paging pg) {
   const long rows = long(B) * T * hkv;
   if (rows == 0) return cudaSuccess;
   const long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   kv_append_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), start_pos,
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), B, T, hkv, cap, is_ring, f,
-      ctl, from_len ? 1 : 0);
+      ctl, from_len ? 1 : 0, pg);
   return cudaGetLastError();
 }
 

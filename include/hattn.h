@@ -253,6 +253,32 @@ hattn_status_t hattn_decode_append(const void* q, const void* k_new, const void*
                                    void* stream);
 
 /*
+ * hattn_decode_append() over paged caches: position p of sequence b lives in
+ * page block_table[b * table_stride + p / page], slot p % page.
+ *
+ *   k_pages, v_pages  [num_pages, hkv, page, dqk|dv]: K stored as
+ *               hattn_rope_kv_append() writes it (dims 0..63 fp16, rest bf16),
+ *               V bf16; the new tokens are written into their pages
+ *   block_table int32 [B, table_stride] DEVICE: page of each run of `page`
+ *               positions; entries past a sequence's last position are not read
+ *   page        positions per page, a multiple of 64
+ *   every other argument as for hattn_decode_append() with is_ring = 0 and
+ *   cap = table_stride * page (so max_seqlen_k <= table_stride * page).
+ * A page index outside [0, num_pages) is recorded as HATTN_ERR_INVALID_ARG and
+ * reads as zeros (it is never written).  The workspace is that of
+ * hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window,
+ * table_stride * page, 0).
+ */
+hattn_status_t hattn_decode_append_paged(const void* q, const void* k_new, const void* v_new,
+                                         void* k_pages, void* v_pages, const int* block_table,
+                                         int table_stride, int num_pages, int page,
+                                         const int* seqlens_k, const float* sink, void* out,
+                                         float* lse, int B, int T, int hq, int hkv, int dqk,
+                                         int dv, int window, int max_seqlen_k, int rope_dim,
+                                         float rope_base, float softmax_scale, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/*
  * hattn_decode() for callers that cannot allocate device memory.  The paper
  * has no counterpart to this entry point; it exists for callers that cannot
  * call cudaMalloc -- code running inside a host framework that owns all

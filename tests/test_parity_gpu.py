@@ -499,3 +499,48 @@ def test_prefill_cached_without_prefix_matches_prefill():
     out, lse, o_ref, l_ref, (kc, vc, d, k_new, v_new) = _prefill_cached_case(
         [0, 0, 0], news, G, 128, 1e4, seed=2000)
     compare(out, lse, o_ref, l_ref, "cached prefix, none cached")
+
+
+# ------------------------------------------------------------ paged caches
+@pytest.mark.parametrize("page,G,window,base,T,lens", [
+    (64, 16, 0, 5e6, 4, [4, 63, 64, 65, 700, 3000]),     # one or many pages, one chunk
+    (128, 8, 128, 1e4, 4, [4, 200, 1000]),                # a window over pages
+    (256, 16, 0, 5e6, 1, [5000, 9000, 130]),              # split-KV chunks over pages
+])
+def test_decode_append_paged(page, G, window, base, T, lens):
+    """Paged caches (pages in shuffled order) hold the bytes of the contiguous
+    caches, give their outputs (bit for bit without a window), and match the
+    oracle."""
+    dev = torch.device("cuda")
+    d = synth.decode_case(lens, T, 2 * G, 2, window=window, rope_base=base,
+                          seed=2100 + page + G + T)
+    stride = (max(lens) + 3 + page - 1) // page
+    kc, vc, k_new, v_new, sl = _append_step(d, stride * page, False)
+    B, hkv = len(lens), 2
+    num_pages = B * stride + 5
+    rs = np.random.RandomState(2200 + page)
+    table = torch.tensor(rs.permutation(num_pages)[:B * stride].reshape(B, stride),
+                         dtype=torch.int32, device=dev)
+    kp = torch.zeros((num_pages, hkv, page, synth.D_QK), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros((num_pages, hkv, page, synth.D_V), dtype=torch.bfloat16, device=dev)
+    for b in range(B):
+        for lp in range(stride):
+            kp[table[b, lp]] = kc[b, :, lp * page:(lp + 1) * page]
+            vp[table[b, lp]] = vc[b, :, lp * page:(lp + 1) * page]
+    q, sink = d.q.to(dev), d.sink.to(dev)
+    kw = dict(max_seqlen_k=max(lens), window=window, rope_base=base, softmax_scale=d.scale)
+    out_p, lse_p = ha.decode_append_paged(q, k_new, v_new, kp, vp, table, sl, sink, **kw)
+    out_l, lse_l = ha.decode_append(q, k_new, v_new, kc, vc, sl, sink, is_ring=False, **kw)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    if window == 0:  # same blocks as the contiguous cache: the same bits
+        assert torch.equal(out_p, out_l) and torch.equal(lse_p, lse_l), "paged != contiguous"
+    # (with a window the paged item starts on a 64-slot boundary, so its blocks
+    # and hence its rounding differ from the contiguous cache's)
+    for b in range(B):
+        for lp in range(stride):
+            assert torch.equal(kp[table[b, lp]], kc[b, :, lp * page:(lp + 1) * page])
+            assert torch.equal(vp[table[b, lp]], vc[b, :, lp * page:(lp + 1) * page])
+    o_ref, l_ref = oracle.decode(d.q, d.k_hist, d.v_hist, d.seqlens, d.sink, window=window,
+                                 rope_base=base, scale=d.scale)
+    compare(out_p, lse_p, o_ref, l_ref, f"paged decode page={page} G={G} W={window}")
