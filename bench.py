@@ -654,6 +654,74 @@ def run_prefix_prefill(args):
             "algorithmic": {"flops": flops, "bytes": byts}, "clocks": clk.summary()}
 
 
+def run_paged_decode(args):
+    """The global layer's decode step of the bench (batch 64 x 4 verify tokens,
+    lengths U[8192, 65536]) over a paged copy of its cache: pages of 256
+    positions in shuffled order, one hattn_decode_append_paged call per step."""
+    import global_attention_sinks_gqa_b300 as ha
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = Workload(dev)
+    dd = [d for d in wl.dec if not d["ring"]][0]
+    p = dd["p"]
+    page = 256
+    stride = (dd["cap"] + page - 1) // page
+    kc, vc = dd["kc"], dd["vc"]
+    B, hkv = wl.B, p["hkv"]
+    num_pages = B * stride
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(11)
+    table = torch.randperm(num_pages, generator=gen).to(torch.int32).reshape(B, stride).to(dev)
+    kp = torch.empty((num_pages, hkv, page, D_QK), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty((num_pages, hkv, page, D_V), dtype=torch.bfloat16, device=dev)
+    for b in range(B):
+        for lp in range(stride):
+            hi = min((lp + 1) * page, dd["cap"])
+            kp[table[b, lp], :, :hi - lp * page] = kc[b, :, lp * page:hi]
+            vp[table[b, lp], :, :hi - lp * page] = vc[b, :, lp * page:hi]
+    del wl.layers
+    ws_n = ha.hattn_decode_workspace_size(B, wl.T, p["hq"], hkv, D_V, wl.lmax, p["window"],
+                                          stride * page, 0)
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    sptr = torch.cuda.current_stream(dev).cuda_stream
+
+    def step():
+        st = ha.hattn_decode_append_paged(dd["q"], dd["k_new"], dd["v_new"], kp, vp, table,
+                                          stride, num_pages, page, dd["seqlens"], dd["sink"],
+                                          dd["out"], dd["lse"], B, wl.T, p["hq"], hkv, D_QK,
+                                          D_V, p["window"], wl.lmax, R, p["rope_base"],
+                                          1.0 / math.sqrt(D_QK), ws, ws.numel(), sptr)
+        assert st == 0, ha.status_string(st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        start.record()
+        for _ in range(args.steps):
+            step()
+        stop.record()
+        torch.cuda.synchronize()
+    ha.check_device_status()
+    ms = start.elapsed_time(stop) / args.steps
+    hbm, tf_burst, tf_sust, src = measured_peaks()
+    byts = dd["bytes"] + dd["abytes"]
+    gbs = byts / (ms / 1e3) / 1e9
+    return {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks)",
+            "config": {"workload": "paged_decode: global layer, batch 64 x 4 verify tokens, "
+                                   "L ~ U[8192, 65536], pages of 256 positions, shuffled"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(gbs / hbm, 4), "traffic": None,
+                         "peak_source": f"{src} hbm_gbs"},
+            "clocks": clk.summary()}
+
+
 def run_profile_case(args):
     """One call of one part of the step at a chosen size, for an ncu capture:
     a warm-up call, then the profiled call inside the NVTX range "profile"."""
@@ -718,9 +786,10 @@ def main():
     ap.add_argument("--seq", type=int, default=0, help="prefill length for --profile-case")
     ap.add_argument("--batch", type=int, default=0, help="decode batch for --profile-case")
     ap.add_argument("--workload", default="step",
-                    choices=["step", "hybrid_block_256k", "prefix_prefill"],
+                    choices=["step", "hybrid_block_256k", "prefix_prefill", "paged_decode"],
                     help="step: the default bench step; hybrid_block_256k: config 5 alone; "
-                         "prefix_prefill: 4096 new tokens over a cached 28672-token prefix")
+                         "prefix_prefill: 4096 new tokens over a cached 28672-token prefix; "
+                         "paged_decode: the global decode step over a paged cache")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
@@ -730,6 +799,9 @@ def main():
         return
     if args.workload == "prefix_prefill":
         print(json.dumps(run_prefix_prefill(args)))
+        return
+    if args.workload == "paged_decode":
+        print(json.dumps(run_paged_decode(args)))
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
