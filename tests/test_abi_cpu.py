@@ -130,6 +130,55 @@ def test_append_rejects_bad_arguments(lib, kw, code):
     assert ha.hattn_rope_kv_append(**args) == code
 
 
+def _prefill_cached(**kw):
+    args = dict(q=FAKE, k_new=FAKE, v_new=FAKE, k_cache=FAKE, v_cache=FAKE, cu_seqlens=FAKE,
+                prefix_lens=FAKE, sink=FAKE, out=FAKE, lse=FAKE, batch=2, total_tokens=512,
+                max_seqlen=300, max_prefix=4096, cap=8192, hq=32, hkv=2, dqk=192, dv=128,
+                rope_dim=64, rope_base=5e6, window=0, softmax_scale=0.07, workspace=FAKE,
+                workspace_bytes=256, stream=0)
+    args.update(kw)
+    return ha.hattn_prefill_cached(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(workspace_bytes=128), ha.HATTN_ERR_WORKSPACE),    # the work counter needs 256 bytes
+    (dict(workspace=None), ha.HATTN_ERR_WORKSPACE),
+    (dict(prefix_lens=None), ha.HATTN_ERR_INVALID_ARG),
+    (dict(k_cache=FAKE + 4), ha.HATTN_ERR_INVALID_ARG),      # misaligned
+    (dict(max_prefix=-1), ha.HATTN_ERR_INVALID_ARG),
+    (dict(cap=0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(max_seqlen=513), ha.HATTN_ERR_INVALID_ARG),
+    (dict(dv=64), ha.HATTN_ERR_UNSUPPORTED),
+])
+def test_prefill_cached_rejects_bad_arguments(lib, kw, code):
+    assert _prefill_cached(**kw) == code
+
+
+def _decode_paged(**kw):
+    args = dict(q=FAKE, k_new=FAKE, v_new=FAKE, k_pages=FAKE, v_pages=FAKE, block_table=FAKE,
+                table_stride=256, num_pages=16384, page=256, seqlens_k=FAKE, sink=FAKE, out=FAKE,
+                lse=FAKE, B=64, T=4, hq=64, hkv=4, dqk=192, dv=128, window=0,
+                max_seqlen_k=65536, rope_dim=64, rope_base=5e6, softmax_scale=0.07,
+                workspace=None, workspace_bytes=0, stream=0)
+    args.update(kw)
+    return ha.hattn_decode_append_paged(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(page=100), ha.HATTN_ERR_INVALID_ARG),              # pages hold whole 64-slot blocks
+    (dict(page=0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(table_stride=0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(num_pages=0), ha.HATTN_ERR_INVALID_ARG),
+    (dict(block_table=None), ha.HATTN_ERR_INVALID_ARG),
+    (dict(block_table=FAKE + 2), ha.HATTN_ERR_INVALID_ARG),  # misaligned int32
+    (dict(max_seqlen_k=65537), ha.HATTN_ERR_INVALID_ARG),     # past table_stride * page
+    (dict(T=9), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(), ha.HATTN_ERR_WORKSPACE),                         # split chunks need a workspace
+])
+def test_decode_paged_rejects_bad_arguments(lib, kw, code):
+    assert _decode_paged(**kw) == code
+
+
 def test_oracle_is_not_reachable_from_the_product():
     """The product package never imports the oracle."""
     pkg = os.path.join(ROOT, "global_attention_sinks_gqa_b300")
