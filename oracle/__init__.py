@@ -10,10 +10,12 @@ Two independent implementations live here:
 * ``hattn_oracle.c`` (loaded through ctypes): the definition written out row
   by row in double precision -- RoPE at each token's position, the visible key
   set, the logits, the softmax with the sink in its denominator, the weighted
-  sum of values and the log-sum-exp.
+  sum of values and the log-sum-exp -- and its backward (the chain rule
+  through the same steps, for the gradients of q, k, v and the sink).
 * ``brute.py`` (numpy): the same definition written as whole matrices (a sink
   column appended to an explicit masked logit matrix, RoPE as a complex
-  rotation), used only on tiny shapes to cross-check the C oracle.
+  rotation), forward and backward, used only on tiny shapes to cross-check the
+  C oracle; its backward is pinned by finite differences of its forward.
 
 Citations (page title, section): MiMo-V2-Flash Technical Report paper review
 (xllm-io), sections 3.1 (shapes, GQA, partial RoPE, W = 128), 3.2 (learnable
@@ -64,6 +66,9 @@ def _load():
             lib.hattn_oracle_decode.restype = i
             lib.hattn_oracle_rope.argtypes = [P, P, P, l, i, i, d]
             lib.hattn_oracle_rope.restype = i
+            lib.hattn_oracle_prefill_backward.argtypes = [P, P, P, P, P, P, P, P, P, i, P, i, i, i,
+                                                          i, i, d, i, d, i]
+            lib.hattn_oracle_prefill_backward.restype = i
             lib.hattn_oracle_num_threads.argtypes = [i]
             lib.hattn_oracle_num_threads.restype = i
             _lib = lib
@@ -173,3 +178,33 @@ def rope(x, positions, *, rope_base: float, rope_dim: int = 64):
     if rc != 0:
         raise RuntimeError(f"oracle rope failed with code {rc}")
     return y
+
+
+def prefill_backward(q, k, v, sink, dout, cu_seqlens, *, window: int, rope_base: float,
+                     scale: float, rope_dim: int = 64, nthreads: int = 0):
+    """Gradients of sum(dout * out) of :func:`prefill` with respect to q, k, v
+    (un-rotated inputs) and the sink logits.
+
+    q, k, v as for :func:`prefill`; dout [total, hq, dv] bf16.  Returns
+    (dq [total, hq, dqk], dk [total, hkv, dqk], dv [total, hkv, dv], dsink [hq])
+    as float64 arrays.
+    """
+    qb, kb, vb, gb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v), _bf16_bits(dout)
+    total, hq, dqk = qb.shape
+    hkv, dv = kb.shape[1], vb.shape[2]
+    assert gb.shape == (total, hq, dv)
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32).reshape(-1))
+    assert cu[-1] == total and kb.shape[0] == total and vb.shape[0] == total
+    s = _f64(sink).reshape(-1)
+    assert s.shape[0] == hq
+    dq = np.empty((total, hq, dqk), np.float64)
+    dk = np.empty((total, hkv, dqk), np.float64)
+    dvv = np.empty((total, hkv, dv), np.float64)
+    ds = np.empty((hq,), np.float64)
+    rc = _load().hattn_oracle_prefill_backward(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(s), _ptr(gb), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(ds),
+        len(cu) - 1, _ptr(cu), hq, hkv, dqk, dv, rope_dim, float(rope_base), int(window),
+        float(scale), nthreads)
+    if rc != 0:
+        raise RuntimeError(f"oracle prefill backward failed with code {rc}")
+    return dq, dk, dvv, ds

@@ -13,7 +13,11 @@ matrices so that it shares no structure with the row-by-row C oracle:
   Sink": the sink joins the denominator and has no value, i.e. a zero value
   row);
 * softmax over the S + 1 columns, then out = P @ [V; 0] and lse = log-sum-exp
-  of the row.
+  of the row;
+* backward (gradients of sum(dout * out)) in matrix form: dP = dout [V; 0]^T,
+  dZ = P * (dP - rowsum(dP * P)) over all S + 1 columns (the sink's column
+  gives the sink gradient), dQ' = scale dZ K', dK' = scale dZ^T Q',
+  dV = P^T dout, and the rotation undone by the conjugate complex factor.
 """
 from __future__ import annotations
 
@@ -104,3 +108,74 @@ def prefill(q, k, v, sink, cu_seqlens, *, window, rope_base, scale, rope_dim=64)
         outs.append(o)
         lses.append(l)
     return np.concatenate(outs, 0), np.concatenate(lses, 0)
+
+
+def rope_complex_transposed(g: np.ndarray, pos: np.ndarray, base: float,
+                            rope_dim: int) -> np.ndarray:
+    """Gradient through :func:`rope_complex`: multiply by the conjugate rotation."""
+    if rope_dim == 0:
+        return g.copy()
+    half = rope_dim // 2
+    theta = base ** (-2.0 * np.arange(half) / rope_dim)
+    rot = np.exp(-1j * np.outer(pos.astype(np.float64), theta))
+    zc = (g[..., :half] + 1j * g[..., half:rope_dim]) * rot
+    y = g.copy()
+    y[..., :half] = zc.real
+    y[..., half:rope_dim] = zc.imag
+    return y
+
+
+def attention_backward_one_sequence(q, k, v, sink, dout, *, window, rope_base, scale,
+                                    rope_dim=64):
+    """Gradients of sum(dout * out) for one sequence (float64 arrays as in
+    :func:`attention_one_sequence`; dout [S, hq, dv]).  Returns dq, dk, dv,
+    dsink [hq]."""
+    S, hq, dqk = q.shape
+    hkv, dv = k.shape[1], v.shape[2]
+    G = hq // hkv
+    pos = np.arange(S)
+    qh = rope_complex(np.transpose(q, (1, 0, 2)), pos, rope_base, rope_dim)
+    kh = rope_complex(np.transpose(k, (1, 0, 2)), pos, rope_base, rope_dim)
+    vh = np.transpose(v, (1, 0, 2))
+    gh = np.transpose(dout, (1, 0, 2))
+    mask = visible_mask(S, S, pos, window)
+    dqr = np.zeros((hq, S, dqk))
+    dkr = np.zeros((hkv, S, dqk))
+    dvh = np.zeros((hkv, S, dv))
+    dsink = np.zeros(hq)
+    for h in range(hq):
+        g = h // G
+        logits = np.where(mask, scale * qh[h] @ kh[g].T, -np.inf)
+        full = np.concatenate([logits, np.full((S, 1), float(sink[h]))], axis=1)
+        e = np.exp(full - full.max(axis=1, keepdims=True))
+        P = e / e.sum(axis=1, keepdims=True)                       # [S, S + 1]
+        vext = np.concatenate([vh[g], np.zeros((1, dv))], axis=0)
+        dP = gh[h] @ vext.T                                        # [S, S + 1]
+        dZ = P * (dP - (dP * P).sum(axis=1, keepdims=True))
+        dsink[h] = dZ[:, S].sum()
+        dZk = dZ[:, :S]
+        dqr[h] = scale * dZk @ kh[g]
+        dkr[g] += scale * dZk.T @ qh[h]
+        dvh[g] += P[:, :S].T @ gh[h]
+    dq = np.transpose(rope_complex_transposed(dqr, pos, rope_base, rope_dim), (1, 0, 2))
+    dk = np.transpose(rope_complex_transposed(dkr, pos, rope_base, rope_dim), (1, 0, 2))
+    return dq, dk, np.transpose(dvh, (1, 0, 2)), dsink
+
+
+def prefill_backward(q, k, v, sink, dout, cu_seqlens, *, window, rope_base, scale, rope_dim=64):
+    """Packed varlen backward (float64 results), one sequence at a time."""
+    qd, kd, vd, gd = bf16_to_f64(q), bf16_to_f64(k), bf16_to_f64(v), bf16_to_f64(dout)
+    sd = np.asarray(sink, dtype=np.float64).reshape(-1)
+    cu = np.asarray(cu_seqlens).reshape(-1)
+    dqs, dks, dvs = [], [], []
+    dsink = np.zeros(sd.shape[0])
+    for b in range(len(cu) - 1):
+        a, e = int(cu[b]), int(cu[b + 1])
+        dq, dk, dv, ds = attention_backward_one_sequence(
+            qd[a:e], kd[a:e], vd[a:e], sd, gd[a:e], window=window, rope_base=rope_base,
+            scale=scale, rope_dim=rope_dim)
+        dqs.append(dq)
+        dks.append(dk)
+        dvs.append(dv)
+        dsink += ds
+    return np.concatenate(dqs, 0), np.concatenate(dks, 0), np.concatenate(dvs, 0), dsink

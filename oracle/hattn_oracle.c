@@ -343,3 +343,157 @@ int hattn_oracle_decode(const uint16_t* q, const uint16_t* k_hist, const uint16_
     free(th);
     return bad;
 }
+
+/*
+ * Backward of the prefill: the gradients of the scalar sum(dout * out) with
+ * respect to q, k, v and the sink logits, i.e. the chain rule through the
+ * forward definition above (MiMo-V2-Flash paper review, section 3.2: the sink
+ * is a learnable per-head parameter, so its gradient is part of the step; the
+ * sink carries no value, so it enters only through the softmax denominator).
+ * Written out per row, in the forward's notation:
+ *   z_j = scale * q'.k'_j over the visible keys, p_j = exp(z_j - lse),
+ *   p_sink = exp(sink - lse), o = sum_j p_j v_j;
+ *   delta = dout . o;  dp_j = dout . v_j;  dz_j = p_j (dp_j - delta);
+ *   dsink += -p_sink * delta;
+ *   dq' += scale * sum_j dz_j k'_j;  dk'_j += scale * dz_j q';  dv_j += p_j dout;
+ * then dq, dk = the transposed rotation of dq', dk' (pairs (i, i + R/2) turned
+ * back by the same angle).  o and lse are recomputed here in double, not taken
+ * from any forward output.
+ *   dout bf16 [total, hq, dv];  dq double [total, hq, dqk], dk [total, hkv, dqk],
+ *   dv double [total, hkv, dv], dsink double [hq]
+ * Work is split by (sequence, KV head): each task owns its keys' dk, dv rows
+ * and its queries' dq rows, so the tasks write disjoint outputs; the sink
+ * gradient is summed over the tasks afterwards, in task order.
+ */
+static void rope_apply_transposed(double* g, int rope_dim, const double* c, const double* s) {
+    int half = rope_dim / 2;
+    for (int i = 0; i < half; ++i) {
+        double a = g[i], b = g[i + half];
+        g[i] = a * c[i] + b * s[i];
+        g[i + half] = b * c[i] - a * s[i];
+    }
+}
+
+int hattn_oracle_prefill_backward(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  const double* sink, const uint16_t* dout, double* dq, double* dk,
+                                  double* dv_out, double* dsink, int batch, const int* cu_seqlens,
+                                  int hq, int hkv, int dqk, int dv, int rope_dim, double rope_base,
+                                  int window, double scale, int nthreads) {
+    if (!q || !k || !v || !sink || !dout || !dq || !dk || !dv_out || !dsink || !cu_seqlens ||
+        batch <= 0 || hq <= 0 || hkv <= 0 || hq % hkv || dqk <= 0 || dv <= 0 || rope_dim < 0 ||
+        rope_dim > dqk || (rope_dim & 1) || window < 0)
+        return ORACLE_BAD_ARG;
+    int G = hq / hkv;
+    int maxlen = 0;
+    for (int b = 0; b < batch; ++b) {
+        int L = cu_seqlens[b + 1] - cu_seqlens[b];
+        if (L < 0) return ORACLE_BAD_ARG;
+        if (L > maxlen) maxlen = L;
+    }
+    double* th = rope_thetas(rope_dim, rope_base);
+    double* ds_task = (double*)calloc((size_t)batch * hkv * G, sizeof(double));
+    if (!th || !ds_task) {
+        free(th); free(ds_task);
+        return ORACLE_NO_MEM;
+    }
+    int bad = 0;
+    int nt = omp_threads_used(nthreads);
+    long ntask = (long)batch * hkv;
+    long ml = maxlen > 0 ? maxlen : 1;
+#pragma omp parallel num_threads(nt)
+    {
+        int half = rope_dim / 2 + 1;
+        double* c = (double*)malloc(sizeof(double) * (size_t)half);
+        double* s = (double*)malloc(sizeof(double) * (size_t)half);
+        double* xd = (double*)malloc(sizeof(double) * (size_t)dqk);
+        double* kr = (double*)malloc(sizeof(double) * (size_t)ml * dqk);  /* rotated keys */
+        double* vd = (double*)malloc(sizeof(double) * (size_t)ml * dv);
+        double* gk = (double*)malloc(sizeof(double) * (size_t)ml * dqk);  /* dk' */
+        double* gv = (double*)malloc(sizeof(double) * (size_t)ml * dv);
+        double* qr = (double*)malloc(sizeof(double) * (size_t)dqk);
+        double* gq = (double*)malloc(sizeof(double) * (size_t)dqk);       /* dq' */
+        double* go = (double*)malloc(sizeof(double) * (size_t)dv);
+        double* o = (double*)malloc(sizeof(double) * (size_t)dv);
+        double* z = (double*)malloc(sizeof(double) * (size_t)ml);
+        if (!c || !s || !xd || !kr || !vd || !gk || !gv || !qr || !gq || !go || !o || !z) {
+#pragma omp atomic write
+            bad = ORACLE_NO_MEM;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long task = 0; task < ntask; ++task) {
+                int b = (int)(task / hkv), g = (int)(task % hkv);
+                long tok0 = cu_seqlens[b];
+                long L = cu_seqlens[b + 1] - tok0;
+                for (long j = 0; j < L; ++j) {
+                    const uint16_t* ks = k + ((tok0 + j) * hkv + g) * (long)dqk;
+                    for (int d = 0; d < dqk; ++d) xd[d] = bf16_to_double(ks[d]);
+                    rope_angles(j, rope_dim, th, c, s);
+                    rope_apply(xd, kr + j * dqk, dqk, rope_dim, c, s);
+                    const uint16_t* vs = v + ((tok0 + j) * hkv + g) * (long)dv;
+                    for (int e = 0; e < dv; ++e) vd[j * dv + e] = bf16_to_double(vs[e]);
+                }
+                for (long j = 0; j < L * dqk; ++j) gk[j] = 0.0;
+                for (long j = 0; j < L * dv; ++j) gv[j] = 0.0;
+                for (int hh = 0; hh < G; ++hh) {
+                    int h = g * G + hh;
+                    double dsink_h = 0.0;
+                    for (long p = 0; p < L; ++p) {
+                        long n = tok0 + p;
+                        long lo = (window > 0 && p - window + 1 > 0) ? p - window + 1 : 0;
+                        const uint16_t* qs = q + (n * hq + h) * (long)dqk;
+                        for (int d = 0; d < dqk; ++d) xd[d] = bf16_to_double(qs[d]);
+                        rope_angles(p, rope_dim, th, c, s);
+                        rope_apply(xd, qr, dqk, rope_dim, c, s);
+                        const uint16_t* gs = dout + (n * hq + h) * (long)dv;
+                        for (int e = 0; e < dv; ++e) go[e] = bf16_to_double(gs[e]);
+                        /* forward again: logits, lse (with the sink), o */
+                        double m = sink[h];
+                        for (long j = lo; j <= p; ++j) {
+                            z[j] = scale * dot(qr, kr + j * dqk, dqk);
+                            if (z[j] > m) m = z[j];
+                        }
+                        double Z = exp(sink[h] - m);
+                        for (long j = lo; j <= p; ++j) Z += exp(z[j] - m);
+                        double lse = m + log(Z);
+                        for (int e = 0; e < dv; ++e) o[e] = 0.0;
+                        for (long j = lo; j <= p; ++j) {
+                            double pj = exp(z[j] - lse);
+                            for (int e = 0; e < dv; ++e) o[e] += pj * vd[j * dv + e];
+                        }
+                        double delta = dot(go, o, dv);
+                        dsink_h += -exp(sink[h] - lse) * delta;
+                        for (int d = 0; d < dqk; ++d) gq[d] = 0.0;
+                        for (long j = lo; j <= p; ++j) {
+                            double pj = exp(z[j] - lse);
+                            double dz = pj * (dot(go, vd + j * dv, dv) - delta);
+                            for (int d = 0; d < dqk; ++d) {
+                                gq[d] += scale * dz * kr[j * dqk + d];
+                                gk[j * dqk + d] += scale * dz * qr[d];
+                            }
+                            for (int e = 0; e < dv; ++e) gv[j * dv + e] += pj * go[e];
+                        }
+                        rope_apply_transposed(gq, rope_dim, c, s);
+                        for (int d = 0; d < dqk; ++d) dq[(n * hq + h) * (long)dqk + d] = gq[d];
+                    }
+                    ds_task[task * G + hh] = dsink_h;
+                }
+                for (long j = 0; j < L; ++j) {
+                    rope_angles(j, rope_dim, th, c, s);
+                    rope_apply_transposed(gk + j * dqk, rope_dim, c, s);
+                    for (int d = 0; d < dqk; ++d)
+                        dk[((tok0 + j) * hkv + g) * (long)dqk + d] = gk[j * dqk + d];
+                    for (int e = 0; e < dv; ++e)
+                        dv_out[((tok0 + j) * hkv + g) * (long)dv + e] = gv[j * dv + e];
+                }
+            }
+        }
+        free(c); free(s); free(xd); free(kr); free(vd); free(gk); free(gv); free(qr); free(gq);
+        free(go); free(o); free(z);
+    }
+    for (int h = 0; h < hq; ++h) dsink[h] = 0.0;
+    for (long task = 0; task < ntask; ++task)
+        for (int hh = 0; hh < G; ++hh) dsink[(task % hkv) * G + hh] += ds_task[task * G + hh];
+    free(th);
+    free(ds_task);
+    return bad;
+}
