@@ -44,6 +44,9 @@ SIGNATURES = {
                            _P, _Z, _P]),
     "hattn_prefill_cached": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _I,
                                   _I, _I, _I, _I, _F, _I, _F, _P, _Z, _P]),
+    "hattn_prefill_backward_workspace_size": (_Z, [_L, _I, _I]),
+    "hattn_prefill_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _L, _I, _I,
+                                    _I, _I, _I, _I, _F, _I, _F, _P, _Z, _P]),
     "hattn_rope_kv_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "hattn_decode_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "hattn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -114,6 +117,23 @@ hattn_status_string = status_string
 
 def hattn_prefill_workspace_size(total_tokens, hkv, dqk=D_QK) -> int:
     return load_library().hattn_prefill_workspace_size(int(total_tokens), int(hkv), int(dqk))
+
+
+def hattn_prefill_backward_workspace_size(total_tokens, hq, hkv) -> int:
+    return load_library().hattn_prefill_backward_workspace_size(int(total_tokens), int(hq),
+                                                                int(hkv))
+
+
+def hattn_prefill_backward(q, k, v, sink, out, lse, dout, grad_q, grad_k, grad_v, grad_sink, batch,
+                           cu_seqlens, total_tokens, max_seqlen, hq, hkv, dqk, dv, rope_dim,
+                           rope_base, window, softmax_scale, workspace, workspace_bytes,
+                           stream=None) -> int:
+    return load_library().hattn_prefill_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(out), _ptr(lse), _ptr(dout), _ptr(grad_q),
+        _ptr(grad_k), _ptr(grad_v), _ptr(grad_sink), int(batch), _ptr(cu_seqlens),
+        int(total_tokens), int(max_seqlen), int(hq), int(hkv), int(dqk), int(dv), int(rope_dim),
+        float(rope_base), int(window), float(softmax_scale), _ptr(workspace),
+        int(workspace_bytes), _stream(stream))
 
 
 def hattn_prefill(q, k, v, sink, out, lse, batch, cu_seqlens, total_tokens, max_seqlen, hq, hkv,
@@ -233,6 +253,28 @@ def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_bas
                          max_seqlen, hq, hkv, dqk, dv, ROPE_DIM, rope_base, window, softmax_scale,
                          workspace, workspace.numel()), "hattn_prefill")
     return out, lse
+
+
+def prefill_backward(q, k, v, sink, out, lse, dout, cu_seqlens, *, max_seqlen: int, window: int,
+                     rope_base: float, softmax_scale: float | None = None, workspace=None):
+    """Gradients of one layer's prefill; returns (grad_q, grad_k, grad_v, grad_sink).
+    out and lse are the forward's results for the same inputs."""
+    total, hq, dqk = q.shape
+    hkv, dv = k.shape[1], v.shape[2]
+    if softmax_scale is None:
+        softmax_scale = dqk ** -0.5
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dvv = torch.empty_like(v)
+    ds = torch.empty((hq,), dtype=torch.float32, device=q.device)
+    need = hattn_prefill_backward_workspace_size(total, hq, hkv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(hattn_prefill_backward(q, k, v, sink, out, lse, dout, dq, dk, dvv, ds,
+                                  cu_seqlens.numel() - 1, cu_seqlens, total, max_seqlen, hq, hkv,
+                                  dqk, dv, ROPE_DIM, rope_base, window, softmax_scale, workspace,
+                                  workspace.numel()), "hattn_prefill_backward")
+    return dq, dk, dvv, ds
 
 
 def prefill_cached(q, k_new, v_new, k_cache, v_cache, cu_seqlens, prefix_lens, sink, *,

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhattn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["hattn_api.cu", "prefill_tc.cu", "decode.cu", "rope_append.cu",
-           "decode_static_scratch.cu"]
+           "decode_static_scratch.cu", "backward.cu"]
 HEADERS = ["common.cuh", "hattn_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -174,6 +174,88 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
   return HATTN_OK;
 }
 
+size_t hattn_prefill_backward_workspace_size(long total_tokens, int hq, int hkv) {
+  if (total_tokens <= 0 || hq <= 0 || hkv <= 0) return 0;
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t t = size_t(total_tokens);
+  return r256(t * hq * kRopeDim * 2) + r256(t * hkv * kRopeDim * 2) + r256(t * hq * 4) +
+         r256(size_t(backward_prep_blocks(total_tokens)) * hq * 4);
+}
+
+hattn_status_t hattn_prefill_backward(const void* q, const void* k, const void* v,
+                                      const float* sink, const void* out, const float* lse,
+                                      const void* dout, void* grad_q, void* grad_k, void* grad_v,
+                                      float* grad_sink, int batch, const int* cu_seqlens,
+                                      long total_tokens, int max_seqlen, int hq, int hkv, int dqk,
+                                      int dv, int rope_dim, float rope_base, int window,
+                                      float softmax_scale, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
+  if (st != HATTN_OK) return st;
+  if (batch <= 0 || total_tokens < 0 || max_seqlen < 0 || window < 0) return HATTN_ERR_INVALID_ARG;
+  if (total_tokens > 2147483647L || max_seqlen > total_tokens) return HATTN_ERR_INVALID_ARG;
+  if (!finite_positive(rope_base) || !finite_positive(softmax_scale)) return HATTN_ERR_INVALID_ARG;
+  if (!grad_sink || reinterpret_cast<uintptr_t>(grad_sink) & 3u) return HATTN_ERR_INVALID_ARG;
+  if (total_tokens == 0) {
+    // no rows: the sink gradient is an empty sum
+    return cudaMemsetAsync(grad_sink, 0, size_t(hq) * 4, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? HATTN_OK
+               : HATTN_ERR_CUDA;
+  }
+  if (!q || !k || !v || !sink || !out || !lse || !dout || !grad_q || !grad_k || !grad_v ||
+      !cu_seqlens)
+    return HATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(grad_q) || !aligned16(grad_k) || !aligned16(grad_v) || !aligned16(workspace))
+    return HATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(sink) & 3u || reinterpret_cast<uintptr_t>(lse) & 3u ||
+      reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)
+    return HATTN_ERR_INVALID_ARG;
+  if (size_t(8) * hq * 4 > 48 * 1024) return HATTN_ERR_UNSUPPORTED;  // prep-pass partials
+  if (!workspace ||
+      workspace_bytes < hattn_prefill_backward_workspace_size(total_tokens, hq, hkv))
+    return HATTN_ERR_WORKSPACE;
+  DeviceCtl ctl;
+  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t t = size_t(total_tokens);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BackwardArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = grad_q;
+  a.dk = grad_k;
+  a.dv = grad_v;
+  a.dsink = grad_sink;
+  a.cu_seqlens = cu_seqlens;
+  a.batch = batch;
+  a.total = total_tokens;
+  a.max_seqlen = max_seqlen;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.window = window >= max_seqlen ? 0 : window;  // a window covering every key is global
+  a.scale = softmax_scale;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  make_rope_freqs(rope_base, &a.freqs);
+  a.ctl = ctl;
+  a.q_rot = ws;
+  ws += r256(t * hq * kRopeDim * 2);
+  a.k_rot = ws;
+  ws += r256(t * hkv * kRopeDim * 2);
+  a.delta = reinterpret_cast<float*>(ws);
+  ws += r256(t * hq * 4);
+  a.sink_part = reinterpret_cast<float*>(ws);
+  a.nprep = backward_prep_blocks(total_tokens);
+  if (launch_backward(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return HATTN_ERR_CUDA;
+  return HATTN_OK;
+}
+
 hattn_status_t hattn_prefill_cached(const void* q, const void* k_new, const void* v_new,
                                     void* k_cache, void* v_cache, const int* cu_seqlens,
                                     const int* prefix_lens, const float* sink, void* out,

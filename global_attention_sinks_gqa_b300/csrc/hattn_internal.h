@@ -121,6 +121,37 @@ int decode_num_splits(int max_seqlen_k, int T, int window, int is_ring, int cap,
 size_t decode_workspace_bytes(int B, int T, int hq, int nsplit);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// ---- backward of the prefill (backward.cu) ---------------------------------
+struct BackwardArgs {
+  const void* q;      // bf16 [total, hq, dqk], un-rotated
+  const void* k;      // bf16 [total, hkv, dqk], un-rotated
+  const void* v;      // bf16 [total, hkv, dv]
+  const float* sink;  // [hq]
+  const void* out;    // bf16 [total, hq, dv], the forward's output
+  const float* lse;   // [total, hq], the forward's lse (natural log, sink included)
+  const void* dout;   // bf16 [total, hq, dv]
+  void* dq;           // bf16 [total, hq, dqk]
+  void* dk;           // bf16 [total, hkv, dqk]
+  void* dv;           // bf16 [total, hkv, dv]
+  float* dsink;       // [hq]
+  const int* cu_seqlens;
+  int batch;
+  long total;
+  int max_seqlen;
+  int hq, hkv, window;
+  float scale, scale_log2;
+  RopeFreqs freqs;
+  DeviceCtl ctl;
+  // workspace
+  void* q_rot;       // bf16 [total, hq, 64]: rotated dims of q
+  void* k_rot;       // bf16 [total, hkv, 64]
+  float* delta;      // [total, hq]: dout . out
+  float* sink_part;  // [nprep, hq]: sink-gradient partial sums of the prep blocks
+  long nprep;
+};
+long backward_prep_blocks(long total);
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
+
 // ---- status ------------------------------------------------------------------
 cudaError_t launch_lost_arrival_selftest(const DeviceCtl& ctl, cudaStream_t s);
 

@@ -114,6 +114,50 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of workspace hattn_prefill_backward() needs: the rotated dims 0..63 of
+ * q and k (total_tokens * (hq + hkv) * 64 bf16 values), delta = dout . out
+ * (total_tokens * hq floats) and the sink-gradient partials of the prep pass
+ * (ceil(total_tokens / 32) * hq floats), each rounded up to 256 bytes.  All of
+ * it is rewritten by every call: a workspace serves one call at a time.
+ */
+size_t hattn_prefill_backward_workspace_size(long total_tokens, int hq, int hkv);
+
+/*
+ * Backward of hattn_prefill(): the gradients of sum(dout * out) with respect
+ * to q, k, v and the sink logits (the sink is a learnable per-head parameter:
+ * MiMo-V2-Flash paper review, section 3.2).  With p_j = exp(z_j - lse), the
+ * forward's weights, and delta = dout . out per row:
+ *   dv_j = sum over rows of p_j dout;   dz_j = p_j (dout . v_j - delta);
+ *   dq = R^T scale sum_j dz_j k'_j;     dk_j = R^T scale sum over rows of dz_j q';
+ *   dsink_h = -sum over rows of head h of exp(sink_h - lse) delta,
+ * R the row's RoPE rotation (dims 0..63), q', k' the rotated vectors.
+ *
+ *   q, k, v, sink  the forward's inputs (same layouts as hattn_prefill())
+ *   out        bf16 [total_tokens, hq, dv]  the forward's output
+ *   lse        fp32 [total_tokens, hq]      the forward's lse (required)
+ *   dout       bf16 [total_tokens, hq, dv]  gradient of the loss w.r.t. out
+ *   grad_q     bf16 [total_tokens, hq, dqk]  written
+ *   grad_k     bf16 [total_tokens, hkv, dqk] written (summed over the G query
+ *              heads of each KV head)
+ *   grad_v     bf16 [total_tokens, hkv, dv]  written
+ *   grad_sink  fp32 [hq] DEVICE, written (summed over every row of the head)
+ *   workspace  DEVICE scratch of >= hattn_prefill_backward_workspace_size()
+ *   other arguments as for hattn_prefill().  Outputs must not overlap inputs
+ *   or the workspace.  Every gradient row is written by one thread and no
+ *   atomics are used: the results are the same on every run.  The products
+ *   take bf16 operands (P, dS and the rotated dims rounded to bf16) with fp32
+ *   accumulation.
+ */
+hattn_status_t hattn_prefill_backward(const void* q, const void* k, const void* v,
+                                      const float* sink, const void* out, const float* lse,
+                                      const void* dout, void* grad_q, void* grad_k, void* grad_v,
+                                      float* grad_sink, int batch, const int* cu_seqlens,
+                                      long total_tokens, int max_seqlen, int hq, int hkv, int dqk,
+                                      int dv, int rope_dim, float rope_base, int window,
+                                      float softmax_scale, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
  * Rotate new keys and write them and their values into the KV cache.
  *
  *   k_new     bf16 [B, T, hkv, dqk]   un-rotated keys of the T new tokens
