@@ -654,6 +654,88 @@ def run_prefix_prefill(args):
             "algorithmic": {"flops": flops, "bytes": byts}, "clocks": clk.summary()}
 
 
+BWD_PAIR_FLOPS = 2 * (3 * D_QK + 2 * D_V)  # S, dQ, dK (192 deep) and dP, dV (128) per pair
+
+
+def run_backward(args):
+    """Backward of one window layer (64q/8kv, W 128, base 1e4) and one global
+    layer (64q/4kv, base 5e6) over 32768 tokens each: hattn_prefill_backward
+    per layer per step (the forward's out / lse are computed once, untimed)."""
+    import global_attention_sinks_gqa_b300 as ha
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    sptr = torch.cuda.current_stream(dev).cuda_stream
+    layers = []
+    for name in ("swa_prefill_32k", "ga_prefill_32k"):
+        p = synth.CONFIGS[name]
+        c = synth.prefill_case(p["seqlens"], p["hq"], p["hkv"], window=p["window"],
+                               rope_base=p["rope_base"], seed=p["seed"], device=dev)
+        S = c.total
+        g = synth.randn_bf16((S, c.hq, D_V), synth._gen(p["seed"] + 100, dev), dev)
+        out, lse = ha.prefill(c.q, c.k, c.v, c.sink, c.cu_seqlens, max_seqlen=S,
+                              window=c.window, rope_base=c.rope_base)
+        ws = torch.empty(ha.hattn_prefill_backward_workspace_size(S, c.hq, c.hkv),
+                         dtype=torch.uint8, device=dev)
+        grads = (torch.empty_like(c.q), torch.empty_like(c.k), torch.empty_like(c.v),
+                 torch.empty((c.hq,), dtype=torch.float32, device=dev))
+        pairs = prefill_pairs(S, c.window)
+        # read q, out, dout, lse, k, v; write dq, dk, dv
+        byts = S * (c.hq * (2 * D_QK * 2 + 2 * D_V * 2 + 4) + c.hkv * 2 * (D_QK + D_V) * 2)
+        layers.append(dict(name=name, c=c, g=g, out=out, lse=lse, ws=ws, grads=grads, S=S,
+                           flops=BWD_PAIR_FLOPS * c.hq * pairs, bytes=byts))
+
+    def run_layer(L):
+        c, (dq, dk, dv, ds) = L["c"], L["grads"]
+        st = ha.hattn_prefill_backward(c.q, c.k, c.v, c.sink, L["out"], L["lse"], L["g"], dq, dk,
+                                       dv, ds, 1, c.cu_seqlens, L["S"], L["S"], c.hq, c.hkv, D_QK,
+                                       D_V, R, c.rope_base, c.window, c.scale, L["ws"],
+                                       L["ws"].numel(), sptr)
+        assert st == 0, ha.status_string(st)
+
+    for _ in range(args.warmup):
+        for L in layers:
+            run_layer(L)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        for e in ev:
+            e[0].record()
+            run_layer(layers[0])
+            e[1].record()
+            run_layer(layers[1])
+            e[2].record()
+        torch.cuda.synchronize()
+    ha.check_device_status()
+    t_swa = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps / 1e3
+    t_ga = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps / 1e3
+    t = ev[0][0].elapsed_time(ev[-1][2]) / args.steps / 1e3
+    hbm, tf_burst, tf_sust, src = measured_peaks()
+    flops = sum(L["flops"] for L in layers)
+    swa, ga = layers
+    ga_tf = ga["flops"] / t_ga / 1e12
+    return {"metric": "prefill backward TFLOP/s (SWA+GA sink attention) vs B300 roofline",
+            "value": round(flops / t / 1e12, 3), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v/dout, N(0,1) fp32 sinks)",
+            "config": {"workload": "backward: one window layer (32768 tokens, 64q/8kv, W 128) "
+                                   "and one global layer (32768 tokens, 64q/4kv)",
+                       "flop_per_pair": BWD_PAIR_FLOPS},
+            "roofline": {"bound": "tensor", "achieved": round(ga_tf, 2), "peak": tf_sust,
+                         "unit": "TFLOP/s", "frac": round(ga_tf / tf_sust, 4), "traffic": None,
+                         "kernel": "global layer backward (dK/dV + dQ kernels)",
+                         "peak_source": f"{src} bf16_tflops_sustained"},
+            "parts": {"swa_backward": {"ms": round(t_swa * 1e3, 4),
+                                       "GB/s": round(swa["bytes"] / t_swa / 1e9, 1),
+                                       "frac_hbm": round(swa["bytes"] / t_swa / 1e9 / hbm, 4),
+                                       "bytes": swa["bytes"]},
+                      "ga_backward": {"ms": round(t_ga * 1e3, 4), "TFLOP/s": round(ga_tf, 2),
+                                      "frac_tensor_sustained": round(ga_tf / tf_sust, 4),
+                                      "flops": ga["flops"]}},
+            "clocks": clk.summary()}
+
+
 def run_paged_decode(args):
     """The global layer's decode step of the bench (batch 64 x 4 verify tokens,
     lengths U[8192, 65536]) over a paged copy of its cache: pages of 256
@@ -786,16 +868,22 @@ def main():
     ap.add_argument("--seq", type=int, default=0, help="prefill length for --profile-case")
     ap.add_argument("--batch", type=int, default=0, help="decode batch for --profile-case")
     ap.add_argument("--workload", default="step",
-                    choices=["step", "hybrid_block_256k", "prefix_prefill", "paged_decode"],
-                    help="step: the default bench step; hybrid_block_256k: config 5 alone; "
+                    choices=["step", "hybrid_block_256k", "prefix_prefill", "paged_decode",
+                             "backward"],
+                    help="step: the default bench step; hybrid_block_256k: one hybrid block "
+                         "(5 window + 1 global layer) over 262144 tokens; "
                          "prefix_prefill: 4096 new tokens over a cached 28672-token prefix; "
-                         "paged_decode: the global decode step over a paged cache")
+                         "paged_decode: the global decode step over a paged cache; "
+                         "backward: the gradients of one window and one global layer")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
         return
     if args.workload == "hybrid_block_256k":
         print(json.dumps(run_hybrid_block(args)))
+        return
+    if args.workload == "backward":
+        print(json.dumps(run_backward(args)))
         return
     if args.workload == "prefix_prefill":
         print(json.dumps(run_prefix_prefill(args)))

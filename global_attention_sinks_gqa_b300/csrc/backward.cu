@@ -28,6 +28,10 @@
 // operands here (the forward uses fp16 for them); all products accumulate in
 // fp32.
 //
+// A key block's query tiles are walked from the sequence end down, so the
+// CTAs of one KV head that run at the same time read the same query tile
+// (L2 hits instead of one DRAM read per CTA).
+//
 // TMEM (512 columns).  dK/dV: S^T 0..63, dP^T 64..127, P^T 128..159 and dS^T
 // 160..191 (bf16 pairs), dV 192..319, dK 320..511; a tile's S^T / dP^T are
 // rewritten by the next tile's MMAs as soon as the row threads have read
@@ -58,26 +62,60 @@ __device__ __forceinline__ int seq_of(const int* cu, int batch, long t) {
   return lo;
 }
 
-// Rotate dims (2i, 2i+1) and (2i+32, 2i+33) of one head row, i = lane % 16.
-__device__ __forceinline__ void rotate_pair(const __nv_bfloat16* src, __nv_bfloat16* dst,
-                                            int i2, float2 cs0, float2 cs1) {
-  const uint32_t xr = *reinterpret_cast<const uint32_t*>(src + i2);
-  const uint32_t yr = *reinterpret_cast<const uint32_t*>(src + i2 + 32);
+// Rotated dims (2i, 2i+1) and (2i+32, 2i+33) of one head row (i = lane % 16)
+// from its raw pairs x = (2i, 2i+1), y = (2i+32, 2i+33).
+__device__ __forceinline__ uint2 rotate_pair(uint32_t xr, uint32_t yr, float2 cs0, float2 cs1) {
   const float2 x = unpack_bf16x2(xr), y = unpack_bf16x2(yr);
   const float a0 = x.x * cs0.x - y.x * cs0.y, a1 = x.y * cs1.x - y.y * cs1.y;
   const float b0 = y.x * cs0.x + x.x * cs0.y, b1 = y.y * cs1.x + x.y * cs1.y;
-  *reinterpret_cast<uint32_t*>(dst + i2) = pack_bf16x2(a0, a1);
-  *reinterpret_cast<uint32_t*>(dst + i2 + 32) = pack_bf16x2(b0, b1);
+  return make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(b0, b1));
+}
+
+// Rotated dims 0..63 of nh head rows of one token: half-warps take alternate
+// heads; kU head pairs are loaded before any is stored, so the loads of a
+// group are in flight together.
+template <int kU>
+__device__ __forceinline__ void rotate_heads(const __nv_bfloat16* __restrict__ src,
+                                             __nv_bfloat16* __restrict__ dst, int nh, int half,
+                                             int i2, float2 cs0, float2 cs1) {
+  for (int h0 = 0; h0 < nh; h0 += 2 * kU) {
+    uint32_t x[kU], y[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int h = h0 + 2 * u + half;
+      x[u] = y[u] = 0u;
+      if (h < nh) {
+        x[u] = __ldg(reinterpret_cast<const unsigned int*>(src + long(h) * kDqk + i2));
+        y[u] = __ldg(reinterpret_cast<const unsigned int*>(src + long(h) * kDqk + i2 + 32));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int h = h0 + 2 * u + half;
+      if (h < nh) {
+        const uint2 r = rotate_pair(x[u], y[u], cs0, cs1);
+        *reinterpret_cast<uint32_t*>(dst + long(h) * kRopeDim + i2) = r.x;
+        *reinterpret_cast<uint32_t*>(dst + long(h) * kRopeDim + i2 + 32) = r.y;
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kPrepWarps * 32)
     bwd_prep_kernel(const BackwardArgs a) {
   extern __shared__ float sp[];  // [warp][hq] sink partials
+  constexpr int kU = 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, i2 = 2 * (lane & 15);
   for (int h = threadIdx.x; h < kPrepWarps * a.hq; h += blockDim.x) sp[h] = 0.f;
   __syncthreads();
   float* spw = sp + warp * a.hq;
+  const __nv_bfloat16* __restrict__ q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* __restrict__ kk = static_cast<const __nv_bfloat16*>(a.k);
+  __nv_bfloat16* __restrict__ qr = static_cast<__nv_bfloat16*>(a.q_rot);
+  __nv_bfloat16* __restrict__ kr = static_cast<__nv_bfloat16*>(a.k_rot);
+  const uint4* __restrict__ o4 = static_cast<const uint4*>(a.out);
+  const uint4* __restrict__ g4 = static_cast<const uint4*>(a.dout);
   for (int k = 0; k < kPrepTok / kPrepWarps; ++k) {
     const long t = long(blockIdx.x) * kPrepTok + warp + k * kPrepWarps;
     if (t >= a.total) break;
@@ -85,38 +123,39 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
     const int p = int(t - __ldg(a.cu_seqlens + b));
     const float2 cs0 = rope_cos_sin(p, a.freqs.hi[i2], a.freqs.lo[i2]);
     const float2 cs1 = rope_cos_sin(p, a.freqs.hi[i2 + 1], a.freqs.lo[i2 + 1]);
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* kk = static_cast<const __nv_bfloat16*>(a.k);
-    __nv_bfloat16* qr = static_cast<__nv_bfloat16*>(a.q_rot);
-    __nv_bfloat16* kr = static_cast<__nv_bfloat16*>(a.k_rot);
-    for (int h = half; h < a.hq; h += 2)
-      rotate_pair(q + (t * a.hq + h) * kDqk, qr + (t * a.hq + h) * kRopeDim, i2, cs0, cs1);
-    for (int h = half; h < a.hkv; h += 2)
-      rotate_pair(kk + (t * a.hkv + h) * kDqk, kr + (t * a.hkv + h) * kRopeDim, i2, cs0, cs1);
+    rotate_heads<kU>(q + t * a.hq * kDqk, qr + t * a.hq * kRopeDim, a.hq, half, i2, cs0, cs1);
+    rotate_heads<kU>(kk + t * a.hkv * kDqk, kr + t * a.hkv * kRopeDim, a.hkv, half, i2, cs0, cs1);
     // delta = dout . out, 16 lanes per head row (8 dims each)
-    const uint4* o4 = static_cast<const uint4*>(a.out);
-    const uint4* g4 = static_cast<const uint4*>(a.dout);
-    for (int h0 = 0; h0 < a.hq; h0 += 2) {
-      const int h = h0 + half;
-      float d = 0.f;
-      if (h < a.hq) {
-        const uint4 ov = __ldg(o4 + (t * a.hq + h) * 16 + (lane & 15));
-        const uint4 gv = __ldg(g4 + (t * a.hq + h) * 16 + (lane & 15));
-        const uint32_t* ow = reinterpret_cast<const uint32_t*>(&ov);
-        const uint32_t* gw = reinterpret_cast<const uint32_t*>(&gv);
+    for (int h0 = 0; h0 < a.hq; h0 += 2 * kU) {
+      uint4 ov[kU], gv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int h = h0 + 2 * u + half;
+        ov[u] = gv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (h < a.hq) {
+          ov[u] = __ldg(o4 + (t * a.hq + h) * 16 + (lane & 15));
+          gv[u] = __ldg(g4 + (t * a.hq + h) * 16 + (lane & 15));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int h = h0 + 2 * u + half;
+        const uint32_t* ow = reinterpret_cast<const uint32_t*>(&ov[u]);
+        const uint32_t* gw = reinterpret_cast<const uint32_t*>(&gv[u]);
+        float d = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 x = unpack_bf16x2(ow[e]), y = unpack_bf16x2(gw[e]);
           d = fmaf(x.x, y.x, d);
           d = fmaf(x.y, y.y, d);
         }
-      }
 #pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      if ((lane & 15) == 0 && h < a.hq) {
-        a.delta[t * a.hq + h] = d;
-        const float ps = exp2f((__ldg(a.sink + h) - __ldg(a.lse + t * a.hq + h)) * kLog2e);
-        spw[h] -= ps * d;
+        for (int o = 8; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        if ((lane & 15) == 0 && h < a.hq) {
+          a.delta[t * a.hq + h] = d;
+          const float ps = exp2f((__ldg(a.sink + h) - __ldg(a.lse + t * a.hq + h)) * kLog2e);
+          spw[h] -= ps * d;
+        }
       }
     }
   }
@@ -128,12 +167,20 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
   }
 }
 
-__global__ void bwd_dsink_kernel(const BackwardArgs a) {
-  const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  if (h >= a.hq) return;
+// One block per head: thread i sums partials i, i + 256, ... in order, then a
+// fixed tree over the 256 sums (the same order on every run).
+__global__ void __launch_bounds__(256) bwd_dsink_kernel(const BackwardArgs a) {
+  __shared__ float red[256];
+  const int h = blockIdx.x;
   float s = 0.f;
-  for (int i = 0; i < a.nprep; ++i) s += a.sink_part[long(i) * a.hq + h];
-  a.dsink[h] = s;
+  for (long i = threadIdx.x; i < a.nprep; i += 256) s += a.sink_part[i * a.hq + h];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.dsink[h] = red[0];
 }
 
 // ---- shared pieces of the two MMA kernels -----------------------------------
@@ -228,7 +275,8 @@ __device__ __forceinline__ void bwd_init(BwdBars* bars, uint32_t st_full_count) 
 // ---- dK / dV -----------------------------------------------------------------
 
 // Unit u: (key block kb, sequence b, KV head g), key blocks in ascending order
-// so that a global layer's longest units (its first keys) start first.
+// so that a global layer's longest units (its first keys) start first; each
+// walks its query tiles from the last one down.
 template <int G, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mKr, const __grid_constant__ CUtensorMap mK,
@@ -283,7 +331,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < ntile; ++i) {
       const int s = i % kNst;
       if (i >= kNst && !warp_wait(&bars->st_empty[s], ((i / kNst) - 1) & 1, a.ctl, abort)) break;
-      const int tq0 = k0 + i * TQ;
+      const int tq0 = k0 + (ntile - 1 - i) * TQ;
       uint8_t* st = smem + kOffStage + s * kStageBytes;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->st_full[s], kStageBytes);
@@ -387,7 +435,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int i = 0; i < ntile; ++i) {
       const int s = i % kNst;
-      const int tq0 = k0 + i * TQ;
+      const int tq0 = k0 + (ntile - 1 - i) * TQ;
       if (!warp_wait(&bars->s_full, i & 1, a.ctl, abort)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[64], dp[64];
@@ -688,7 +736,7 @@ cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s) {
   bwd_prep_kernel<<<unsigned(a.nprep), kPrepWarps * 32, prep_smem, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dsink_kernel<<<unsigned((a.hq + 127) / 128), 128, 0, s>>>(a);
+  bwd_dsink_kernel<<<unsigned(a.hq), 256, 0, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.max_seqlen == 0) return e;
   switch (a.hq / a.hkv) {

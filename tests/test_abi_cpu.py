@@ -188,3 +188,44 @@ def test_oracle_is_not_reachable_from_the_product():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
                 assert "hattn_oracle" not in txt, f
+
+
+def test_backward_workspace_size(lib):
+    # rotated q and k dims 0..63 (bf16), delta (fp32), sink partials of
+    # 32-token blocks (fp32), each rounded to 256 bytes
+    n = ha.hattn_prefill_backward_workspace_size(32768, 64, 8)
+    assert n == 32768 * 64 * 128 + 32768 * 8 * 128 + 32768 * 64 * 4 + 1024 * 64 * 4
+    r = lambda x: (x + 255) // 256 * 256
+    assert ha.hattn_prefill_backward_workspace_size(33, 4, 2) == \
+        r(33 * 4 * 128) + r(33 * 2 * 128) + r(33 * 4 * 4) + r(2 * 4 * 4)
+    assert ha.hattn_prefill_backward_workspace_size(0, 4, 2) == 0
+
+
+def _backward(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, sink=FAKE, out=FAKE, lse=FAKE, dout=FAKE, grad_q=FAKE,
+                grad_k=FAKE, grad_v=FAKE, grad_sink=FAKE, batch=1, cu_seqlens=FAKE,
+                total_tokens=512, max_seqlen=512, hq=8, hkv=1, dqk=192, dv=128, rope_dim=64,
+                rope_base=1e4, window=128, softmax_scale=0.07, workspace=FAKE,
+                workspace_bytes=1 << 24, stream=0)
+    args.update(kw)
+    return ha.hattn_prefill_backward(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hkv=3), ha.HATTN_ERR_INVALID_ARG),
+    (dict(dqk=128), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(hq=64, hkv=2), ha.HATTN_ERR_UNSUPPORTED),      # G = 32
+    (dict(lse=None), ha.HATTN_ERR_INVALID_ARG),           # the backward needs the forward's lse
+    (dict(dout=None), ha.HATTN_ERR_INVALID_ARG),
+    (dict(grad_sink=None), ha.HATTN_ERR_INVALID_ARG),
+    (dict(grad_q=FAKE + 8), ha.HATTN_ERR_INVALID_ARG),    # misaligned
+    (dict(dout=FAKE + 2), ha.HATTN_ERR_INVALID_ARG),
+    (dict(window=-1), ha.HATTN_ERR_INVALID_ARG),
+    (dict(softmax_scale=float("inf")), ha.HATTN_ERR_INVALID_ARG),
+    (dict(max_seqlen=513), ha.HATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=1000), ha.HATTN_ERR_WORKSPACE),
+    (dict(workspace=None), ha.HATTN_ERR_WORKSPACE),
+    (dict(batch=0), ha.HATTN_ERR_INVALID_ARG),
+])
+def test_backward_rejects_bad_arguments(lib, kw, code):
+    assert _backward(**kw) == code
