@@ -20,7 +20,7 @@
 //                        P^T, dS^T (bf16, TMEM) and dV += P^T dout,
 //                        dK += dS^T Q' with both accumulators in TMEM;
 //   bwd_dq_kernel        one CTA per (sequence, KV head, 128-row query tile):
-//                        S = Q' K^T, dP = dout V^T over 64-key blocks, dS to
+//                        S = Q' K^T, dP = dout V^T over 128-key blocks, dS to
 //                        TMEM, dQ += dS K;
 //   bwd_dsink_kernel     the sink partials summed in block order.
 // Each gradient row is written once, by one thread, so no pass uses atomics
@@ -36,7 +36,10 @@
 // 160..191 (bf16 pairs), dV 192..319, dK 320..511; a tile's S^T / dP^T are
 // rewritten by the next tile's MMAs as soon as the row threads have read
 // them, so the tensor core runs the next tile while they compute.  dQ: S
-// 0..63, dP 64..127, dS 128..159, dQ 192..383.
+// 0..127, dP 128..255, dS 256..319, dQ 320..511.  An MMA costs about the same
+// to issue at N = 64 as at N = 128, so the dQ kernel takes 128-key blocks;
+// the dK/dV kernel stays at 64 query columns because dK (192 columns) and dV
+// (128) leave only 192 for the rest.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -221,13 +224,14 @@ __device__ __forceinline__ void store_row64(void* dst, const uint32_t* w) {
   for (int e = 0; e < 4; ++e) d[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
 }
 
-// Epilogue of a 192-dim gradient row held in TMEM columns col..col+191 of
-// this thread's lane: times f, dims 0..63 turned back by the row's RoPE angle
-// (the transpose of the forward rotation), bf16 to dst.  All lanes call it
-// (tcgen05.ld is warp-wide); only `write` lanes store.
-__device__ __forceinline__ void finish_qk_row(uint32_t taddr, float f, int pos,
-                                              const RopeFreqs& fr, bool write,
-                                              __nv_bfloat16* dst) {
+// Epilogue pieces of a 192-dim gradient row held in TMEM columns
+// taddr..taddr+191 of this thread's lane, times f, to bf16 at dst.  All lanes
+// call them (tcgen05.ld is warp-wide); only `write` lanes store.
+// Dims 0..63, turned back by the row's RoPE angle (the transpose of the
+// forward rotation):
+__device__ __forceinline__ void finish_rot64(uint32_t taddr, float f, int pos,
+                                             const RopeFreqs& fr, bool write,
+                                             __nv_bfloat16* dst) {
   uint32_t x[32], y[32];
   tmem_ld32_nowait(taddr, x);
   tmem_ld32_nowait(taddr + 32, y);
@@ -246,14 +250,15 @@ __device__ __forceinline__ void finish_qk_row(uint32_t taddr, float f, int pos,
     store_row64(dst, w);
     store_row64(dst + 32, w + 16);
   }
-#pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    uint32_t v[32], o[16];
-    tmem_ld32_nowait(taddr + 64 + 32 * ch, v);
-    tmem_ld_wait();
-    pack_scaled(v, f, o);
-    if (write) store_row64(dst + 64 + 32 * ch, o);
-  }
+}
+// 32 plain dims starting at dim d0:
+__device__ __forceinline__ void finish_chunk32(uint32_t taddr, float f, bool write,
+                                               __nv_bfloat16* dst, int d0) {
+  uint32_t v[32], o[16];
+  tmem_ld32_nowait(taddr + d0, v);
+  tmem_ld_wait();
+  pack_scaled(v, f, o);
+  if (write) store_row64(dst + d0, o);
 }
 
 __device__ __forceinline__ void bwd_init(BwdBars* bars, uint32_t st_full_count) {
@@ -487,8 +492,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pack_scaled(v, 1.f, o);
         if (jvalid) store_row64(dvr + 32 * ch, o);
       }
-      finish_qk_row(t_row + 320, a.scale, j, a.freqs, jvalid,
-                    static_cast<__nv_bfloat16*>(a.dk) + row * kDqk);
+      __nv_bfloat16* dkr = static_cast<__nv_bfloat16*>(a.dk) + row * kDqk;
+      finish_rot64(t_row + 320, a.scale, j, a.freqs, jvalid, dkr);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) finish_chunk32(t_row + 320, a.scale, jvalid, dkr, 64 + 32 * ch);
     }
   }
   tc_fence_before();
@@ -501,8 +508,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ---- dQ ----------------------------------------------------------------------
 
+// Shared memory of the dQ kernel: Q' and dout of the tile (5 boxes of
+// [128 rows][64 dims]), two K buffers of 128 keys (3 boxes each: K is read by
+// S = Q' K^T and again by dQ += dS K, which runs after the next block's S) and
+// one V buffer (2 boxes: V is read only by dP = dout V^T and is refilled as
+// soon as that completes).
+constexpr int kDqOffK = kFixedBytes;
+constexpr int kDqKBytes = 3 * kBoxBytes128;
+constexpr int kDqOffV = kDqOffK + 2 * kDqKBytes;
+constexpr int kDqOffBar = kDqOffV + 2 * kBoxBytes128;
+constexpr int kDqSmem = kDqOffBar + 256 + 1024;
+static_assert(kDqSmem <= 232448, "shared memory");
+
+struct DqBars {
+  uint64_t fixed_full, k_full[2], k_empty[2], v_full, v_empty;
+  uint64_t s_full, s_free, p_full, p_free, acc_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(DqBars) <= 256, "barrier area");
+
 // Unit u: (query tile, sequence b, KV head g); a global layer's latest (longest)
-// tiles first.
+// tiles first.  128-key blocks: TMEM S 0..127, dP 128..255, dS 256..319 (bf16
+// pairs), dQ 320..511.
 template <int G, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap mQr, const __grid_constant__ CUtensorMap mQ,
@@ -510,9 +538,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                   const BackwardArgs a, int nqt) {
   constexpr int TQ = 128 / G;  // tokens per 128-row tile
+  constexpr int BN = 128;      // keys per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_base_1k(smem_raw);
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + kOffBar);
+  DqBars* bars = reinterpret_cast<DqBars*>(smem + kDqOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -526,10 +555,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (t0 >= L) return;  // uniform over the CTA
   const int kstart = WIN ? max(0, t0 - a.window + 1) : 0;
   const int kend = min(L, t0 + TQ);
-  const int nblk = (kend - kstart + 63) / 64;
+  const int nblk = (kend - kstart + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
-    bwd_init(bars, 1);
+    mbar_init(&bars->fixed_full, 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&bars->k_full[j], 1);
+      mbar_init(&bars->k_empty[j], 1);
+    }
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 4);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    mbar_fence_init();
     fence_proxy_async_smem();
   }
   if (warp == 1) {
@@ -542,6 +585,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
+    // ---------------------------------------------------------------- loads
     if (lane == 0) {
       tma_prefetch_map(&mKr);
       tma_prefetch_map(&mK);
@@ -552,73 +596,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_load_3d(smem + 2 * kBoxBytes128, &mQ, &bars->fixed_full, 128, g * G, tok0 + t0);
       tma_load_3d(smem + 3 * kBoxBytes128, &mDO, &bars->fixed_full, 0, g * G, tok0 + t0);
       tma_load_3d(smem + 4 * kBoxBytes128, &mDO, &bars->fixed_full, 64, g * G, tok0 + t0);
-      int filled = 0;
+      int kfilled = 0, vfilled = 0;
       for (int i = 0; i < nblk; ++i) {
-        const int s = i % kNst;
-        if (i >= kNst && !mbar_wait(&bars->st_empty[s], ((i / kNst) - 1) & 1, a.ctl, abort))
-          break;
-        const int kr0 = tok0 + kstart + 64 * i;
-        uint8_t* st = smem + kOffStage + s * kStageBytes;
-        mbar_arrive_expect_tx(&bars->st_full[s], kStageBytes);
-        tma_load_3d(st, &mKr, &bars->st_full[s], 0, g, kr0);
-        tma_load_3d(st + kBoxBytes64, &mK, &bars->st_full[s], 64, g, kr0);
-        tma_load_3d(st + 2 * kBoxBytes64, &mK, &bars->st_full[s], 128, g, kr0);
-        tma_load_3d(st + 3 * kBoxBytes64, &mV, &bars->st_full[s], 0, g, kr0);
-        tma_load_3d(st + 4 * kBoxBytes64, &mV, &bars->st_full[s], 64, g, kr0);
-        filled = i + 1;
+        const int kr0 = tok0 + kstart + BN * i;
+        const int j = i & 1;
+        if (i >= 2 && !mbar_wait(&bars->k_empty[j], ((i >> 1) - 1) & 1, a.ctl, abort)) break;
+        uint8_t* kb = smem + kDqOffK + j * kDqKBytes;
+        mbar_arrive_expect_tx(&bars->k_full[j], kDqKBytes);
+        tma_load_3d(kb, &mKr, &bars->k_full[j], 0, g, kr0);
+        tma_load_3d(kb + kBoxBytes128, &mK, &bars->k_full[j], 64, g, kr0);
+        tma_load_3d(kb + 2 * kBoxBytes128, &mK, &bars->k_full[j], 128, g, kr0);
+        kfilled = i + 1;
+        if (i >= 1 && !mbar_wait(&bars->v_empty, (i - 1) & 1, a.ctl, abort)) break;
+        uint8_t* vb = smem + kDqOffV;
+        mbar_arrive_expect_tx(&bars->v_full, 2 * kBoxBytes128);
+        tma_load_3d(vb, &mV, &bars->v_full, 0, g, kr0);
+        tma_load_3d(vb + kBoxBytes128, &mV, &bars->v_full, 64, g, kr0);
+        vfilled = i + 1;
       }
+      // copies still in flight must land before the CTA may exit
       mbar_wait_drain(&bars->fixed_full, 0, a.ctl);
-      for (int i = max(0, filled - kNst); i < filled; ++i)
-        mbar_wait_drain(&bars->st_full[i % kNst], (i / kNst) & 1, a.ctl);
+      for (int i = max(0, kfilled - 2); i < kfilled; ++i)
+        mbar_wait_drain(&bars->k_full[i & 1], (i >> 1) & 1, a.ctl);
+      if (vfilled > 0) mbar_wait_drain(&bars->v_full, (vfilled - 1) & 1, a.ctl);
     }
   } else if (warp == 1) {
-    const uint32_t id_s = make_idesc_bf16(128, 64, 0, 0);
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t id_s = make_idesc_bf16(128, BN, 0, 0);
     const uint32_t id_dq = make_idesc_bf16(128, 192, 0, 1);
     const uint32_t sb = smem_u32(smem);
     const uint64_t qa = make_sdesc_sw128(sb, 16, 1024);                      // Q', K-major
     const uint64_t ga = make_sdesc_sw128(sb + 3 * kBoxBytes128, 16, 1024);   // dout, K-major
+    const uint64_t vd = make_sdesc_sw128(sb + kDqOffV, 16, 1024);            // V, K-major
     bool ok = warp_wait(&bars->fixed_full, 0, a.ctl, abort);
-    auto issue_s = [&](int i) {
-      const uint32_t st = sb + kOffStage + (i % kNst) * kStageBytes;
-      const uint64_t kd = make_sdesc_sw128(st, 16, 1024);
-      const uint64_t vd = make_sdesc_sw128(st + 3 * kBoxBytes64, 16, 1024);
+    // S(i) = Q' K_i^T once K_i has landed, then dP(i) = dout V_i^T once V_i has
+    auto issue_s = [&](int i) -> bool {
+      if (!warp_wait(&bars->k_full[i & 1], (i >> 1) & 1, a.ctl, abort)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t kd = make_sdesc_sw128(sb + kDqOffK + (i & 1) * kDqKBytes, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < 12; ++kk)
-        umma_ss(tmem, qa + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4),
-                kd + uint64_t(((kk >> 2) * kBoxBytes64 + (kk & 3) * 32) >> 4), id_s, kk > 0);
+        for (int kk = 0; kk < 12; ++kk)
+          umma_ss(tmem, qa + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4),
+                  kd + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4), id_s, kk > 0);
+      }
+      __syncwarp();
+      if (!warp_wait(&bars->v_full, i & 1, a.ctl, abort)) return false;
+      tc_fence_after();
+      if (lane == 0) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_ss(tmem + 64, ga + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4),
-                vd + uint64_t(((kk >> 2) * kBoxBytes64 + (kk & 3) * 32) >> 4), id_s, kk > 0);
-      umma_commit(&bars->s_full);
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + BN, ga + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4),
+                  vd + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4), id_s, kk > 0);
+        umma_commit(&bars->v_empty);
+        umma_commit(&bars->s_full);
+      }
+      __syncwarp();
+      return true;
     };
     bool issued = false;
     for (int i = 0; ok && i < nblk; ++i) {
-      const int s = i % kNst;
       if (i == 0) {
-        if (!warp_wait(&bars->st_full[0], 0, a.ctl, abort)) break;
-        tc_fence_after();
-        if (lane == 0) issue_s(0);
         issued = true;
+        if (!issue_s(0)) break;
       }
       if (i + 1 < nblk) {
-        const int s1 = (i + 1) % kNst;
-        if (!warp_wait(&bars->st_full[s1], ((i + 1) / kNst) & 1, a.ctl, abort)) break;
         if (!warp_wait(&bars->s_free, i & 1, a.ctl, abort)) break;
-        tc_fence_after();
-        if (lane == 0) issue_s(i + 1);
+        if (!issue_s(i + 1)) break;
       }
       if (!warp_wait(&bars->p_full, i & 1, a.ctl, abort)) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t st = sb + kOffStage + s * kStageBytes;
-        const uint64_t kb = make_sdesc_sw128(st, kBoxBytes64, 1024);  // K', MN-major
+        const uint64_t kb = make_sdesc_sw128(sb + kDqOffK + (i & 1) * kDqKBytes, kBoxBytes128,
+                                             1024);  // K', MN-major
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts(tmem + 192, tmem + 128 + kk * 8, kb + uint64_t((kk * 2048) >> 4), id_dq,
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts(tmem + 320, tmem + 2 * BN + kk * 8, kb + uint64_t((kk * 2048) >> 4), id_dq,
                   (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars->p_free);
-        umma_commit(&bars->st_empty[s]);
+        umma_commit(&bars->k_empty[i & 1]);
         if (i + 1 == nblk) umma_commit(&bars->acc_done);
       }
       __syncwarp();
@@ -639,35 +695,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_row = tmem + (uint32_t((warp & 3) * 32) << 16);
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
-      const int kb0 = kstart + 64 * i;
       if (!warp_wait(&bars->s_full, i & 1, a.ctl, abort)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[64], dp[64];
-      tmem_ld32_nowait(t_row, sv);
-      tmem_ld32_nowait(t_row + 32, sv + 32);
-      tmem_ld32_nowait(t_row + 64, dp);
-      tmem_ld32_nowait(t_row + 96, dp + 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free);
-      uint32_t dw[32];
-      const int d0 = p - kb0;  // query position minus key position, column 0
+      uint32_t dw[64];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float dc[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int d = d0 - (c + e);
-          const bool vis = valid && d >= 0 && (!WIN || d < a.window);
-          const float x = __uint_as_float(sv[c + e]) * a.scale_log2 - l2;
-          dc[e] = vis ? fast_exp2(x) * (__uint_as_float(dp[c + e]) - de) : 0.f;
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t sv[64], dp[64];
+        tmem_ld32_nowait(t_row + 64 * hb, sv);
+        tmem_ld32_nowait(t_row + 64 * hb + 32, sv + 32);
+        tmem_ld32_nowait(t_row + BN + 64 * hb, dp);
+        tmem_ld32_nowait(t_row + BN + 64 * hb + 32, dp + 32);
+        tmem_ld_wait();
+        if (hb == 1) {
+          // S and dP are in registers: the next block's products may overwrite them
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->s_free);
         }
-        dw[c >> 1] = pack_bf16x2(dc[0], dc[1]);
+        const int d0 = p - (kstart + BN * i + 64 * hb);  // query minus key position, column 0
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float dc[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = d0 - (c + e);
+            const bool vis = valid && d >= 0 && (!WIN || d < a.window);
+            const float x = __uint_as_float(sv[c + e]) * a.scale_log2 - l2;
+            dc[e] = vis ? fast_exp2(x) * (__uint_as_float(dp[c + e]) - de) : 0.f;
+          }
+          dw[32 * hb + (c >> 1)] = pack_bf16x2(dc[0], dc[1]);
+        }
       }
       if (i > 0 && !warp_wait(&bars->p_free, (i - 1) & 1, a.ctl, abort)) { ok = false; break; }
       tc_fence_after();
-      tmem_st32(t_row + 128, dw);
+      tmem_st32(t_row + 2 * BN, dw);
+      tmem_st32(t_row + 2 * BN + 32, dw + 32);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -675,8 +737,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok && warp_wait(&bars->acc_done, 0, a.ctl, abort)) {
       tc_fence_after();
-      finish_qk_row(t_row + 192, a.scale, p, a.freqs, valid,
-                    static_cast<__nv_bfloat16*>(a.dq) + orow * kDqk);
+      __nv_bfloat16* dqr = static_cast<__nv_bfloat16*>(a.dq) + orow * kDqk;
+      finish_rot64(t_row + 320, a.scale, p, a.freqs, valid, dqr);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) finish_chunk32(t_row + 320, a.scale, valid, dqr, 64 + 32 * ch);
     }
   }
   tc_fence_before();
@@ -694,7 +758,7 @@ cudaError_t launch_g(const BackwardArgs& a, cudaStream_t s) {
   auto qk = win ? bwd_dq_kernel<G, true> : bwd_dq_kernel<G, false>;
   cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(qk, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
+  e = cudaFuncSetAttribute(qk, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
   if (e != cudaSuccess) return e;
   CUtensorMap mKr128, mK128, mV128, mQr64, mQ64, mDO64;
   if (!make_map(&mKr128, a.k_rot, a.total, a.hkv, kRopeDim, 1, 128) ||
@@ -711,18 +775,15 @@ cudaError_t launch_g(const BackwardArgs& a, cudaStream_t s) {
                                                          a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  CUtensorMap mQr128, mQ128, mDO128, mKr64, mK64, mV64;
+  CUtensorMap mQr128, mQ128, mDO128;
   if (!make_map(&mQr128, a.q_rot, a.total, a.hq, kRopeDim, G, 128 / G) ||
       !make_map(&mQ128, a.q, a.total, a.hq, kDqk, G, 128 / G) ||
-      !make_map(&mDO128, a.dout, a.total, a.hq, kDv, G, 128 / G) ||
-      !make_map(&mKr64, a.k_rot, a.total, a.hkv, kRopeDim, 1, 64) ||
-      !make_map(&mK64, a.k, a.total, a.hkv, kDqk, 1, 64) ||
-      !make_map(&mV64, a.v, a.total, a.hkv, kDv, 1, 64))
+      !make_map(&mDO128, a.dout, a.total, a.hq, kDv, G, 128 / G))
     return cudaErrorInvalidValue;
   const int nqt = (a.max_seqlen + 128 / G - 1) / (128 / G);
   if (long(nqt) * per > 0x7fffffffL) return cudaErrorInvalidValue;
-  qk<<<unsigned(nqt * per), kBwdThreads, kBwdSmem, s>>>(mQr128, mQ128, mDO128, mKr64, mK64, mV64,
-                                                         a, nqt);
+  qk<<<unsigned(nqt * per), kBwdThreads, kDqSmem, s>>>(mQr128, mQ128, mDO128, mKr128, mK128,
+                                                        mV128, a, nqt);
   return cudaGetLastError();
 }
 
