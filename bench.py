@@ -338,7 +338,7 @@ def run_cuda(args, rank, world):
     ga = wl.layers[1]
     ga_s = part_ms["p1"] / 1e3
     flops = wl.flops()
-    value = flops * world / (ms / 1e3) / 1e12
+    value = whole_job_tflops(flops, world, ms)
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -499,12 +499,21 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest of the ranks' x (every rank gets it): the job's time is its
+    slowest rank's."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: every rank runs the same step (weak scaling), the
+    step takes the slowest rank's time."""
+    return flops_per_rank_step * world / (ms_per_step / 1e3) / 1e12
 
 
 def run_hybrid_block(args):

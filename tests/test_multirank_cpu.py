@@ -1,0 +1,60 @@
+"""The N > 1 host path of bench.py on CPU: two gloo ranks (127.0.0.1) take the
+barrier, agree on the slowest rank's time and form the whole-job value; the
+reference arm runs on rank 0 only."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        bench.barrier(world)
+        ms = 10.0 + 5.0 * rank           # rank 1 is the slow one
+        m = bench.max_over_ranks(ms, world)
+        value = bench.whole_job_tflops(2.0e12, world, m)
+        bench.barrier(world)
+        out[rank] = (m, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.start_processes(_rank, args=(world, port, out), nprocs=world, start_method="spawn",
+                           join=True)
+        res = dict(out)
+    assert res[0] == res[1]
+    m, value = res[0]
+    assert m == 15.0
+    # 2 ranks x 2e12 FLOPs per step in 15 ms
+    assert value == pytest.approx(2 * 2.0e12 / 0.015 / 1e12)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
+                       text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
