@@ -521,44 +521,58 @@ constexpr int kDqSmem = kDqOffBar + 256 + 1024;
 static_assert(kDqSmem <= 232448, "shared memory");
 
 struct DqBars {
-  uint64_t fixed_full, k_full[2], k_empty[2], v_full, v_empty;
-  uint64_t s_full, s_free, p_full, p_free, acc_done, drain;
+  uint64_t fixed_full, fixed_empty, k_full[2], k_empty[2], v_full, v_empty;
+  uint64_t s_full, s_free, p_full, p_free, acc_done, acc_free, drain;
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(DqBars) <= 256, "barrier area");
 
 // Unit u: (query tile, sequence b, KV head g); a global layer's latest (longest)
-// tiles first.  128-key blocks: TMEM S 0..127, dP 128..255, dS 256..319 (bf16
-// pairs), dQ 320..511.
+// tiles first.  An empty unit (tile past its sequence's end) is skipped.
+struct DqUnit {
+  int b, g, tok0, L, t0, kstart, nblk;
+};
+template <int G, bool WIN>
+__device__ __forceinline__ bool dq_unit(int u, const BackwardArgs& a, int nqt, DqUnit& du) {
+  constexpr int TQ = 128 / G;
+  const int per = a.batch * a.hkv;
+  const int q_ord = u / per, rem = u - q_ord * per;
+  const int qt = WIN ? q_ord : nqt - 1 - q_ord;
+  du.b = rem / a.hkv;
+  du.g = rem - du.b * a.hkv;
+  du.tok0 = __ldg(a.cu_seqlens + du.b);
+  du.L = __ldg(a.cu_seqlens + du.b + 1) - du.tok0;
+  du.t0 = qt * TQ;
+  if (du.t0 >= du.L) return false;
+  du.kstart = WIN ? max(0, du.t0 - a.window + 1) : 0;
+  const int kend = min(du.L, du.t0 + TQ);
+  du.nblk = (kend - du.kstart + 127) / 128;
+  return true;
+}
+
+// CTA c takes units c, c + grid, ... (a grid of one CTA per unit, or one per
+// SM); the block counters (K / V buffers, S / dS hand-offs) run on across
+// units, so a unit's loads and first products overlap the previous unit's
+// last products and epilogue.
+// 128-key blocks: TMEM S 0..127, dP 128..255, dS 256..319 (bf16 pairs), dQ
+// 320..511.
 template <int G, bool WIN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap mQr, const __grid_constant__ CUtensorMap mQ,
                   const __grid_constant__ CUtensorMap mDO, const __grid_constant__ CUtensorMap mKr,
                   const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
-                  const BackwardArgs a, int nqt) {
-  constexpr int TQ = 128 / G;  // tokens per 128-row tile
-  constexpr int BN = 128;      // keys per block
+                  const BackwardArgs a, int nqt, int nunits) {
+  constexpr int BN = 128;  // keys per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_base_1k(smem_raw);
   DqBars* bars = reinterpret_cast<DqBars*>(smem + kDqOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int per = a.batch * a.hkv;
-  const int q_ord = blockIdx.x / per, rem = blockIdx.x - q_ord * per;
-  const int qt = WIN ? q_ord : nqt - 1 - q_ord;
-  const int b = rem / a.hkv, g = rem - b * a.hkv;
-  const int tok0 = __ldg(a.cu_seqlens + b);
-  const int L = __ldg(a.cu_seqlens + b + 1) - tok0;
-  const int t0 = qt * TQ;
-  if (t0 >= L) return;  // uniform over the CTA
-  const int kstart = WIN ? max(0, t0 - a.window + 1) : 0;
-  const int kend = min(L, t0 + TQ);
-  const int nblk = (kend - kstart + BN - 1) / BN;
-
   if (threadIdx.x == 0) {
     mbar_init(&bars->fixed_full, 1);
+    mbar_init(&bars->fixed_empty, 1);
     for (int j = 0; j < 2; ++j) {
       mbar_init(&bars->k_full[j], 1);
       mbar_init(&bars->k_empty[j], 1);
@@ -570,6 +584,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->p_full, 4);
     mbar_init(&bars->p_free, 1);
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->acc_free, 4);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -587,38 +602,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- loads
     if (lane == 0) {
+      tma_prefetch_map(&mQr);
       tma_prefetch_map(&mKr);
       tma_prefetch_map(&mK);
       tma_prefetch_map(&mV);
-      mbar_arrive_expect_tx(&bars->fixed_full, kFixedBytes);
-      tma_load_3d(smem, &mQr, &bars->fixed_full, 0, g * G, tok0 + t0);
-      tma_load_3d(smem + kBoxBytes128, &mQ, &bars->fixed_full, 64, g * G, tok0 + t0);
-      tma_load_3d(smem + 2 * kBoxBytes128, &mQ, &bars->fixed_full, 128, g * G, tok0 + t0);
-      tma_load_3d(smem + 3 * kBoxBytes128, &mDO, &bars->fixed_full, 0, g * G, tok0 + t0);
-      tma_load_3d(smem + 4 * kBoxBytes128, &mDO, &bars->fixed_full, 64, g * G, tok0 + t0);
-      int kfilled = 0, vfilled = 0;
-      for (int i = 0; i < nblk; ++i) {
-        const int kr0 = tok0 + kstart + BN * i;
-        const int j = i & 1;
-        if (i >= 2 && !mbar_wait(&bars->k_empty[j], ((i >> 1) - 1) & 1, a.ctl, abort)) break;
-        uint8_t* kb = smem + kDqOffK + j * kDqKBytes;
-        mbar_arrive_expect_tx(&bars->k_full[j], kDqKBytes);
-        tma_load_3d(kb, &mKr, &bars->k_full[j], 0, g, kr0);
-        tma_load_3d(kb + kBoxBytes128, &mK, &bars->k_full[j], 64, g, kr0);
-        tma_load_3d(kb + 2 * kBoxBytes128, &mK, &bars->k_full[j], 128, g, kr0);
-        kfilled = i + 1;
-        if (i >= 1 && !mbar_wait(&bars->v_empty, (i - 1) & 1, a.ctl, abort)) break;
-        uint8_t* vb = smem + kDqOffV;
-        mbar_arrive_expect_tx(&bars->v_full, 2 * kBoxBytes128);
-        tma_load_3d(vb, &mV, &bars->v_full, 0, g, kr0);
-        tma_load_3d(vb + kBoxBytes128, &mV, &bars->v_full, 64, g, kr0);
-        vfilled = i + 1;
+      int it = 0, nu = 0;        // blocks and units whose loads were issued
+      int kfill = 0, vfill = 0;  // K and V copies issued
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        DqUnit du;
+        if (!dq_unit<G, WIN>(u, a, nqt, du)) continue;
+        // Q' and dout of the tile, once the previous tile's products are done with them
+        if (nu > 0 && !mbar_wait(&bars->fixed_empty, (nu - 1) & 1, a.ctl, abort)) break;
+        const int qrow = du.tok0 + du.t0;
+        mbar_arrive_expect_tx(&bars->fixed_full, kFixedBytes);
+        tma_load_3d(smem, &mQr, &bars->fixed_full, 0, du.g * G, qrow);
+        tma_load_3d(smem + kBoxBytes128, &mQ, &bars->fixed_full, 64, du.g * G, qrow);
+        tma_load_3d(smem + 2 * kBoxBytes128, &mQ, &bars->fixed_full, 128, du.g * G, qrow);
+        tma_load_3d(smem + 3 * kBoxBytes128, &mDO, &bars->fixed_full, 0, du.g * G, qrow);
+        tma_load_3d(smem + 4 * kBoxBytes128, &mDO, &bars->fixed_full, 64, du.g * G, qrow);
+        ++nu;
+        for (int i = 0; i < du.nblk; ++i, ++it) {
+          const int kr0 = du.tok0 + du.kstart + BN * i;
+          const int j = it & 1;
+          if (it >= 2 && !mbar_wait(&bars->k_empty[j], ((it >> 1) - 1) & 1, a.ctl, abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* kb = smem + kDqOffK + j * kDqKBytes;
+          mbar_arrive_expect_tx(&bars->k_full[j], kDqKBytes);
+          tma_load_3d(kb, &mKr, &bars->k_full[j], 0, du.g, kr0);
+          tma_load_3d(kb + kBoxBytes128, &mK, &bars->k_full[j], 64, du.g, kr0);
+          tma_load_3d(kb + 2 * kBoxBytes128, &mK, &bars->k_full[j], 128, du.g, kr0);
+          ++kfill;
+          if (it >= 1 && !mbar_wait(&bars->v_empty, (it - 1) & 1, a.ctl, abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* vb = smem + kDqOffV;
+          mbar_arrive_expect_tx(&bars->v_full, 2 * kBoxBytes128);
+          tma_load_3d(vb, &mV, &bars->v_full, 0, du.g, kr0);
+          tma_load_3d(vb + kBoxBytes128, &mV, &bars->v_full, 64, du.g, kr0);
+          ++vfill;
+        }
       }
-      // copies still in flight must land before the CTA may exit
-      mbar_wait_drain(&bars->fixed_full, 0, a.ctl);
-      for (int i = max(0, kfilled - 2); i < kfilled; ++i)
-        mbar_wait_drain(&bars->k_full[i & 1], (i >> 1) & 1, a.ctl);
-      if (vfilled > 0) mbar_wait_drain(&bars->v_full, (vfilled - 1) & 1, a.ctl);
+      // copies still in flight must land before the CTA may exit: the last
+      // fill of each barrier
+      if (nu > 0) mbar_wait_drain(&bars->fixed_full, (nu - 1) & 1, a.ctl);
+      for (int f = max(0, kfill - 2); f < kfill; ++f)
+        mbar_wait_drain(&bars->k_full[f & 1], (f >> 1) & 1, a.ctl);
+      if (vfill > 0) mbar_wait_drain(&bars->v_full, (vfill - 1) & 1, a.ctl);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -628,20 +661,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t qa = make_sdesc_sw128(sb, 16, 1024);                      // Q', K-major
     const uint64_t ga = make_sdesc_sw128(sb + 3 * kBoxBytes128, 16, 1024);   // dout, K-major
     const uint64_t vd = make_sdesc_sw128(sb + kDqOffV, 16, 1024);            // V, K-major
-    bool ok = warp_wait(&bars->fixed_full, 0, a.ctl, abort);
-    // S(i) = Q' K_i^T once K_i has landed, then dP(i) = dout V_i^T once V_i has
-    auto issue_s = [&](int i) -> bool {
-      if (!warp_wait(&bars->k_full[i & 1], (i >> 1) & 1, a.ctl, abort)) return false;
+    // S(it) = Q' K^T once K has landed, then dP(it) = dout V^T once V has;
+    // first: the unit's Q' / dout must have landed; last: they may be refilled
+    // once these products complete
+    auto issue_s = [&](int it, bool first, int nu, bool last) -> bool {
+      if (first && !warp_wait(&bars->fixed_full, nu & 1, a.ctl, abort)) return false;
+      if (!warp_wait(&bars->k_full[it & 1], (it >> 1) & 1, a.ctl, abort)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t kd = make_sdesc_sw128(sb + kDqOffK + (i & 1) * kDqKBytes, 16, 1024);
+        const uint64_t kd = make_sdesc_sw128(sb + kDqOffK + (it & 1) * kDqKBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk)
           umma_ss(tmem, qa + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4),
                   kd + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4), id_s, kk > 0);
       }
       __syncwarp();
-      if (!warp_wait(&bars->v_full, i & 1, a.ctl, abort)) return false;
+      if (!warp_wait(&bars->v_full, it & 1, a.ctl, abort)) return false;
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
@@ -650,34 +685,79 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   vd + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4), id_s, kk > 0);
         umma_commit(&bars->v_empty);
         umma_commit(&bars->s_full);
+        if (last) umma_commit(&bars->fixed_empty);
       }
       __syncwarp();
       return true;
     };
-    bool issued = false;
-    for (int i = 0; ok && i < nblk; ++i) {
-      if (i == 0) {
-        issued = true;
-        if (!issue_s(0)) break;
-      }
-      if (i + 1 < nblk) {
-        if (!warp_wait(&bars->s_free, i & 1, a.ctl, abort)) break;
-        if (!issue_s(i + 1)) break;
-      }
-      if (!warp_wait(&bars->p_full, i & 1, a.ctl, abort)) break;
+    // dQ += dS K(it); the unit's first block overwrites dQ, so it waits for the
+    // previous unit's epilogue to have read it
+    auto issue_dq = [&](int it, bool first, int nu, bool last) -> bool {
+      if (first && nu > 0 && !warp_wait(&bars->acc_free, (nu - 1) & 1, a.ctl, abort))
+        return false;
+      if (!warp_wait(&bars->p_full, it & 1, a.ctl, abort)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t kb = make_sdesc_sw128(sb + kDqOffK + (i & 1) * kDqKBytes, kBoxBytes128,
+        const uint64_t kb = make_sdesc_sw128(sb + kDqOffK + (it & 1) * kDqKBytes, kBoxBytes128,
                                              1024);  // K', MN-major
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           umma_ts(tmem + 320, tmem + 2 * BN + kk * 8, kb + uint64_t((kk * 2048) >> 4), id_dq,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+                  (!first || kk > 0) ? 1u : 0u);
         umma_commit(&bars->p_free);
-        umma_commit(&bars->k_empty[i & 1]);
-        if (i + 1 == nblk) umma_commit(&bars->acc_done);
+        umma_commit(&bars->k_empty[it & 1]);
+        if (last) umma_commit(&bars->acc_done);
       }
       __syncwarp();
+      return true;
+    };
+    // the CTA's blocks in order: block counter, first / last of its unit, unit counter
+    int u = int(blockIdx.x) - int(gridDim.x), i = 0, it = 0, nu = -1;
+    DqUnit du;
+    du.nblk = 0;
+    auto advance = [&](int& bit, bool& bfirst, bool& blast, int& bnu) -> bool {
+      while (i >= du.nblk) {
+        u += gridDim.x;
+        i = 0;
+        du.nblk = 0;
+        if (u >= nunits) return false;
+        if (dq_unit<G, WIN>(u, a, nqt, du)) ++nu;
+      }
+      bit = it++;
+      bfirst = i == 0;
+      blast = i + 1 == du.nblk;
+      bnu = nu;
+      ++i;
+      return true;
+    };
+    bool issued = false, ok = true;
+    int c_it = 0, c_nu = 0, n_it = 0, n_nu = 0;  // current block and the next one
+    bool c_first = false, c_last = false, n_first = false, n_last = false;
+    bool have_c = advance(c_it, c_first, c_last, c_nu);
+    if (have_c) {
+      issued = true;
+      ok = issue_s(c_it, c_first, c_nu, c_last);
+    }
+    while (ok && have_c) {
+      const bool have_n = advance(n_it, n_first, n_last, n_nu);
+      if (have_n && !n_first) {
+        // same unit: the next block's S / dP first (they overlap this block's row work)
+        if (!warp_wait(&bars->s_free, c_it & 1, a.ctl, abort)) break;
+        if (!issue_s(n_it, n_first, n_nu, n_last)) break;
+        if (!issue_dq(c_it, c_first, c_nu, c_last)) break;
+      } else {
+        // unit boundary: finish this unit's dQ first
+        if (!issue_dq(c_it, c_first, c_nu, c_last)) break;
+        if (have_n) {
+          if (!warp_wait(&bars->s_free, c_it & 1, a.ctl, abort)) break;
+          if (!issue_s(n_it, n_first, n_nu, n_last)) break;
+        }
+      }
+      have_c = have_n;
+      c_it = n_it;
+      c_first = n_first;
+      c_last = n_last;
+      c_nu = n_nu;
     }
     if (issued && lane == 0) {
       umma_commit(&bars->drain);
@@ -686,61 +766,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp >= 4) {
     // ---------------------------------------------------- one thread per row
     const int r = (warp & 3) * 32 + lane;
-    const int p = t0 + r / G;  // query position
-    const int h = g * G + r % G;
-    const bool valid = p < L;
-    const long orow = long(tok0 + p) * a.hq + h;
-    const float l2 = valid ? __ldg(a.lse + orow) * kLog2e : 0.f;
-    const float de = valid ? __ldg(a.delta + orow) : 0.f;
     const uint32_t t_row = tmem + (uint32_t((warp & 3) * 32) << 16);
+    int it = 0, nu = 0;
     bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
-      if (!warp_wait(&bars->s_full, i & 1, a.ctl, abort)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t dw[64];
+    for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+      DqUnit du;
+      if (!dq_unit<G, WIN>(u, a, nqt, du)) continue;
+      const int p = du.t0 + r / G;  // query position
+      const int h = du.g * G + r % G;
+      const bool valid = p < du.L;
+      const long orow = long(du.tok0 + p) * a.hq + h;
+      const float l2 = valid ? __ldg(a.lse + orow) * kLog2e : 0.f;
+      const float de = valid ? __ldg(a.delta + orow) : 0.f;
+      for (int i = 0; i < du.nblk; ++i, ++it) {
+        if (!warp_wait(&bars->s_full, it & 1, a.ctl, abort)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dw[64];
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        uint32_t sv[64], dp[64];
-        tmem_ld32_nowait(t_row + 64 * hb, sv);
-        tmem_ld32_nowait(t_row + 64 * hb + 32, sv + 32);
-        tmem_ld32_nowait(t_row + BN + 64 * hb, dp);
-        tmem_ld32_nowait(t_row + BN + 64 * hb + 32, dp + 32);
-        tmem_ld_wait();
-        if (hb == 1) {
-          // S and dP are in registers: the next block's products may overwrite them
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->s_free);
-        }
-        const int d0 = p - (kstart + BN * i + 64 * hb);  // query minus key position, column 0
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float dc[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int d = d0 - (c + e);
-            const bool vis = valid && d >= 0 && (!WIN || d < a.window);
-            const float x = __uint_as_float(sv[c + e]) * a.scale_log2 - l2;
-            dc[e] = vis ? fast_exp2(x) * (__uint_as_float(dp[c + e]) - de) : 0.f;
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t sv[64], dp[64];
+          tmem_ld32_nowait(t_row + 64 * hb, sv);
+          tmem_ld32_nowait(t_row + 64 * hb + 32, sv + 32);
+          tmem_ld32_nowait(t_row + BN + 64 * hb, dp);
+          tmem_ld32_nowait(t_row + BN + 64 * hb + 32, dp + 32);
+          tmem_ld_wait();
+          if (hb == 1) {
+            // S and dP are in registers: the next block's products may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_free);
           }
-          dw[32 * hb + (c >> 1)] = pack_bf16x2(dc[0], dc[1]);
+          const int d0 = p - (du.kstart + BN * i + 64 * hb);  // query minus key position, col 0
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float dc[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int d = d0 - (c + e);
+              const bool vis = valid && d >= 0 && (!WIN || d < a.window);
+              const float x = __uint_as_float(sv[c + e]) * a.scale_log2 - l2;
+              dc[e] = vis ? fast_exp2(x) * (__uint_as_float(dp[c + e]) - de) : 0.f;
+            }
+            dw[32 * hb + (c >> 1)] = pack_bf16x2(dc[0], dc[1]);
+          }
         }
+        if (it > 0 && !warp_wait(&bars->p_free, (it - 1) & 1, a.ctl, abort)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st32(t_row + 2 * BN, dw);
+        tmem_st32(t_row + 2 * BN + 32, dw + 32);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
       }
-      if (i > 0 && !warp_wait(&bars->p_free, (i - 1) & 1, a.ctl, abort)) { ok = false; break; }
-      tc_fence_after();
-      tmem_st32(t_row + 2 * BN, dw);
-      tmem_st32(t_row + 2 * BN + 32, dw + 32);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);
-    }
-    if (ok && warp_wait(&bars->acc_done, 0, a.ctl, abort)) {
+      if (!ok || !warp_wait(&bars->acc_done, nu & 1, a.ctl, abort)) { ok = false; break; }
       tc_fence_after();
       __nv_bfloat16* dqr = static_cast<__nv_bfloat16*>(a.dq) + orow * kDqk;
       finish_rot64(t_row + 320, a.scale, p, a.freqs, valid, dqr);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) finish_chunk32(t_row + 320, a.scale, valid, dqr, 64 + 32 * ch);
+      // dQ has been read: the next unit's first product may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_free);
+      ++nu;
     }
   }
   tc_fence_before();
@@ -782,8 +871,13 @@ cudaError_t launch_g(const BackwardArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const int nqt = (a.max_seqlen + 128 / G - 1) / (128 / G);
   if (long(nqt) * per > 0x7fffffffL) return cudaErrorInvalidValue;
-  qk<<<unsigned(nqt * per), kBwdThreads, kDqSmem, s>>>(mQr128, mQ128, mDO128, mKr128, mK128,
-                                                        mV128, a, nqt);
+  const int nunits = int(nqt * per);
+  // window layers: short, equal units, a persistent CTA per SM; global layers:
+  // one CTA per unit (their lengths differ, and the hardware's dispatch of the
+  // next CTA to the SM that frees first balances them better than a fixed split)
+  const int grid = win ? (nunits < num_sms() ? nunits : num_sms()) : nunits;
+  qk<<<unsigned(grid), kBwdThreads, kDqSmem, s>>>(mQr128, mQ128, mDO128, mKr128, mK128, mV128, a,
+                                                   nqt, nunits);
   return cudaGetLastError();
 }
 
