@@ -742,6 +742,7 @@ def run_backward(args):
                       "ga_backward": {"ms": round(t_ga * 1e3, 4), "TFLOP/s": round(ga_tf, 2),
                                       "frac_tensor_sustained": round(ga_tf / tf_sust, 4),
                                       "flops": ga["flops"]}},
+            "gpu_launches": 8 * args.steps,  # prep, sink sum, dK/dV, dQ per layer
             "clocks": clk.summary()}
 
 

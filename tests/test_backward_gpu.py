@@ -34,9 +34,10 @@ def _rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def _run(seqlens, hq, hkv, window, base, seed, dout_seed=None):
+def _run(seqlens, hq, hkv, window, base, seed, dout_seed=None, sink_mean=0.0, sink_std=1.0):
     dev = torch.device("cuda")
-    c = synth.prefill_case(seqlens, hq, hkv, window=window, rope_base=base, seed=seed)
+    c = synth.prefill_case(seqlens, hq, hkv, window=window, rope_base=base, seed=seed,
+                           sink_mean=sink_mean, sink_std=sink_std)
     total = c.total
     g = synth.randn_bf16((total, hq, 128), synth._gen(seed + 1000 if dout_seed is None
                                                       else dout_seed, "cpu"), "cpu")
@@ -86,6 +87,19 @@ def test_backward_matches_oracle(seqlens, hq, hkv, window, base, seed):
     got, ref, extra = _run(seqlens, hq, hkv, window, base, seed)
     errs = _check(got, ref, (seqlens, hq, hkv, window), extra)
     print(seqlens, hq, hkv, window, {k: (f"{r:.2e}", f"{m:.2e}") for k, (r, m) in errs.items()})
+
+
+@pytest.mark.parametrize("seqlens,hq,hkv,window,sink_mean,sink_std,seed", [
+    ([140, 9], 16, 2, 1, 0.0, 1.0, 11),      # W = 1: each query sees only itself
+    ([300], 16, 2, 128, 8.0, 2.0, 12),       # heavy sinks: the sink takes most of the weight
+    ([260], 32, 2, 0, 6.0, 2.0, 13),
+])
+def test_backward_degenerate_and_heavy_sinks(seqlens, hq, hkv, window, sink_mean, sink_std,
+                                             seed):
+    base = 1e4 if window else 5e6
+    got, ref, extra = _run(seqlens, hq, hkv, window, base, seed, sink_mean=sink_mean,
+                           sink_std=sink_std)
+    _check(got, ref, (seqlens, hq, hkv, window, sink_mean), extra)
 
 
 def test_backward_is_deterministic():
