@@ -517,7 +517,7 @@ def whole_job_tflops(flops_per_rank_step, world, ms_per_step):
 
 
 def run_hybrid_block(args):
-    """Config 5: one hybrid block at seq 262144 -- 5 sliding-window layers (64q/8kv,
+    """One hybrid block at seq 262144 -- 5 sliding-window layers (64q/8kv,
     W=128, base 1e4) then 1 global layer (64q/4kv, base 5e6), fresh N(0,1) inputs
     per layer, all resident in HBM; one step = the 6 layer calls."""
     import global_attention_sinks_gqa_b300 as ha
