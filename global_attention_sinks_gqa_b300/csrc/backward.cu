@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256) bwd_dsink_kernel(const BackwardArgs a) {
 struct BwdBars {
   uint64_t fixed_full;            // the operand loaded once per CTA
   uint64_t st_full[kNst], st_empty[kNst];
-  uint64_t s_full, s_free, p_full, p_free, acc_done, drain;
+  uint64_t s_full, s_free, p_full, acc_done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -270,7 +270,6 @@ __device__ __forceinline__ void bwd_init(BwdBars* bars, uint32_t st_full_count) 
   mbar_init(&bars->s_full, 1);
   mbar_init(&bars->s_free, 4);
   mbar_init(&bars->p_full, 4);
-  mbar_init(&bars->p_free, 1);
   mbar_init(&bars->acc_done, 1);
   mbar_init(&bars->drain, 1);
   bars->abort = 0;
@@ -420,7 +419,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ts(tmem + 192, tmem + 128 + kk * 8, gb + uint64_t((kk * 2048) >> 4), id_dv, acc);
           umma_ts(tmem + 320, tmem + 160 + kk * 8, qb + uint64_t((kk * 2048) >> 4), id_dk, acc);
         }
-        umma_commit(&bars->p_free);
+        // completes with dV / dK of this tile: its stage may be refilled and its
+        // P^T / dS^T columns rewritten
         umma_commit(&bars->st_empty[s]);
         if (i + 1 == ntile) umma_commit(&bars->acc_done);
       }
@@ -470,7 +470,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pw[c >> 1] = pack_bf16x2(pc[0], pc[1]);
         dw[c >> 1] = pack_bf16x2(dc[0], dc[1]);
       }
-      if (i > 0 && !warp_wait(&bars->p_free, (i - 1) & 1, a.ctl, abort)) { ok = false; break; }
+      // the previous tile's dV / dK products have read its P^T / dS^T (its
+      // stage's empty barrier cannot move on before this tile is handed over)
+      if (i > 0 && !warp_wait(&bars->st_empty[(i - 1) % kNst], ((i - 1) / kNst) & 1, a.ctl, abort)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       tmem_st32(t_row + 128, pw);
       tmem_st32(t_row + 160, dw);
@@ -522,7 +527,7 @@ static_assert(kDqSmem <= 232448, "shared memory");
 
 struct DqBars {
   uint64_t fixed_full, fixed_empty, k_full[2], k_empty[2], v_full, v_empty;
-  uint64_t s_full, s_free, p_full, p_free, acc_done, acc_free, drain;
+  uint64_t s_full, s_free, p_full, acc_done, acc_free, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -582,7 +587,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 4);
     mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->p_free, 1);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->acc_free, 4);
     mbar_init(&bars->drain, 1);
@@ -704,7 +708,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < BN / 16; ++kk)
           umma_ts(tmem + 320, tmem + 2 * BN + kk * 8, kb + uint64_t((kk * 2048) >> 4), id_dq,
                   (!first || kk > 0) ? 1u : 0u);
-        umma_commit(&bars->p_free);
+        // completes with this block's dQ product: its K buffer may be refilled
+        // and its dS columns rewritten
         umma_commit(&bars->k_empty[it & 1]);
         if (last) umma_commit(&bars->acc_done);
       }
@@ -810,7 +815,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dw[32 * hb + (c >> 1)] = pack_bf16x2(dc[0], dc[1]);
           }
         }
-        if (it > 0 && !warp_wait(&bars->p_free, (it - 1) & 1, a.ctl, abort)) { ok = false; break; }
+        // the previous block's dQ product has read its dS (that K buffer's empty
+        // barrier cannot move on before this block is handed over)
+        if (it > 0 &&
+            !warp_wait(&bars->k_empty[(it - 1) & 1], ((it - 1) >> 1) & 1, a.ctl, abort)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         tmem_st32(t_row + 2 * BN, dw);
         tmem_st32(t_row + 2 * BN + 32, dw + 32);
