@@ -60,6 +60,7 @@ SIGNATURES = {
     "hattn_check_device_status": (_I, [_P]),
     "hattn_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
     "hattn_selftest_lost_arrival": (_I, [_P]),
+    "hattn_test_fail_next_launches": (_I, [_I]),
 }
 
 _lib = None
@@ -226,6 +227,10 @@ def hattn_set_wait_limit_ns(limit_ns: int) -> int:
 
 def hattn_selftest_lost_arrival(stream=None) -> int:
     return load_library().hattn_selftest_lost_arrival(_stream(stream))
+
+
+def hattn_test_fail_next_launches(n: int) -> int:
+    return load_library().hattn_test_fail_next_launches(int(n))
 
 
 # ---------------------------------------------------------------- conveniences

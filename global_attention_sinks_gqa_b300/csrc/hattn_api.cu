@@ -7,6 +7,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -44,6 +45,21 @@ bool device_ctl(DeviceCtl* ctl) {
   ctl->wait_limit_ns = g_wait_limit_ns[dev] ? g_wait_limit_ns[dev] : kDefaultWaitLimitNs;
   return true;
 }
+
+// Host-side fault injection (hattn_test_fail_next_launches): calls that would
+// launch kernels consume one pending failure each and report HATTN_ERR_CUDA
+// before touching the device, as a failed launch would.
+std::atomic<int> g_fail_launches{0};
+
+bool take_injected_failure() {
+  int n = g_fail_launches.load();
+  while (n > 0)
+    if (g_fail_launches.compare_exchange_weak(n, n - 1)) return true;
+  return false;
+}
+
+// device_ctl for the entry points that launch kernels.
+bool launch_ctl(DeviceCtl* ctl) { return !take_injected_failure() && device_ctl(ctl); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -142,7 +158,7 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
   if (!workspace || workspace_bytes < hattn_prefill_workspace_size(total_tokens, hkv, dqk))
     return HATTN_ERR_WORKSPACE;
   DeviceCtl ctl;
-  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  if (!launch_ctl(&ctl)) return HATTN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrefillArgs a;
   a.q = q;
@@ -217,7 +233,7 @@ hattn_status_t hattn_prefill_backward(const void* q, const void* k, const void* 
       workspace_bytes < hattn_prefill_backward_workspace_size(total_tokens, hq, hkv))
     return HATTN_ERR_WORKSPACE;
   DeviceCtl ctl;
-  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  if (!launch_ctl(&ctl)) return HATTN_ERR_CUDA;
   auto r256 = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t t = size_t(total_tokens);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -283,7 +299,7 @@ hattn_status_t hattn_prefill_cached(const void* q, const void* k_new, const void
     return HATTN_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < 256) return HATTN_ERR_WORKSPACE;
   DeviceCtl ctl;
-  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  if (!launch_ctl(&ctl)) return HATTN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrefillArgs a;
   a.q = q;
@@ -329,7 +345,7 @@ hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const 
       (reinterpret_cast<uintptr_t>(start_pos) & 3u))
     return HATTN_ERR_INVALID_ARG;
   DeviceCtl ctl;
-  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  if (!launch_ctl(&ctl)) return HATTN_ERR_CUDA;
   RopeFreqs f;
   make_rope_freqs(rope_base, &f);
   if (launch_kv_append(k_new, v_new, start_pos, k_cache, v_cache, B, T, hkv, cap, is_ring, f,
@@ -411,7 +427,7 @@ hattn_status_t decode_step(const void* q, const void* k_new, const void* v_new, 
     a.item_ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + o_bytes +
                                                  l_bytes);
   }
-  if (!device_ctl(&a.ctl)) return HATTN_ERR_CUDA;
+  if (!launch_ctl(&a.ctl)) return HATTN_ERR_CUDA;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return HATTN_ERR_CUDA;
   return HATTN_OK;
 }
@@ -491,10 +507,12 @@ hattn_status_t hattn_set_wait_limit_ns(unsigned long long limit_ns) {
 
 hattn_status_t hattn_selftest_lost_arrival(void* stream) {
   DeviceCtl ctl;
-  if (!device_ctl(&ctl)) return HATTN_ERR_CUDA;
+  if (!launch_ctl(&ctl)) return HATTN_ERR_CUDA;
   if (launch_lost_arrival_selftest(ctl, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return HATTN_ERR_CUDA;
   return HATTN_OK;
 }
+
+int hattn_test_fail_next_launches(int n) { return g_fail_launches.exchange(n > 0 ? n : 0); }
 
 }  // extern "C"

@@ -376,6 +376,16 @@ hattn_status_t hattn_set_wait_limit_ns(unsigned long long limit_ns);
  */
 hattn_status_t hattn_selftest_lost_arrival(void* stream);
 
+/*
+ * Test hook, host-side fault injection: the next n calls that would launch
+ * kernels (after their argument checks pass) return HATTN_ERR_CUDA without
+ * touching the device, as a failed launch would, so a caller's error handling
+ * can be exercised without faulting a GPU.  n <= 0 clears it.  Returns the
+ * number of injected failures that were still pending.  Process-wide,
+ * thread-safe; calls rejected by their argument checks do not consume one.
+ */
+int hattn_test_fail_next_launches(int n);
+
 #ifdef __cplusplus
 }
 #endif

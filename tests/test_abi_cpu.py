@@ -229,3 +229,20 @@ def _backward(**kw):
 ])
 def test_backward_rejects_bad_arguments(lib, kw, code):
     assert _backward(**kw) == code
+
+
+def test_injected_launch_failures_are_consumed_by_launching_calls(lib):
+    """Host-side fault injection: pending failures are consumed only by calls
+    that passed their argument checks, each returning HATTN_ERR_CUDA."""
+    assert ha.hattn_test_fail_next_launches(2) == 0
+    try:
+        assert _prefill(hkv=3) == ha.HATTN_ERR_INVALID_ARG       # rejected first: not consumed
+        assert _decode(cap=130) == ha.HATTN_ERR_RING_TOO_SMALL
+        assert ha.hattn_test_fail_next_launches(2) == 2
+        assert _prefill(workspace_bytes=1 << 20) == ha.HATTN_ERR_CUDA
+        assert ha.hattn_test_fail_next_launches(2) == 1
+        assert _decode() == ha.HATTN_ERR_CUDA
+        assert _backward() == ha.HATTN_ERR_CUDA
+        assert ha.hattn_test_fail_next_launches(0) == 0
+    finally:
+        ha.hattn_test_fail_next_launches(0)

@@ -54,3 +54,25 @@ def test_append_position_beyond_linear_cache_is_reported():
     ha.rope_kv_append(k, v, pos, kc, vc, is_ring=False, rope_base=1e4)
     assert ha.hattn_check_device_status() == ha.HATTN_ERR_INVALID_ARG
     assert torch.equal(vc[0, 0, 7].cpu(), v[0, 0, 0].cpu())  # position 7 was written
+
+
+def test_injected_launch_failure_leaves_outputs_untouched():
+    """A launch failure injected on the host surfaces as HATTN_ERR_CUDA through
+    the Python binding, writes nothing, and the next call runs normally."""
+    dev = torch.device("cuda")
+    c = synth.prefill_case([300], 16, 2, window=128, rope_base=1e4, seed=61, device=dev)
+    kw = dict(max_seqlen=300, window=128, rope_base=1e4)
+    ref, ref_lse = ha.prefill(c.q, c.k, c.v, c.sink, c.cu_seqlens, **kw)
+    out = torch.full_like(ref, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    assert ha.hattn_test_fail_next_launches(1) == 0
+    with pytest.raises(ha.HattnError) as e:
+        ha.prefill(c.q, c.k, c.v, c.sink, c.cu_seqlens, out=out, lse=lse, **kw)
+    assert e.value.status == ha.HATTN_ERR_CUDA
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all() and torch.isnan(lse).all()
+    assert ha.hattn_test_fail_next_launches(0) == 0
+    ha.prefill(c.q, c.k, c.v, c.sink, c.cu_seqlens, out=out, lse=lse, **kw)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
