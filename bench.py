@@ -449,6 +449,7 @@ def cpu_baseline(budget_s: float = 20.0):
     # GA prefill rows (32K, 64/4): rows spread over the sequence until the budget is spent
     c = cf["ga_prefill_32k"]
     pc = _cpu_case("ga_prefill_32k")
+    S = pc.total
     order = rs.permutation(S)
     n_ok, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s - secs and n_ok < S:
