@@ -42,3 +42,28 @@ def test_reference_line_has_the_contract_keys(small_workloads):
 def test_whole_job_value_is_weak_scaling():
     assert bench.whole_job_tflops(1e12, 1, 1000.0) == pytest.approx(1.0)
     assert bench.whole_job_tflops(1e12, 4, 1000.0) == pytest.approx(4.0)
+
+
+def _pairs_brute(S, W):
+    return sum(min(p + 1, W) if W else p + 1 for p in range(S))
+
+
+def test_accounting_matches_brute_force_and_the_stated_workload_figures():
+    # visible pairs against a per-row count
+    for S, W in ((1, 0), (7, 3), (129, 128), (128, 128), (300, 1), (50, 0)):
+        assert bench.prefill_pairs(S, W) == _pairs_brute(S, W), (S, W)
+    # the workload figures the measurements are quoted on
+    assert bench.prefill_pairs(32768, 128) == 4_186_176
+    assert bench.prefill_pairs(32768, 0) == 536_887_296
+    assert bench.prefill_flops(32768, 64, 128) == pytest.approx(1.7147e11, rel=1e-4)
+    assert bench.prefill_flops(32768, 64, 0) == pytest.approx(2.1991e13, rel=1e-4)
+    assert bench.prefill_bytes(32768, 64, 8) == pytest.approx(1.5183e9, rel=1e-4)
+    assert bench.prefill_bytes(32768, 64, 4) == pytest.approx(1.4345e9, rel=1e-4)
+    # decode: the window ring's 131 keys per sequence at T = 4, W = 128
+    lens = [9000, 131, 70000]
+    assert bench.decode_pairs(lens, 4, 128) == sum(
+        min(L - 4 + t + 1, 128) for L in lens for t in range(4))
+    kv = sum(min(L, 131) for L in lens) * 8 * (192 + 128) * 2
+    assert bench.decode_bytes(lens, 4, 64, 8, 128) == kv + 3 * 4 * 64 * (384 + 256 + 4) + 64 * 4
+    # the backward's minimal products: S, dP, dV, dQ, dK
+    assert bench.BWD_PAIR_FLOPS == 2 * (192 + 128 + 128 + 192 + 192)
