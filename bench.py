@@ -854,6 +854,22 @@ def run_profile_case(args):
                              window=p["window"], is_ring=kind == "swa",
                              rope_base=p["rope_base"])
         work = f"{name} batch {B} x {T}"
+    elif name in ("swa_backward", "ga_backward"):
+        c = synth.CONFIGS[name.split("_")[0] + "_prefill_32k"]
+        S = args.seq or c["seqlens"][0]
+        pc = synth.prefill_case([S], c["hq"], c["hkv"], window=c["window"],
+                                rope_base=c["rope_base"], seed=c["seed"], device=dev)
+        g = synth.randn_bf16((S, pc.hq, D_V), synth._gen(c["seed"] + 100, dev), dev)
+        out, lse = ha.prefill(pc.q, pc.k, pc.v, pc.sink, pc.cu_seqlens, max_seqlen=S,
+                              window=pc.window, rope_base=pc.rope_base, softmax_scale=pc.scale)
+        ws = torch.empty(ha.hattn_prefill_backward_workspace_size(S, pc.hq, pc.hkv),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            return ha.prefill_backward(pc.q, pc.k, pc.v, pc.sink, out, lse, g, pc.cu_seqlens,
+                                       max_seqlen=S, window=pc.window, rope_base=pc.rope_base,
+                                       softmax_scale=pc.scale, workspace=ws)
+        work = f"{name} seq {S}"
     else:
         raise SystemExit(f"unknown profile case {name}")
     call()
@@ -875,7 +891,8 @@ def main():
     ap.add_argument("--cpu-baseline", type=int, default=1)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--profile-case", default=None,
-                    help="swa_prefill | ga_prefill | decode_swa | decode_ga: one call, for ncu")
+                    help="swa_prefill | ga_prefill | decode_swa | decode_ga | swa_backward | "
+                         "ga_backward: one call, for ncu")
     ap.add_argument("--seq", type=int, default=0, help="prefill length for --profile-case")
     ap.add_argument("--batch", type=int, default=0, help="decode batch for --profile-case")
     ap.add_argument("--workload", default="step",
