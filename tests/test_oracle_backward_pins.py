@@ -7,7 +7,9 @@ Nothing here compares the oracle with itself: the whole-matrix numpy backward
 is pinned by central finite differences of the whole-matrix forward; the C
 backward is checked against that, against torch autograd through its library
 attention in the no-sink / no-RoPE special case, against finite differences of
-the C forward in the sink, and against a closed form for the column sums of dv.
+the C forward in the sink, and against a closed form for the column sums of dv;
+plus identities any correct backward keeps (a window covering the sequence is
+global, packing restarts positions, a dominating sink zeroes every gradient).
 """
 import math
 
@@ -177,3 +179,44 @@ def test_planted_backward_mistakes_are_caught():
                                                                100.0, 4), pos, 100.0, 4), (1, 0, 2))
     assert np.max(np.abs(twice - ref_dk)) > 1e-3
     assert np.max(np.abs(dk - ref_dk)) < 1e-7
+
+
+def test_backward_window_covering_the_sequence_equals_global():
+    c = synth.prefill_case([45], 8, 2, window=45, rope_base=1e4, seed=71)
+    g = synth.randn_bf16((45, 8, 128), synth._gen(72, "cpu"), "cpu")
+    a = oracle.prefill_backward(c.q, c.k, c.v, c.sink, g, [0, 45], window=45, rope_base=1e4,
+                                scale=c.scale)
+    b = oracle.prefill_backward(c.q, c.k, c.v, c.sink, g, [0, 45], window=0, rope_base=1e4,
+                                scale=c.scale)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_backward_packing_restarts_positions():
+    """A packed batch equals its sequences run one by one (positions restart at
+    0 in each); the sink gradient is their sum."""
+    lens = [17, 30]
+    c = synth.prefill_case(lens, 8, 4, window=9, rope_base=1e4, seed=73)
+    g = synth.randn_bf16((47, 8, 128), synth._gen(74, "cpu"), "cpu")
+    kw = dict(window=9, rope_base=1e4, scale=c.scale)
+    packed = oracle.prefill_backward(c.q, c.k, c.v, c.sink, g, [0, 17, 47], **kw)
+    parts = [oracle.prefill_backward(c.q[a:e], c.k[a:e], c.v[a:e], c.sink, g[a:e], [0, e - a],
+                                     **kw) for a, e in ((0, 17), (17, 47))]
+    for i in range(3):
+        ref = np.concatenate([p[i] for p in parts], 0)
+        assert np.max(np.abs(packed[i] - ref)) < 1e-12
+    assert np.max(np.abs(packed[3] - (parts[0][3] + parts[1][3]))) < 1e-12
+
+
+def test_backward_vanishes_as_the_sink_dominates():
+    """With a sink logit far above every key's, the keys' weights and the output
+    go to 0, and with them every gradient (the sink's: -p_sink (dout . out))."""
+    c = synth.prefill_case([25], 4, 2, window=0, rope_base=1e4, seed=75)
+    g = synth.randn_bf16((25, 4, 128), synth._gen(76, "cpu"), "cpu")
+    for s in (40.0, 80.0):
+        sink = torch.full((4,), s)
+        dq, dk, dv, ds = oracle.prefill_backward(c.q, c.k, c.v, sink, g, [0, 25], window=0,
+                                                 rope_base=1e4, scale=c.scale)
+        bound = 1e3 * math.exp(-(s - 10.0))
+        for x in (dq, dk, dv, ds):
+            assert np.max(np.abs(x)) < bound, (s, np.max(np.abs(x)))
