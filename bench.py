@@ -152,6 +152,54 @@ def measured_peaks():
         return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+# Which bf16 peak a kernel's FLOP rate is divided by.  The burst figure (a
+# cuBLAS GEMM timed alone, SM clock near its 2032 MHz maximum) fits a kernel
+# that runs for milliseconds inside a step whose own clock record stays near
+# the maximum; the sustained figure (the same GEMM back to back for seconds,
+# SM clock pulled down by the power cap) fits a kernel that itself runs for
+# seconds.  The line records which one each fraction used.
+SUSTAINED_AFTER_S = 1.0
+
+
+def tensor_peak(kernel_s, tf_burst, tf_sust):
+    if kernel_s >= SUSTAINED_AFTER_S:
+        return tf_sust, "bf16_tflops_sustained"
+    return tf_burst, "bf16_tflops"
+
+
+# DRAM traffic per launch of a kernel, as counted by one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), with a digest of the sources
+# the kernel was built from: once the sources change, the count no longer
+# describes the kernel and the line reports null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "prefill": ["prefill_tc.cu", "rope_append.cu", "common.cuh", "hattn_internal.h"],
+    "decode": ["decode.cu", "rope_append.cu", "common.cuh", "hattn_internal.h"],
+    "backward": ["backward.cu", "common.cuh", "hattn_internal.h"],
+}
+
+
+def sources_digest(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "global_attention_sinks_gqa_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key):
+    """(bytes per launch, source note) of a recorded capture, or (None, why)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[key]
+    except (OSError, KeyError, ValueError):
+        return None, "no capture recorded"
+    if rec.get("sources") != sources_digest(rec["kind"]):
+        return None, "kernel changed since the capture"
+    return rec["dram_bytes"], rec["profile"]
+
+
 def step_config(world: int = 1):
     return {"workload": "swa_prefill_32k + ga_prefill_32k + decode_b64_t4 (swa ring 131 "
                         "+ ga 8K-64K)",
@@ -319,24 +367,29 @@ def run_cuda(args, rank, world):
     e2e = run_e2e(wl, args, stream, sptr)
 
     hbm, tf_burst, tf_sust, src = measured_peaks()
+    clocks = clk.summary()
     parts = {}
     for i, lay in enumerate(wl.layers):
         t = part_ms[f"p{i}"] / 1e3
-        bound_f = lay["flops"] / (tf_sust * 1e12)
+        tf, tf_name = tensor_peak(t, tf_burst, tf_sust)
+        bound_f = lay["flops"] / (tf * 1e12)
         bound_b = lay["bytes"] / (hbm * 1e9)
         parts[lay["name"]] = dict(ms=part_ms[f"p{i}"], tflops=lay["flops"] / t / 1e12,
                                   gbs=lay["bytes"] / t / 1e9,
                                   roofline_frac=max(bound_f, bound_b) / t,
-                                  bound="tensor" if bound_f > bound_b else "hbm")
+                                  bound="tensor" if bound_f > bound_b else "hbm",
+                                  peak="hbm_gbs" if bound_b > bound_f else tf_name)
     for i, dd in enumerate(wl.dec):
         t = part_ms[f"d{i}"] / 1e3
         byts = dd["bytes"] + dd["abytes"]
         parts[f"decode_{dd['kind']}_b64_t4"] = dict(
             ms=part_ms[f"d{i}"], tflops=dd["flops"] / t / 1e12, gbs=byts / t / 1e9,
-            roofline_frac=max(byts / (hbm * 1e9), dd["flops"] / (tf_sust * 1e12)) / t,
-            bound="hbm", verify_tokens_per_s=wl.B * wl.T / t)
+            roofline_frac=byts / (hbm * 1e9) / t, bound="hbm", peak="hbm_gbs",
+            verify_tokens_per_s=wl.B * wl.T / t)
     ga = wl.layers[1]
     ga_s = part_ms["p1"] / 1e3
+    ga_tf, ga_tf_name = tensor_peak(ga_s, tf_burst, tf_sust)
+    ga_traffic, ga_traffic_src = recorded_traffic("prefill_ga_32k")
     flops = wl.flops()
     value = whole_job_tflops(flops, world, ms)
     out = {
@@ -346,19 +399,37 @@ def run_cuda(args, rank, world):
         "data": "synthetic (seeded N(0,1) bf16 q/k/v, N(0,1) fp32 sinks)",
         "config": step_config(world),
         "parts": parts,
-        "roofline": {"bound": "tensor", "kernel": "prefill GA (hattn_prefill window=0)",
+        "roofline": {"bound": "tensor", "kernel": "prefill GA (hattn_prefill window=0: "
+                                                  "key-rotation pass + prefill_kernel)",
                      "achieved": round(ga["flops"] / ga_s / 1e12, 2),
-                     "peak": tf_sust, "unit": "TFLOP/s",
-                     "frac": round(ga["flops"] / ga_s / 1e12 / tf_sust, 4),
-                     "traffic": None,
-                     "peak_source": f"{src} bf16_tflops_sustained"},
+                     "peak": ga_tf, "unit": "TFLOP/s",
+                     "frac": round(ga["flops"] / ga_s / 1e12 / ga_tf, 4),
+                     "traffic": ga_traffic, "traffic_source": ga_traffic_src,
+                     "algorithmic_bytes": ga["bytes"],
+                     "peak_source": f"{src} {ga_tf_name} (of measured; step SM clock median "
+                                    f"{clocks.get('sm_mhz')} MHz)"},
         "e2e": e2e,
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
+    if args.extras and world == 1:
+        # the other workloads of the path, timed after the step on the same
+        # GPU: the hybrid block at 256K (a10) and the backward of both layers
+        del wl
+        torch.cuda.empty_cache()
+        out["extra_workloads"] = {
+            "hybrid_block_256k": _extra(run_hybrid_block(argparse.Namespace(steps=2, warmup=1))),
+            "backward_32k": _extra(run_backward(argparse.Namespace(steps=5, warmup=3))),
+        }
     if rank == 0 and args.cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     return out
+
+
+def _extra(line):
+    """A workload's own result line, less the keys the main line already states."""
+    drop = ("metric", "data", "higher_is_better", "scaling", "vs_baseline", "dtype", "n_gpus")
+    return {k: v for k, v in line.items() if k not in drop}
 
 
 def run_e2e(wl, args, stream, sptr):
@@ -383,16 +454,43 @@ def run_e2e(wl, args, stream, sptr):
     h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
     d2h = sum(t.numel() * t.element_size() for t in host_out + host_lse)
 
+    # Copies overlap the layers: uploads run on one copy stream, read-backs on
+    # another, the C-ABI calls on the compute stream.  Part i's inputs go up
+    # as soon as the previous step's part i no longer needs its buffers (so
+    # the next step's uploads run under this step's layers), and its outputs
+    # come back while the next part computes; part i's next call waits for
+    # that read-back before rewriting its outputs.
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    nparts = len(dev_in)
+    uploaded = [torch.cuda.Event() for _ in range(nparts)]
+    computed = [torch.cuda.Event() for _ in range(nparts)]
+    read_back = [torch.cuda.Event() for _ in range(nparts)]
+    part_outs = [[outs[i], lses[i]] for i in range(nparts)]
+    part_host = [[host_out[i], host_lse[i]] for i in range(nparts)]
+
+    def run_part(i):
+        if i < len(wl.layers):
+            wl.run_prefill(wl.layers[i], sptr, *dev_in[i])
+        else:
+            wl.run_decode(wl.dec[i - len(wl.layers)], sptr, *dev_in[i])
+
     def step():
-        for hs, ds in zip(host_in, dev_in):
-            for h, d in zip(hs, ds):
-                d.copy_(h, non_blocking=True)
-        for i, lay in enumerate(wl.layers):
-            wl.run_prefill(lay, sptr, *dev_in[i])
-        for i, dd in enumerate(wl.dec):
-            wl.run_decode(dd, sptr, *dev_in[2 + i])
-        for o, h in zip(outs + lses, host_out + host_lse):
-            h.copy_(o, non_blocking=True)
+        for i in range(nparts):
+            up.wait_event(computed[i])  # the previous step's part i is done with its inputs
+            with torch.cuda.stream(up):
+                for h, d in zip(host_in[i], dev_in[i]):
+                    d.copy_(h, non_blocking=True)
+            uploaded[i].record(up)
+        for i in range(nparts):
+            stream.wait_event(uploaded[i])
+            stream.wait_event(read_back[i])  # the previous step's outputs of part i are home
+            run_part(i)
+            computed[i].record(stream)
+            down.wait_event(computed[i])
+            with torch.cuda.stream(down):
+                for o, h in zip(part_outs[i], part_host[i]):
+                    h.copy_(o, non_blocking=True)
+            read_back[i].record(down)
 
     for _ in range(max(1, args.warmup)):
         step()
@@ -400,14 +498,19 @@ def run_e2e(wl, args, stream, sptr):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = max(1, min(args.steps, 5))
     start.record(stream)
+    up.wait_event(start)
+    down.wait_event(start)
     for _ in range(n):
         step()
+    stream.wait_stream(up)
+    stream.wait_stream(down)
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / n
     return {"value": round(wl.flops() / (ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h)}
+            "d2h_bytes_per_step": int(d2h),
+            "copies": "uploads and read-backs on two copy streams, overlapping the layers"}
 
 
 # --------------------------------------------------------------------- CPU oracle arm
@@ -511,6 +614,30 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def launch_replicas(n, argv):
+    """Start n ranks of this script on this node (torch's launcher, rendezvous
+    on 127.0.0.1), one per local GPU; rank 0 prints the line.  Returns the
+    launcher's exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def launch_check(rank, world):
+    """The replica launch without attention work: every rank meets the others
+    at a barrier and the line carries the largest rank and the world size."""
+    barrier(world)
+    top = max_over_ranks(float(rank), world)
+    return {"launch_check": True, "n_gpus": world, "max_rank": int(top),
+            "backend": __import__("torch.distributed", fromlist=["x"]).get_backend()
+            if world > 1 else None}
+
+
 def whole_job_tflops(flops_per_rank_step, world, ms_per_step):
     """Whole-job throughput: every rank runs the same step (weak scaling), the
     step takes the slowest rank's time."""
@@ -574,14 +701,17 @@ def run_hybrid_block(args):
     flops = sum(l["flops"] for l in layers)
     byts = sum(l["bytes"] for l in layers)
     parts = {}
+    frac = 0.0
     for i, lay in enumerate(layers):
         t = statistics.mean(e[i][0].elapsed_time(e[i][1]) for e in ev) / 1e3
-        bf = lay["flops"] / (tf_sust * 1e12)
+        tf, tf_name = tensor_peak(t, tf_burst, tf_sust)
+        bf = lay["flops"] / (tf * 1e12)
         bb = lay["bytes"] / (hbm * 1e9)
+        frac += max(bf, bb)
         parts[f"layer{i}_{lay['kind']}"] = dict(ms=t * 1e3, tflops=lay["flops"] / t / 1e12,
                                                  gbs=lay["bytes"] / t / 1e9,
-                                                 roofline_frac=max(bf, bb) / t)
-    frac = sum(max(l["flops"] / (tf_sust * 1e12), l["bytes"] / (hbm * 1e9)) for l in layers)
+                                                 roofline_frac=max(bf, bb) / t,
+                                                 peak="hbm_gbs" if bb > bf else tf_name)
     return {"metric": METRIC, "value": round(flops / (ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
@@ -650,6 +780,7 @@ def run_prefix_prefill(args):
     byts = (S * (hq * D_QK * 2 + hkv * (D_QK + D_V) * 2 * 2 + hq * D_V * 2 + hq * 4)
             + P * hkv * (D_QK + D_V) * 2 + hq * 4)
     t = ms / 1e3
+    tf, tf_name = tensor_peak(t, tf_burst, tf_sust)
     return {"metric": METRIC, "value": round(flops / t / 1e12, 3), "unit": "TFLOP/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -658,9 +789,9 @@ def run_prefix_prefill(args):
             "config": {"workload": "prefix_prefill: global layer (64q/4kv, base 5e6), 4096 new "
                                    "tokens over a cached prefix of 28672"},
             "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 2),
-                         "peak": tf_sust, "unit": "TFLOP/s",
-                         "frac": round(flops / t / 1e12 / tf_sust, 4), "traffic": None,
-                         "peak_source": f"{src} bf16_tflops_sustained"},
+                         "peak": tf, "unit": "TFLOP/s",
+                         "frac": round(flops / t / 1e12 / tf, 4), "traffic": None,
+                         "peak_source": f"{src} {tf_name}"},
             "algorithmic": {"flops": flops, "bytes": byts}, "clocks": clk.summary()}
 
 
@@ -724,6 +855,7 @@ def run_backward(args):
     flops = sum(L["flops"] for L in layers)
     swa, ga = layers
     ga_tf = ga["flops"] / t_ga / 1e12
+    tf_sust, tf_name = tensor_peak(t_ga, tf_burst, tf_sust)
     return {"metric": "prefill backward TFLOP/s (SWA+GA sink attention) vs B300 roofline",
             "value": round(flops / t / 1e12, 3), "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 4),
@@ -735,14 +867,14 @@ def run_backward(args):
             "roofline": {"bound": "tensor", "achieved": round(ga_tf, 2), "peak": tf_sust,
                          "unit": "TFLOP/s", "frac": round(ga_tf / tf_sust, 4), "traffic": None,
                          "kernel": "global layer backward (dK/dV + dQ kernels)",
-                         "peak_source": f"{src} bf16_tflops_sustained"},
+                         "peak_source": f"{src} {tf_name}"},
             "parts": {"swa_backward": {"ms": round(t_swa * 1e3, 4),
                                        "GB/s": round(swa["bytes"] / t_swa / 1e9, 1),
                                        "frac_hbm": round(swa["bytes"] / t_swa / 1e9 / hbm, 4),
                                        "bytes": swa["bytes"]},
                       "ga_backward": {"ms": round(t_ga * 1e3, 4), "TFLOP/s": round(ga_tf, 2),
-                                      "frac_tensor_sustained": round(ga_tf / tf_sust, 4),
-                                      "flops": ga["flops"]}},
+                                      "frac_tensor": round(ga_tf / tf_sust, 4),
+                                      "peak": tf_name, "flops": ga["flops"]}},
             "gpu_launches": 8 * args.steps,  # prep, sink sum, dK/dV, dQ per layer
             "clocks": clk.summary()}
 
@@ -890,6 +1022,13 @@ def main():
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--cpu-baseline", type=int, default=1)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--extras", type=int, default=1,
+                    help="also time the hybrid block at 256K and the backward after the step "
+                         "(N = 1 only)")
+    ap.add_argument("--launch-check", action="store_true",
+                    help="with --gpus N: start the N ranks, meet at a barrier, take the max "
+                         "over ranks and print one line (no attention work; checks the "
+                         "replica launch)")
     ap.add_argument("--profile-case", default=None,
                     help="swa_prefill | ga_prefill | decode_swa | decode_ga | swa_backward | "
                          "ga_backward: one call, for ncu")
@@ -919,6 +1058,9 @@ def main():
     if args.workload == "paged_decode":
         print(json.dumps(run_paged_decode(args)))
         return
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # not started by a launcher: start one rank per GPU on this node
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
@@ -927,9 +1069,15 @@ def main():
         return
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-        dist.init_process_group("nccl")
-    res = run_cuda(args, rank, world)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    if args.launch_check:
+        res = launch_check(rank, world)
+    else:
+        res = run_cuda(args, rank, world)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

@@ -298,8 +298,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int per = a.batch * a.hkv;
   const int kb = blockIdx.x / per, rem = blockIdx.x - kb * per;
   const int b = rem / a.hkv, g = rem - b * a.hkv;
-  const int tok0 = __ldg(a.cu_seqlens + b);
-  const int L = __ldg(a.cu_seqlens + b + 1) - tok0;
+  // a sequence with out-of-range offsets is skipped (its key block 0 reports it)
+  int tok0, L;
+  if (!seq_slice(a.cu_seqlens, b, a.total, a.max_seqlen, a.ctl, kb == 0 && threadIdx.x == 0,
+                 tok0, L))
+    return;  // uniform over the CTA, before any barrier or TMEM use
   const int k0 = kb * 128;
   if (k0 >= L) return;  // uniform over the CTA, before any barrier or TMEM use
   const int qend = WIN ? min(L, k0 + 128 + a.window - 1) : L;
@@ -534,20 +537,24 @@ struct DqBars {
 static_assert(sizeof(DqBars) <= 256, "barrier area");
 
 // Unit u: (query tile, sequence b, KV head g); a global layer's latest (longest)
-// tiles first.  An empty unit (tile past its sequence's end) is skipped.
+// tiles first.  An empty unit (tile past its sequence's end) is skipped, and
+// so is every unit of a sequence whose offsets are out of range (`report`:
+// record that; the loader, which walks every unit, reports).
 struct DqUnit {
   int b, g, tok0, L, t0, kstart, nblk;
 };
 template <int G, bool WIN>
-__device__ __forceinline__ bool dq_unit(int u, const BackwardArgs& a, int nqt, DqUnit& du) {
+__device__ __forceinline__ bool dq_unit(int u, const BackwardArgs& a, int nqt, DqUnit& du,
+                                        bool report = false) {
   constexpr int TQ = 128 / G;
   const int per = a.batch * a.hkv;
   const int q_ord = u / per, rem = u - q_ord * per;
   const int qt = WIN ? q_ord : nqt - 1 - q_ord;
   du.b = rem / a.hkv;
   du.g = rem - du.b * a.hkv;
-  du.tok0 = __ldg(a.cu_seqlens + du.b);
-  du.L = __ldg(a.cu_seqlens + du.b + 1) - du.tok0;
+  if (!seq_slice(a.cu_seqlens, du.b, a.total, a.max_seqlen, a.ctl, report && q_ord == 0,
+                 du.tok0, du.L))
+    return false;
   du.t0 = qt * TQ;
   if (du.t0 >= du.L) return false;
   du.kstart = WIN ? max(0, du.t0 - a.window + 1) : 0;
@@ -615,7 +622,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
         DqUnit du;
-        if (!dq_unit<G, WIN>(u, a, nqt, du)) continue;
+        if (!dq_unit<G, WIN>(u, a, nqt, du, true)) continue;
         // Q' and dout of the tile, once the previous tile's products are done with them
         if (nu > 0 && !mbar_wait(&bars->fixed_empty, (nu - 1) & 1, a.ctl, abort)) break;
         const int qrow = du.tok0 + du.t0;

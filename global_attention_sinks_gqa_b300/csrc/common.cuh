@@ -27,6 +27,22 @@ __device__ __forceinline__ void record_status(const DeviceCtl& ctl, unsigned int
   atomicCAS(ctl.status, 0u, code);
 }
 
+// Rows [tok0, tok0 + L) of sequence b of a packed batch, from its offsets.
+// The offsets live in device memory, where the host cannot check them: a
+// sequence whose slice is not inside [0, total) or is longer than max_len is
+// reported invalid (false), and the caller skips it, writing none of its
+// rows.  `report`: record HATTN_ERR_INVALID_ARG for it (one role per kernel
+// reports, so that a bad batch costs a handful of atomics).
+__device__ __forceinline__ bool seq_slice(const int* cu, int b, long total, int max_len,
+                                          const DeviceCtl& ctl, bool report, int& tok0, int& L) {
+  tok0 = cu[b];
+  const int end = cu[b + 1];
+  L = end - tok0;
+  const bool ok = tok0 >= 0 && L >= 0 && long(end) <= total && L <= max_len;
+  if (!ok && report) record_status(ctl, HATTN_ERR_INVALID_ARG);
+  return ok;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

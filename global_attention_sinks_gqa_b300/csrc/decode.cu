@@ -1625,7 +1625,8 @@ int decode_num_splits(int max_seqlen_k, int T, int window, int is_ring, int cap,
   if (is_ring)
     range = max_seqlen_k < cap ? max_seqlen_k : cap;
   else if (window > 0)
-    range = max_seqlen_k < window + T - 1 ? max_seqlen_k : window + T - 1;
+    // 64-bit: a window near INT_MAX must not wrap around
+    range = long(max_seqlen_k) < long(window) + T - 1 ? max_seqlen_k : window + T - 1;
   else
     range = max_seqlen_k;
   if (range <= kSingleChunkMax) {

@@ -13,7 +13,10 @@
 // The array lives in every GPU that loads the library, until the process
 // exits.  In host code its name is only a host-side stand-in, not a device
 // address, so the device address is looked up with cudaGetSymbolAddress once
-// per device, with that device current, on the first call made on it.
+// per device, with that device current, on the first call made on it.  The
+// address is kept for the life of the process: it belongs to the device's
+// context, so a cudaDeviceReset() (which ends that context) leaves it stale.
+// A process that resets a device must not call this entry point on it again.
 #include <mutex>
 
 #include "hattn_internal.h"
@@ -49,6 +52,12 @@ extern "C" hattn_status_t hattn_decode_static_scratch(
     const float* sink, void* out, float* lse, int B, int T, int hq, int hkv, int dqk, int dv,
     int cap, int is_ring, int window, int max_seqlen_k, int rope_dim, float rope_base,
     float softmax_scale, void* stream) {
+  // a malformed call reports its argument error, not a scratch shortfall
+  bool empty = false;
+  const hattn_status_t st = hattn::decode_check_args(
+      q, nullptr, nullptr, k_cache, v_cache, seqlens_k, sink, out, lse, B, T, hq, hkv, dqk, dv,
+      cap, is_ring, window, max_seqlen_k, rope_dim, rope_base, softmax_scale, &empty);
+  if (st != HATTN_OK || empty) return st;
   const size_t need =
       hattn_decode_workspace_size(B, T, hq, hkv, dv, max_seqlen_k, window, cap, is_ring);
   if (need > size_t(HATTN_DECODE_STATIC_SCRATCH_BYTES)) return HATTN_ERR_WORKSPACE;

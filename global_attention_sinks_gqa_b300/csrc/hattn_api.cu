@@ -110,6 +110,41 @@ cudaError_t launch_lost_arrival_selftest(const DeviceCtl& ctl, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// The argument checks of a decode step (everything but the workspace);
+// *empty is set when there is nothing to launch (B == 0).
+hattn_status_t decode_check_args(const void* q, const void* k_new, const void* v_new,
+                                 const void* k_cache, const void* v_cache, const int* seqlens_k,
+                                 const float* sink, const void* out, const float* lse, int B,
+                                 int T, int hq, int hkv, int dqk, int dv, int cap, int is_ring,
+                                 int window, int max_seqlen_k, int rope_dim, float rope_base,
+                                 float softmax_scale, bool* empty) {
+  *empty = false;
+  hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
+  if (st != HATTN_OK) return st;
+  if (B < 0 || T <= 0 || cap <= 0 || window < 0 || max_seqlen_k < T ||
+      (is_ring != 0 && is_ring != 1))
+    return HATTN_ERR_INVALID_ARG;
+  if (T > 8 || (hq / hkv) * T > 128) return HATTN_ERR_UNSUPPORTED;
+  if (is_ring && window == 0) return HATTN_ERR_INVALID_ARG;  // a ring only holds a window
+  // 64-bit: a window near INT_MAX must not wrap around
+  if (is_ring && long(cap) < long(window) + T - 1) return HATTN_ERR_RING_TOO_SMALL;
+  if (!is_ring && max_seqlen_k > cap) return HATTN_ERR_INVALID_ARG;
+  if (!finite_positive(rope_base) || !finite_positive(softmax_scale)) return HATTN_ERR_INVALID_ARG;
+  if (B == 0) {
+    *empty = true;
+    return HATTN_OK;
+  }
+  if (!q || !k_cache || !v_cache || !seqlens_k || !sink || !out) return HATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) || (reinterpret_cast<uintptr_t>(sink) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return HATTN_ERR_INVALID_ARG;
+  const bool append = k_new != nullptr || v_new != nullptr;
+  if (append && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+    return HATTN_ERR_INVALID_ARG;
+  return HATTN_OK;
+}
+
 }  // namespace hattn
 
 using namespace hattn;
@@ -373,25 +408,13 @@ hattn_status_t decode_step(const void* q, const void* k_new, const void* v_new, 
                            int is_ring, int window, int max_seqlen_k, int rope_dim,
                            float rope_base, float softmax_scale, void* workspace,
                            size_t workspace_bytes, void* stream, const Paging& pg = Paging()) {
-  hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
-  if (st != HATTN_OK) return st;
-  if (B < 0 || T <= 0 || cap <= 0 || window < 0 || max_seqlen_k < T ||
-      (is_ring != 0 && is_ring != 1))
-    return HATTN_ERR_INVALID_ARG;
-  if (T > 8 || (hq / hkv) * T > 128) return HATTN_ERR_UNSUPPORTED;
-  if (is_ring && window == 0) return HATTN_ERR_INVALID_ARG;  // a ring only holds a window
-  if (is_ring && cap < window + T - 1) return HATTN_ERR_RING_TOO_SMALL;
-  if (!is_ring && max_seqlen_k > cap) return HATTN_ERR_INVALID_ARG;
-  if (!finite_positive(rope_base) || !finite_positive(softmax_scale)) return HATTN_ERR_INVALID_ARG;
-  if (B == 0) return HATTN_OK;
-  if (!q || !k_cache || !v_cache || !seqlens_k || !sink || !out) return HATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) || (reinterpret_cast<uintptr_t>(sink) & 3u) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return HATTN_ERR_INVALID_ARG;
-  const bool append = k_new != nullptr || v_new != nullptr;
-  if (append && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
-    return HATTN_ERR_INVALID_ARG;
+  bool empty = false;
+  hattn_status_t st = decode_check_args(q, k_new, v_new, k_cache, v_cache, seqlens_k, sink, out,
+                                        lse, B, T, hq, hkv, dqk, dv, cap, is_ring, window,
+                                        max_seqlen_k, rope_dim, rope_base, softmax_scale, &empty);
+  if (st != HATTN_OK || empty) return st;
+  // a window covering every key of a linear cache is global attention
+  if (!is_ring && long(window) >= long(max_seqlen_k)) window = 0;
   DecodeArgs a;
   a.q = q;
   a.k_cache = k_cache;

@@ -118,6 +118,14 @@ struct DecodeArgs {
   DeviceCtl ctl;
 };
 int decode_num_splits(int max_seqlen_k, int T, int window, int is_ring, int cap, int* chunk);
+// The argument checks of hattn_decode() / hattn_decode_append() (all but the
+// workspace; hattn_api.cu).  *empty: nothing to launch (B == 0).
+hattn_status_t decode_check_args(const void* q, const void* k_new, const void* v_new,
+                                 const void* k_cache, const void* v_cache, const int* seqlens_k,
+                                 const float* sink, const void* out, const float* lse, int B,
+                                 int T, int hq, int hkv, int dqk, int dv, int cap, int is_ring,
+                                 int window, int max_seqlen_k, int rope_dim, float rope_base,
+                                 float softmax_scale, bool* empty);
 size_t decode_workspace_bytes(int B, int T, int hq, int nsplit);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

@@ -183,10 +183,14 @@ struct UnitInfo {
 };
 
 // Unit u of the persistent loop.  Global units run latest (longest) first so
-// the tail of the schedule is short; window units run in order.
+// the tail of the schedule is short; window units run in order.  False for a
+// unit past its sequence's end and for every unit of a sequence whose
+// device-resident offsets (or prefix) are out of range; `report` records
+// the latter as HATTN_ERR_INVALID_ARG (the producer, which sees every unit
+// once, reports).
 template <int G, int BN, bool WIN>
 __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, const int* cu, int nut,
-                                          UnitInfo& ui) {
+                                          UnitInfo& ui, bool report = false) {
   constexpr int UT = 256 / G;
   const int per = a.batch * a.hkv;
   const int q_ord = u / per;
@@ -194,11 +198,14 @@ __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, const int
   const int qt = WIN ? q_ord : (nut - 1 - q_ord);
   ui.b = rem / a.hkv;
   ui.g = rem - ui.b * a.hkv;
-  ui.tok0 = cu[ui.b];
-  ui.L = cu[ui.b + 1] - ui.tok0;
+  if (!seq_slice(cu, ui.b, a.total, a.max_seqlen, a.ctl, report, ui.tok0, ui.L)) return false;
   ui.t0 = qt * UT;
   if (ui.t0 >= ui.L) return false;
   ui.P = a.prefix != nullptr ? __ldg(a.prefix + ui.b) : 0;
+  if (a.prefix != nullptr && (ui.P < 0 || long(ui.P) + ui.L > a.cap)) {
+    if (report) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
+    return false;
+  }
   const int qend = ui.P + min(ui.t0 + UT, ui.L);  // one past the last valid query position
   ui.kstart = WIN ? max(0, ui.P + ui.t0 - a.window + 1) : 0;
   ui.nblk = (qend - ui.kstart + BN - 1) / BN;
@@ -515,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u;
         do {
           u = int(atomicAdd(a.unit_ctr, 1u));
-        } while (u < nunits && !unit_info<G, BN, WIN>(u, a, cu, nut, ui));
+        } while (u < nunits && !unit_info<G, BN, WIN>(u, a, cu, nut, ui, true));
         if (u >= nunits) u = -1;
         bars->unit[q] = u;
         mbar_arrive(&bars->unit_full[q]);

@@ -94,7 +94,12 @@ size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk);
  *   batch      number of sequences (>= 1)
  *   cu_seqlens int32 [batch + 1] DEVICE; cu_seqlens[0] = 0, non-decreasing,
  *              cu_seqlens[batch] = total_tokens.  RoPE positions restart at 0
- *              in every sequence.
+ *              in every sequence.  The offsets are device memory the host
+ *              cannot read: the kernels check them, and a sequence whose rows
+ *              [cu_seqlens[b], cu_seqlens[b+1]) are not inside
+ *              [0, total_tokens) or number more than max_seqlen is skipped --
+ *              none of its out / lse rows is written -- and
+ *              HATTN_ERR_INVALID_ARG is recorded in the device status.
  *   max_seqlen an upper bound of every sequence length (sizes the grid)
  *   window     > 0: sliding window of `window` keys including the query;
  *              0: global causal attention
@@ -142,8 +147,9 @@ size_t hattn_prefill_backward_workspace_size(long total_tokens, int hq, int hkv)
  *   grad_v     bf16 [total_tokens, hkv, dv]  written
  *   grad_sink  fp32 [hq] DEVICE, written (summed over every row of the head)
  *   workspace  DEVICE scratch of >= hattn_prefill_backward_workspace_size()
- *   other arguments as for hattn_prefill().  Outputs must not overlap inputs
- *   or the workspace.  Every gradient row is written by one thread and no
+ *   other arguments as for hattn_prefill() (a sequence whose offsets fail the
+ *   device-side check is skipped: none of its gradient rows is written).
+ *   Outputs must not overlap inputs or the workspace.  Every gradient row is written by one thread and no
  *   atomics are used: the results are the same on every run.  The products
  *   take bf16 operands (P, dS and the rotated dims rounded to bf16) with fp32
  *   accumulation.
@@ -204,7 +210,9 @@ hattn_status_t hattn_rope_kv_append(const void* k_new, const void* v_new, const 
  *               bound of prefix_lens; prefix_lens[b] + L_b <= cap
  *   workspace   DEVICE scratch of >= 256 bytes (the kernel's work counter)
  *   other arguments as for hattn_prefill().
- * A position outside [0, cap) is skipped and recorded as HATTN_ERR_INVALID_ARG.
+ * A position outside [0, cap) is skipped and recorded as HATTN_ERR_INVALID_ARG;
+ * the attention skips a sequence whose offsets fail hattn_prefill()'s check or
+ * whose prefix_lens[b] + L_b leaves [0, cap] (its out / lse rows are not written).
  */
 hattn_status_t hattn_prefill_cached(const void* q, const void* k_new, const void* v_new,
                                     void* k_cache, void* v_cache, const int* cu_seqlens,
@@ -336,9 +344,15 @@ hattn_status_t hattn_decode_append_paged(const void* q, const void* k_new, const
  *   - Allocates nothing: no cudaMalloc / cudaFree, no allocating library call.
  *   - A step whose scratch need (hattn_decode_workspace_size()) exceeds that
  *     size returns HATTN_ERR_WORKSPACE and launches nothing.
+ *   - Arguments are checked as hattn_decode() checks them (same status
+ *     codes) before the scratch need is compared with the array's size.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.  A failed lookup returns HATTN_ERR_CUDA.
+ *     The address is kept until the process exits; it belongs to the
+ *     device's context, so after cudaDeviceReset() on that device this entry
+ *     point must not be called there again (the same holds for every entry
+ *     point: the device status word's address is cached the same way).
  *   - Every call shares the one array per device and it keeps the last
  *     call's contents.  Nothing in it needs to start at zero: every partial
  *     result is written before it is read.  Calls that overlap on the GPU

@@ -116,6 +116,32 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
     assert _decode(**kw) == code
 
 
+def test_decode_window_near_int_max_does_not_wrap(lib):
+    """A window of INT_MAX ('no window') must not wrap window + T - 1 into a
+    negative number: a ring would then pass the capacity check."""
+    assert _decode(window=2**31 - 1) == ha.HATTN_ERR_RING_TOO_SMALL
+    # over a linear cache such a window is global attention (same workspace need)
+    assert _decode(is_ring=0, window=2**31 - 1, hkv=4, cap=65536) == ha.HATTN_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dqk=64), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(T=9), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(hq=64, hkv=5), ha.HATTN_ERR_INVALID_ARG),
+    (dict(q=None), ha.HATTN_ERR_INVALID_ARG),
+    (dict(), ha.HATTN_ERR_WORKSPACE),        # valid, but its partials exceed the array
+])
+def test_static_scratch_checks_arguments_before_its_size(lib, kw, code):
+    """A malformed call to the allocation-free decode step reports its argument
+    error even when its scratch need would also exceed the fixed array."""
+    args = dict(q=FAKE, k_cache=FAKE, v_cache=FAKE, seqlens_k=FAKE, sink=FAKE, out=FAKE,
+                lse=FAKE, B=64, T=4, hq=64, hkv=4, dqk=192, dv=128, cap=65536, is_ring=0,
+                window=0, max_seqlen_k=65536, rope_dim=64, rope_base=5e6, softmax_scale=0.07,
+                stream=0)
+    args.update(kw)
+    assert ha.hattn_decode_static_scratch(**args) == code
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(T=0), ha.HATTN_ERR_INVALID_ARG),
     (dict(T=200, cap=131), ha.HATTN_ERR_INVALID_ARG),

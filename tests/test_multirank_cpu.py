@@ -58,3 +58,37 @@ def test_reference_arm_runs_on_rank_zero_only():
                        text=True, timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_gpus_flag_launches_that_many_ranks():
+    """`bench.py --gpus 2` started without a launcher starts two ranks itself
+    (gloo here, where there is no GPU); rank 0 alone prints the line, which
+    reports both ranks."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--launch-check"], env=env, capture_output=True, text=True, timeout=300,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    import json
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2 and out["max_rank"] == 1 and out["launch_check"]
+
+
+def test_recorded_traffic_is_dropped_once_the_kernel_changes(tmp_path, monkeypatch):
+    """The roofline's traffic figure is a recorded ncu count; it is reported
+    only while the digest of the kernel's sources matches the capture's."""
+    import json
+    import bench
+    rec = {"k": {"kind": "prefill", "sources": bench.sources_digest("prefill"),
+                 "dram_bytes": 123, "profile": "profiles/x.md"}}
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("k") == (123, "profiles/x.md")
+    rec["k"]["sources"] = "0" * 16
+    f.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("k")[0] is None
+    assert bench.recorded_traffic("missing")[0] is None

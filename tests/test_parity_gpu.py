@@ -48,6 +48,19 @@ def test_prefill_window_widths(window):
     compare(out, lse, o_ref, l_ref, f"W={window}")
 
 
+@pytest.mark.parametrize("G,window", [(4, 5), (4, 64), (4, 97), (2, 1), (2, 16), (2, 33),
+                                      (16, 130), (16, 145)])
+def test_prefill_window_two_block_tiles(G, window):
+    """Window units whose band (W - 1 + 256 / G keys) fits two 80-key blocks
+    but not the one-block tile: G = 4 up to W = 97, G = 2 up to W = 33, and
+    G = 16 just past the 144-key one-block band (W = 130 .. 145); ragged
+    lengths so that tiles end mid-block."""
+    c = synth.prefill_case(RAGGED, 2 * G, 2, window=window, rope_base=1e4, seed=800 + G + window)
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"two-block window tiles G={G} W={window}")
+
+
 def test_prefill_window_covering_sequence_is_global():
     c = synth.prefill_case([600], 8, 1, window=600, rope_base=1e4, seed=300)
     out_w, lse_w = gpu_prefill(c)
