@@ -3,9 +3,10 @@
 One step = one pass of the whole path over one batch of synthetic inputs:
   1. SWA layer prefill, seq 32768, 64 query / 8 KV heads, W = 128, base 1e4
   2. GA layer prefill, seq 32768, 64 query / 4 KV heads, global, base 5e6
-  3. decode / MTP-verify, batch 64 x 4 query tokens: append of the 4 new
-     tokens + decode, for an SWA layer (131-slot ring, 8 KV heads) and a GA
-     layer (lengths uniform in [8K, 64K], 4 KV heads)
+  3. decode / MTP-verify of one hybrid block, batch 64 x 4 query tokens:
+     append of the 4 new tokens + decode, for its five SWA layers (each a
+     131-slot ring, 8 KV heads; called back to back) and its GA layer
+     (lengths uniform in [8K, 64K], 4 KV heads)
 All inputs are bf16 ~ N(0, 1), sinks ~ N(0, 1) (seeded, synthetic).
 
 Prints ONE JSON line (rank 0).  `value` = algorithmic FLOPs of the step /
@@ -40,6 +41,7 @@ import synth  # noqa: E402
 
 METRIC = "prefill TFLOP/s & decode HBM GB/s (SWA+GA sink attention) vs B300 roofline"
 D_QK, D_V, R = 192, 128, 64
+DECODE_SWA_LAYERS = 5  # window layers per hybrid block (5 SWA : 1 GA)
 PAIR_FLOPS = 2 * (D_QK + D_V)  # FLOPs per (query row, visible key) pair and head
 
 
@@ -201,11 +203,12 @@ def recorded_traffic(key):
 
 
 def step_config(world: int = 1):
-    return {"workload": "swa_prefill_32k + ga_prefill_32k + decode_b64_t4 (swa ring 131 "
+    return {"workload": "swa_prefill_32k + ga_prefill_32k + decode_b64_t4 (5 x swa ring 131 "
                         "+ ga 8K-64K)",
             "swa_prefill": "seq 32768, 64q/8kv, W=128, d_qk 192, d_v 128, rope 64 @1e4",
             "ga_prefill": "seq 32768, 64q/4kv, global, rope 64 @5e6",
-            "decode": "batch 64 x 4 verify tokens; swa 8kv ring 131; ga 4kv L~U[8192,65536]",
+            "decode": "batch 64 x 4 verify tokens; 5 swa layers (8kv ring 131 each) + 1 ga "
+                      "layer (4kv, L~U[8192,65536])",
             "l2": "inputs larger than L2 (no flush needed)",
             "parallelism": f"replicas x{world}"}
 
@@ -238,12 +241,16 @@ class Workload:
         self.B, self.T = dc["B"], dc["T"]
         self.lens = synth.random_lengths(self.B, dc["lens"][0], dc["lens"][1], dc["seed"])
         self.lmax = dc["lens"][1]
+        # the decode step of one hybrid block: its five window layers (each
+        # with its own 131-slot ring), called back to back, then its global layer
         self.dec = []
-        for kind, cap, ring in (("swa", 131, True), ("ga", self.lmax, False)):
+        for kind, cap, ring, nl in (("swa", 131, True, DECODE_SWA_LAYERS),
+                                    ("ga", self.lmax, False, 1)):
             p = dc[kind]
-            dd = self._decode_layer(p, cap, ring, dc["seed"] + (0 if ring else 1))
-            dd.update(kind=kind, cap=cap, ring=ring, p=p)
-            self.dec.append(dd)
+            for li in range(nl):
+                dd = self._decode_layer(p, cap, ring, dc["seed"] + (0 if ring else 1) + 100 * li)
+                dd.update(kind=kind, cap=cap, ring=ring, p=p, layer=li)
+                self.dec.append(dd)
 
     def _decode_layer(self, p, cap, ring, seed):
         ha, dev, B, T = self.ha, self.dev, self.B, self.T
@@ -330,19 +337,23 @@ def run_cuda(args, rank, world):
             n += wl.run_prefill(lay, sptr)
             if events is not None:
                 events[f"p{i}"][1].record(stream)
-        for i, dd in enumerate(wl.dec):
+        # the window layers' calls back to back (one event pair around them),
+        # then the global layer's
+        for kind in ("swa", "ga"):
             if events is not None:
-                events[f"d{i}"][0].record(stream)
-            n += wl.run_decode(dd, sptr)
+                events[f"d_{kind}"][0].record(stream)
+            for dd in wl.dec:
+                if dd["kind"] == kind:
+                    n += wl.run_decode(dd, sptr)
             if events is not None:
-                events[f"d{i}"][1].record(stream)
+                events[f"d_{kind}"][1].record(stream)
         return n
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     wl.ha.check_device_status()
-    keys = ["p0", "p1", "d0", "d1"]
+    keys = ["p0", "p1", "d_swa", "d_ga"]
     ev = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for k in keys} for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -379,13 +390,16 @@ def run_cuda(args, rank, world):
                                   roofline_frac=max(bound_f, bound_b) / t,
                                   bound="tensor" if bound_f > bound_b else "hbm",
                                   peak="hbm_gbs" if bound_b > bound_f else tf_name)
-    for i, dd in enumerate(wl.dec):
-        t = part_ms[f"d{i}"] / 1e3
+    for kind in ("swa", "ga"):
+        lays = [dd for dd in wl.dec if dd["kind"] == kind]
+        t = part_ms[f"d_{kind}"] / 1e3 / len(lays)  # per layer
+        dd = lays[0]
         byts = dd["bytes"] + dd["abytes"]
-        parts[f"decode_{dd['kind']}_b64_t4"] = dict(
-            ms=part_ms[f"d{i}"], tflops=dd["flops"] / t / 1e12, gbs=byts / t / 1e9,
+        parts[f"decode_{kind}_b64_t4"] = dict(
+            ms=t * 1e3, tflops=dd["flops"] / t / 1e12, gbs=byts / t / 1e9,
             roofline_frac=byts / (hbm * 1e9) / t, bound="hbm", peak="hbm_gbs",
-            verify_tokens_per_s=wl.B * wl.T / t)
+            verify_tokens_per_s=wl.B * wl.T / t, layers=len(lays),
+            timing="per layer: one event pair around the layers' calls back to back")
     ga = wl.layers[1]
     ga_s = part_ms["p1"] / 1e3
     ga_tf, ga_tf_name = tensor_peak(ga_s, tf_burst, tf_sust)

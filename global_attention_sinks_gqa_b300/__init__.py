@@ -44,6 +44,8 @@ SIGNATURES = {
                            _P, _Z, _P]),
     "hattn_prefill_cached": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _L, _I, _I, _I, _I,
                                   _I, _I, _I, _I, _F, _I, _F, _P, _Z, _P]),
+    "hattn_prefill_shard": (_I, [_P, _P, _P, _P, _P, _P, _L, _I, _L, _I, _I, _I, _I, _I, _F, _I,
+                                 _F, _P, _Z, _P]),
     "hattn_prefill_backward_workspace_size": (_Z, [_L, _I, _I]),
     "hattn_prefill_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _L, _I, _I,
                                     _I, _I, _I, _I, _F, _I, _F, _P, _Z, _P]),
@@ -145,6 +147,15 @@ def hattn_prefill(q, k, v, sink, out, lse, batch, cu_seqlens, total_tokens, max_
         int(total_tokens), int(max_seqlen), int(hq), int(hkv), int(dqk), int(dv), int(rope_dim),
         float(rope_base), int(window), float(softmax_scale), _ptr(workspace), int(workspace_bytes),
         _stream(stream))
+
+
+def hattn_prefill_shard(q, k, v, sink, out, lse, shard_tokens, halo, pos0, hq, hkv, dqk, dv,
+                        rope_dim, rope_base, window, softmax_scale, workspace, workspace_bytes,
+                        stream=None) -> int:
+    return load_library().hattn_prefill_shard(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(sink), _ptr(out), _ptr(lse), int(shard_tokens), int(halo),
+        int(pos0), int(hq), int(hkv), int(dqk), int(dv), int(rope_dim), float(rope_base),
+        int(window), float(softmax_scale), _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def hattn_prefill_cached(q, k_new, v_new, k_cache, v_cache, cu_seqlens, prefix_lens, sink, out,
@@ -257,6 +268,30 @@ def prefill(q, k, v, sink, cu_seqlens, *, max_seqlen: int, window: int, rope_bas
     _check(hattn_prefill(q, k, v, sink, out, lse, cu_seqlens.numel() - 1, cu_seqlens, total,
                          max_seqlen, hq, hkv, dqk, dv, ROPE_DIM, rope_base, window, softmax_scale,
                          workspace, workspace.numel()), "hattn_prefill")
+    return out, lse
+
+
+def prefill_shard(q, k, v, sink, *, pos0: int, halo: int, window: int, rope_base: float,
+                  softmax_scale: float | None = None, out=None, lse=None, workspace=None,
+                  with_lse: bool = True):
+    """One context-parallel shard of a layer's prefill: q [L, hq, dqk] holds the
+    shard's queries (positions pos0 .. pos0 + L - 1), k / v [halo + L, hkv, d]
+    the halo's keys and values followed by the shard's own.  Returns (out, lse)."""
+    L, hq, dqk = q.shape
+    hkv, dv = k.shape[1], v.shape[2]
+    assert k.shape[0] == halo + L and v.shape[0] == halo + L
+    if softmax_scale is None:
+        softmax_scale = dqk ** -0.5
+    if out is None:
+        out = torch.empty((L, hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((L, hq), dtype=torch.float32, device=q.device)
+    need = hattn_prefill_workspace_size(halo + L, hkv, dqk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(hattn_prefill_shard(q, k, v, sink, out, lse, L, halo, pos0, hq, hkv, dqk, dv, ROPE_DIM,
+                               rope_base, window, softmax_scale, workspace, workspace.numel()),
+           "hattn_prefill_shard")
     return out, lse
 
 

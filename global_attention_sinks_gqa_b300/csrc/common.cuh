@@ -54,6 +54,22 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may start while the kernel before it on the
+// stream is still running; grid_dep_wait() returns once that kernel has
+// completed and its writes are visible (a no-op for a normal launch), so a
+// kernel touches no global memory another kernel may write before it.
+// grid_dep_launch() lets the next such kernel start early (its own
+// grid_dep_wait() still orders it after this one's completion).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -1189,11 +1189,9 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
     bars->abort = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
-    // the first two items' Q/K go out before the rest of the setup
     tma_prefetch_map(&mapQ);
     tma_prefetch_map(&mapK);
     tma_prefetch_map(&mapV);
-    for (int i = 0; i < 2 && i < nmine; ++i) load_qk(i);
   }
   if (warp == 2) {
     __syncwarp();
@@ -1212,10 +1210,18 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Everything above touches only this CTA's shared memory and TMEM, so under
+  // a programmatic launch it overlaps the previous kernel's tail; from here on
+  // the previous kernel's writes (the queries, new tokens, the caches) are
+  // visible.  The next kernel may then start its own setup.
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 2) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // the first two items' Q/K go out first
+      for (int i = 0; i < 2 && i < nmine; ++i) load_qk(i);
       int qk_uses[2] = {nmine > 0 ? 1 : 0, nmine > 1 ? 1 : 0}, v_uses[2] = {0, 0};
       // Q/K of item iq once its buffer's Q/K are free; V of item iv once that
       // item's K has landed (the softmax needs it first) and its buffer's V
@@ -1580,8 +1586,19 @@ cudaError_t launch_ring_tc(const DecodeArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const long items = long(a.B) * a.hkv;
   const int grid = int(items < num_sms() ? items : num_sms());
-  decode_ring_tc_kernel<G><<<unsigned(grid), kRingTcThreads, kRingTcSmem, s>>>(mq, mk, mv, a);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs' setup overlaps the tail of the
+  // kernel before them; every global read waits for it (grid_dep_wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kRingTcThreads);
+  cfg.dynamicSmemBytes = kRingTcSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_ring_tc_kernel<G>, mq, mk, mv, a);
 }
 
 cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {

@@ -166,10 +166,16 @@ const char* hattn_status_string(hattn_status_t s) {
   return "HATTN_ERR_UNKNOWN";
 }
 
+namespace {
+// Bytes of the rotated key dims 0..63 in a prefill workspace.
+size_t prefill_rot_bytes(long total_tokens, int hkv) {
+  return (size_t(total_tokens) * size_t(hkv) * kRopeDim * 2 + 255) / 256 * 256;
+}
+}  // namespace
+
 size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk) {
   if (total_tokens <= 0 || hkv <= 0 || dqk <= 0) return 0;
-  const size_t bytes = size_t(total_tokens) * size_t(hkv) * size_t(dqk) * 2;
-  return (bytes + 255) / 256 * 256 + 256;  // rotated keys, then the work counter
+  return prefill_rot_bytes(total_tokens, hkv) + 256;  // rotated dims, then the work counter
 }
 
 hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const float* sink,
@@ -198,11 +204,9 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
   PrefillArgs a;
   a.q = q;
   a.k_rot = workspace;
-  {
-    const size_t kb = size_t(total_tokens) * size_t(hkv) * size_t(dqk) * 2;
-    a.unit_ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
-                                                 (kb + 255) / 256 * 256);
-  }
+  a.k_raw = k;
+  a.unit_ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
+                                               prefill_rot_bytes(total_tokens, hkv));
   a.v = v;
   a.sink = sink;
   a.out = out;
@@ -221,6 +225,66 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
                               a.unit_ctr) != cudaSuccess)
     return HATTN_ERR_CUDA;
   if (max_seqlen == 0) return HATTN_OK;
+  if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;
+  return HATTN_OK;
+}
+
+hattn_status_t hattn_prefill_shard(const void* q, const void* k, const void* v,
+                                   const float* sink, void* out, float* lse, long shard_tokens,
+                                   int halo, long pos0, int hq, int hkv, int dqk, int dv,
+                                   int rope_dim, float rope_base, int window, float softmax_scale,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  hattn_status_t st = check_heads(hq, hkv, dqk, dv, rope_dim);
+  if (st != HATTN_OK) return st;
+  if (shard_tokens < 0 || halo < 0 || pos0 < halo || window < 0) return HATTN_ERR_INVALID_ARG;
+  // positions are int on the device
+  if (pos0 + shard_tokens > 2147483647L) return HATTN_ERR_INVALID_ARG;
+  // the halo must hold every key a query of the shard can see: the last
+  // window - 1 positions before the shard (a window layer), or all of them
+  if (window > 0 ? long(halo) < (long(window) - 1 < pos0 ? long(window) - 1 : pos0)
+                 : long(halo) != pos0)
+    return HATTN_ERR_INVALID_ARG;
+  if (!finite_positive(rope_base) || !finite_positive(softmax_scale)) return HATTN_ERR_INVALID_ARG;
+  if (shard_tokens == 0) return HATTN_OK;
+  const long total_k = long(halo) + shard_tokens;
+  if (!q || !k || !v || !sink || !out) return HATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(workspace))
+    return HATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(sink) & 3u || reinterpret_cast<uintptr_t>(lse) & 3u)
+    return HATTN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < hattn_prefill_workspace_size(total_k, hkv, dqk))
+    return HATTN_ERR_WORKSPACE;
+  DeviceCtl ctl;
+  if (!launch_ctl(&ctl)) return HATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrefillArgs a;
+  a.q = q;
+  a.k_rot = workspace;
+  a.k_raw = k;
+  a.unit_ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
+                                               prefill_rot_bytes(total_k, hkv));
+  a.v = v;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.cu_seqlens = nullptr;  // one sequence: the shard
+  a.batch = 1;
+  a.total = shard_tokens;
+  a.max_seqlen = int(shard_tokens);
+  a.hq = hq;
+  a.hkv = hkv;
+  // a window covering every key the shard holds is global
+  a.window = long(window) >= total_k ? 0 : window;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  make_rope_freqs(rope_base, &a.freqs);
+  a.ctl = ctl;
+  a.total_k = total_k;
+  a.lead = halo;
+  a.rope_off = int(pos0 - halo);
+  if (launch_rope_keys_packed(k, workspace, nullptr, 1, total_k, hkv, a.freqs, ctl, s, a.unit_ctr,
+                              a.rope_off) != cudaSuccess)
+    return HATTN_ERR_CUDA;
   if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;
   return HATTN_OK;
 }
@@ -339,6 +403,7 @@ hattn_status_t hattn_prefill_cached(const void* q, const void* k_new, const void
   PrefillArgs a;
   a.q = q;
   a.k_rot = k_cache;
+  a.k_raw = k_cache;
   a.unit_ctr = static_cast<unsigned int*>(workspace);
   a.v = v_cache;
   a.sink = sink;

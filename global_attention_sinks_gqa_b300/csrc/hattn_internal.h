@@ -39,10 +39,13 @@ bool make_map(CUtensorMap* m, const void* base, long rows, int heads, int dim, i
 int num_sms();
 
 // ---- rope / append (rope_append.cu) --------------------------------------
-// Also zeroes *unit_ctr (the prefill kernel's work counter) when non-null.
+// The rotated dims 0..63 of every key row, as fp16, into k_rot [total, hkv,
+// 64].  Also zeroes *unit_ctr (the prefill kernel's work counter) when non-null.
+// cu_seqlens == nullptr: one sequence whose row n sits at position n + pos_off.
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
-                                    cudaStream_t s, unsigned int* unit_ctr = nullptr);
+                                    cudaStream_t s, unsigned int* unit_ctr = nullptr,
+                                    int pos_off = 0);
 // A paged cache: position p of sequence b lives in page
 // table[b * stride + p / page], slot p % page; pages are [num_pages, hkv,
 // page, d].  table == nullptr: a contiguous cache [B, hkv, cap, d].
@@ -69,7 +72,8 @@ cudaError_t launch_kv_append_packed(const void* k_new, const void* v_new, const 
 // ---- prefill (prefill_tc.cu) ------------------------------------------------
 struct PrefillArgs {
   const void* q;
-  const void* k_rot;
+  const void* k_rot;   // rotated dims 0..63: [total, hkv, 64] fp16, or the K cache
+  const void* k_raw;   // dims 64..191: the un-rotated keys [total, hkv, 192], or the K cache
   unsigned int* unit_ctr;  // work counter (zeroed by the key rotation pass)
   const void* v;
   const float* sink;
@@ -89,6 +93,13 @@ struct PrefillArgs {
   // caches [batch, hkv, cap, d] (k_rot, v point at them), slot = position.
   const int* prefix = nullptr;
   int cap = 0;
+  // One shard of a sequence (hattn_prefill_shard; batch 1, cu_seqlens null):
+  // the packed K/V hold total_k = lead + total rows, the `lead` rows of keys
+  // before the shard's first query followed by the shard's own; RoPE
+  // positions are the rows' indices plus rope_off.
+  long total_k = 0;  // 0: total
+  int lead = 0;
+  int rope_off = 0;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 

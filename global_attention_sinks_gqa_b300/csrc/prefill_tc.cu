@@ -5,8 +5,9 @@
 // on the MiMo series, MiMo-V2-Flash "local window" and "Learnable Attention
 // Sink"): out = softmax over {visible keys, sink} of scale * q'.k' applied to
 // the values (the sink has no value), lse = log of that denominator.  q' and
-// k' carry RoPE on dims 0..63.  Keys arrive already rotated (the rotation of
-// K is a separate pass); Q is rotated here, in shared memory, once per tile.
+// k' carry RoPE on dims 0..63.  The keys' rotated dims 0..63 arrive from a
+// separate pass (or a cache) and their dims 64..191 straight from k, through
+// a second tensor map; Q is rotated here, in shared memory, once per tile.
 // The 64 rotated dims are fp16 operands (11 significant bits) and the other
 // 128 dims bf16, so QK^T runs as 4 fp16 k-steps plus 8 bf16 k-steps into one
 // fp32 accumulator.
@@ -201,7 +202,7 @@ __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, const int
   if (!seq_slice(cu, ui.b, a.total, a.max_seqlen, a.ctl, report, ui.tok0, ui.L)) return false;
   ui.t0 = qt * UT;
   if (ui.t0 >= ui.L) return false;
-  ui.P = a.prefix != nullptr ? __ldg(a.prefix + ui.b) : 0;
+  ui.P = a.prefix != nullptr ? __ldg(a.prefix + ui.b) : a.lead;
   if (a.prefix != nullptr && (ui.P < 0 || long(ui.P) + ui.L > a.cap)) {
     if (report) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
     return false;
@@ -414,7 +415,9 @@ __device__ __forceinline__ void softmax_one(uint32_t t_s, float scale_log2, int 
 
 template <int G, int BN, bool WIN, bool ONE>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+    prefill_kernel(const __grid_constant__ CUtensorMap mapQ,
+                   const __grid_constant__ CUtensorMap mapK0,
+                   const __grid_constant__ CUtensorMap mapK12,
                    const __grid_constant__ CUtensorMap mapV, const PrefillArgs a) {
   using C = Cfg<G, BN, ONE>;
   constexpr int TQ = C::TQ;
@@ -454,16 +457,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&mapQ);
-    tma_prefetch_map(&mapK);
+    tma_prefetch_map(&mapK0);
+    tma_prefetch_map(&mapK12);
     tma_prefetch_map(&mapV);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
-  const bool cu_cached = a.batch + 1 <= kCuCache;
-  if (cu_cached)
+  // no offsets (one shard of a sequence): the single sequence holds every row
+  const bool cu_cached = a.batch + 1 <= kCuCache || a.cu_seqlens == nullptr;
+  if (a.cu_seqlens == nullptr) {
+    if (threadIdx.x == 0) {
+      bars->cu[0] = 0;
+      bars->cu[1] = int(a.total);
+    }
+  } else if (cu_cached) {
     for (int i = threadIdx.x; i <= a.batch; i += kThreads) bars->cu[i] = __ldg(a.cu_seqlens + i);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -502,6 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kv_c2 = [&](const UnitInfo& ui, int kpos) {
         return a.prefix != nullptr ? ui.b * a.hkv + ui.g : ui.tok0 + kpos;
       };
+      // box i of a key block: dims 64 i .. 64 i + 63, the rotated ones (i = 0)
+      // through mapK0, the others through mapK12
+      auto kmap = [&](int i) { return i == 0 ? &mapK0 : &mapK12; };
       auto load_box = [&](const CUtensorMap* map, int dim0, int g, int row) -> bool {
         const uint32_t slot = pos % NSLOT;
         const uint32_t ph = (pos / NSLOT) & 1u;
@@ -536,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K_0, V_0.
         if constexpr (!ONE)
           for (int i = 0; i < 3 && ok; ++i)
-            ok = load_box(&mapK, 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+            ok = load_box(kmap(i), 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -554,14 +568,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (ONE)
           for (int i = 0; i < 3 && ok; ++i)
-            ok = load_box(&mapK, 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+            ok = load_box(kmap(i), 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
         for (int j = 0; j < ui.nblk && ok; ++j) {
           const int vpos = k0pos + j * BN;
           for (int i = 0; i < 2 && ok; ++i)
             ok = load_box(&mapV, 64 * i, kv_c1(ui, vpos), kv_c2(ui, vpos));
           if (j + 1 < ui.nblk)
             for (int i = 0; i < 3 && ok; ++i)
-              ok = load_box(&mapK, 64 * i, kv_c1(ui, vpos + BN), kv_c2(ui, vpos + BN));
+              ok = load_box(kmap(i), 64 * i, kv_c1(ui, vpos + BN), kv_c2(ui, vpos + BN));
         }
       }
       // never leave with copies in flight into this CTA's shared memory
@@ -818,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 cs_own[32 / G];
 #pragma unroll
         for (int k2 = 0; k2 < 32 / G; ++k2)
-          cs_own[k2] = rope_cos_sin(qpos, a.freqs.hi[hl + G * k2], a.freqs.lo[hl + G * k2]);
+          cs_own[k2] = rope_cos_sin(qpos + a.rope_off, a.freqs.hi[hl + G * k2],
+                                    a.freqs.lo[hl + G * k2]);
         uint8_t* qrow = smem + C::kOffQ + t * C::kQBytes + r * 128;
         uint4 ch[8];
 #pragma unroll
@@ -904,13 +919,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int G, int BN, bool WIN, bool ONE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   using C = Cfg<G, BN, ONE>;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk0, mk12, mv;
   const bool cached = a.prefix != nullptr;
+  // packed: rotated dims [total_k, hkv, 64] and raw keys [total_k, hkv, 192];
+  // cached: both from the cache [batch * hkv, cap, 192]
+  const long kr = a.total_k > 0 ? a.total_k : a.total;
   if (!make_map(&mq, a.q, a.total, a.hq, kDqk, G, C::TQ) ||
-      !(cached ? make_map(&mk, a.k_rot, long(a.batch) * a.hkv, a.cap, kDqk, BN, 1)
-               : make_map(&mk, a.k_rot, a.total, a.hkv, kDqk, 1, BN)) ||
+      !(cached ? make_map(&mk0, a.k_rot, long(a.batch) * a.hkv, a.cap, kDqk, BN, 1)
+               : make_map(&mk0, a.k_rot, kr, a.hkv, kRopeDim, 1, BN)) ||
+      !(cached ? make_map(&mk12, a.k_raw, long(a.batch) * a.hkv, a.cap, kDqk, BN, 1)
+               : make_map(&mk12, a.k_raw, kr, a.hkv, kDqk, 1, BN)) ||
       !(cached ? make_map(&mv, a.v, long(a.batch) * a.hkv, a.cap, kDv, BN, 1)
-               : make_map(&mv, a.v, a.total, a.hkv, kDv, 1, BN)))
+               : make_map(&mv, a.v, kr, a.hkv, kDv, 1, BN)))
     return cudaErrorInvalidValue;
   auto kern = prefill_kernel<G, BN, WIN, ONE>;
   static bool attr_set = false;
@@ -929,7 +949,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   const long nunits = nut * a.batch * a.hkv;
   if (nunits == 0) return cudaSuccess;
   const int grid = int(nunits < num_sms() ? nunits : num_sms());
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, a);
+  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk0, mk12, mv, a);
   return cudaGetLastError();
 }
 

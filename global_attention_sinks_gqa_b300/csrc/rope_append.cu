@@ -13,10 +13,10 @@
 // so unlike the untouched dims they are no longer exact bf16 numbers).  A
 // rotated value beyond the fp16 range is recorded as HATTN_ERR_INVALID_ARG.
 //
-// Both kernels give one warp one 192-element key row: lane l < 24 holds the
-// 16-byte chunk of dims 8l..8l+7, so the rotated pair (i, i + 32) of a lane
-// l < 4 sits in lane l + 4 and one shuffle brings the partner over.  Loads
-// and stores are 128-bit and coalesced along the row.
+// The append kernels give one warp one 192-element key row: lane l < 24 holds
+// the 16-byte chunk of dims 8l..8l+7, so the rotated pair (i, i + 32) of a
+// lane l < 4 sits in lane l + 4 and one shuffle brings the partner over.
+// Loads and stores are 128-bit and coalesced along the row.
 #include "common.cuh"
 
 namespace hattn {
@@ -71,56 +71,59 @@ __device__ __forceinline__ bool rope_key_row(const uint4* src, uint4* dst, int p
 constexpr int kRowsPerBlock = 8;  // one warp per row
 
 // Rotated-key pre-pass of prefill: one warp per token, all hkv heads of it.
-// The token's 32 (cos, sin) pairs are computed once (lane i: frequency i) and
-// shared through shared memory by every head; the warp then walks the
-// token's hkv x 24 16-byte chunks with coalesced 128-bit loads and stores.
-// A chunk of dims 0..63 loads its partner chunk (i <-> i + 32) as well.
+// Only the rotated dims 0..63 of each key row are read and written (as fp16,
+// into k_rot [total, hkv, 64]); the attention kernel reads dims 64..191
+// straight from k.  The token's 32 (cos, sin) pairs are computed once (lane i:
+// frequency i) and shared through shared memory by every head.  A task is one
+// head's pair of 16-byte chunks (c, c + 4), c < 4 -- the dims i and i + 32 a
+// rotation mixes -- so a warp covers 8 heads per pass with 64-byte pieces of
+// each 384-byte source row and whole 128-byte destination rows.
 constexpr int kTokWarps = 8;
 
 __global__ void __launch_bounds__(256) rope_keys_packed_kernel(
     const uint4* __restrict__ k, uint4* __restrict__ k_rot, const int* __restrict__ cu_seqlens,
     int batch, long total, int hkv, const RopeFreqs f, const DeviceCtl ctl,
-    unsigned int* __restrict__ unit_ctr) {
+    unsigned int* __restrict__ unit_ctr, int pos_off) {
   __shared__ float2 cs_tab[kTokWarps][32];
   if (unit_ctr != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *unit_ctr = 0u;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const long nchunks = long(hkv) * 24;
+  const int ntask = hkv * 4;
   bool overflow = false;
   for (long n = long(blockIdx.x) * kTokWarps + w; n < total; n += long(gridDim.x) * kTokWarps) {
-    // sequence holding packed token n: largest b with cu[b] <= n
-    int lo = 0, hi = batch;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(cu_seqlens + mid) <= n) lo = mid; else hi = mid - 1;
+    int pos = int(n) + pos_off;
+    if (cu_seqlens != nullptr) {
+      // sequence holding packed token n: largest b with cu[b] <= n
+      int lo = 0, hi = batch;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu_seqlens + mid) <= n) lo = mid; else hi = mid - 1;
+      }
+      pos = int(n - __ldg(cu_seqlens + lo));
     }
-    const int pos = int(n - __ldg(cu_seqlens + lo));
     __syncwarp();
     cs_tab[w][lane] = rope_cos_sin(pos, f.hi[lane], f.lo[lane]);
     __syncwarp();
-    const uint4* src = k + n * nchunks;
-    uint4* dst = k_rot + n * nchunks;
-    for (long q = lane; q < nchunks; q += 32) {
-      const int c = int(q % 24);
-      uint4 x = __ldg(src + q);
-      if (c < 8) {
-        const bool first = c < 4;  // dims i (first half) vs i + 32 (second half)
-        const uint4 pr = __ldg(src + (first ? q + 4 : q - 4));
-        const int i0 = 8 * (c & 3);
-        uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-        const uint32_t ps[4] = {pr.x, pr.y, pr.z, pr.w};
+    for (int task = lane; task < ntask; task += 32) {
+      const int h = task >> 2, c = task & 3;
+      const uint4* src = k + (n * hkv + h) * 24;
+      uint4* dst = k_rot + (n * hkv + h) * 8;
+      const uint4 x = __ldg(src + c), y = __ldg(src + c + 4);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+      uint32_t a[4], b[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 a = unpack_bf16x2(xs[e]);
-          const float2 b = unpack_bf16x2(ps[e]);
-          const float2 cs0 = cs_tab[w][i0 + 2 * e], cs1 = cs_tab[w][i0 + 2 * e + 1];
-          const float y0 = first ? a.x * cs0.x - b.x * cs0.y : a.x * cs0.x + b.x * cs0.y;
-          const float y1 = first ? a.y * cs1.x - b.y * cs1.y : a.y * cs1.x + b.y * cs1.y;
-          if (fabsf(y0) > kF16Max || fabsf(y1) > kF16Max) overflow = true;
-          xs[e] = pack_f16x2(y0, y1);
-        }
-        x = make_uint4(xs[0], xs[1], xs[2], xs[3]);
+      for (int e = 0; e < 4; ++e) {
+        const int i = 8 * c + 2 * e;  // dims (i, i+1) pair with (i+32, i+33)
+        const float2 xv = unpack_bf16x2(xs[e]), yv = unpack_bf16x2(ys[e]);
+        const float2 cs0 = cs_tab[w][i], cs1 = cs_tab[w][i + 1];
+        const float a0 = xv.x * cs0.x - yv.x * cs0.y, a1 = xv.y * cs1.x - yv.y * cs1.y;
+        const float b0 = yv.x * cs0.x + xv.x * cs0.y, b1 = yv.y * cs1.x + xv.y * cs1.y;
+        if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
+          overflow = true;
+        a[e] = pack_f16x2(a0, a1);
+        b[e] = pack_f16x2(b0, b1);
       }
-      dst[q] = x;
+      dst[c] = make_uint4(a[0], a[1], a[2], a[3]);
+      dst[c + 4] = make_uint4(b[0], b[1], b[2], b[3]);
     }
   }
   if (overflow) record_status(ctl, HATTN_ERR_INVALID_ARG);
@@ -224,14 +227,14 @@ cudaError_t launch_kv_append_packed(const void* k_new, const void* v_new, const 
 
 cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_seqlens, int batch,
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
-                                    cudaStream_t s, unsigned int* unit_ctr) {
+                                    cudaStream_t s, unsigned int* unit_ctr, int pos_off) {
   if (total == 0) return cudaSuccess;
   long blocks = (total + kTokWarps - 1) / kTokWarps;
   const long cap_blocks = long(num_sms()) * 8;  // grid-stride beyond 8 blocks per SM
   if (blocks > cap_blocks) blocks = cap_blocks;
   rope_keys_packed_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
       static_cast<const uint4*>(k), static_cast<uint4*>(k_rot), cu_seqlens, batch, total, hkv, f,
-      ctl, unit_ctr);
+      ctl, unit_ctr, pos_off);
   return cudaGetLastError();
 }
 

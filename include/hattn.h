@@ -74,10 +74,10 @@ int hattn_version(void);
 const char* hattn_status_string(hattn_status_t status);
 
 /*
- * Bytes of workspace hattn_prefill() needs: the rotated keys,
- * total_tokens * hkv * dqk 16-bit values, rounded up to 256 bytes, then 256
+ * Bytes of workspace hattn_prefill() needs: the keys' rotated dims 0..63,
+ * total_tokens * hkv * 64 fp16 values, rounded up to 256 bytes, then 256
  * bytes for the attention kernel's work counter (both rewritten by every
- * call: a workspace serves one call at a time).
+ * call: a workspace serves one call at a time).  dqk must be 192.
  */
 size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk);
 
@@ -106,8 +106,9 @@ size_t hattn_prefill_workspace_size(long total_tokens, int hkv, int dqk);
  *   rope_base  RoPE base (1e4 for SWA layers, 5e6 for GA layers)
  *   softmax_scale  logit scale (1/sqrt(192) for this model)
  *   workspace  DEVICE scratch of >= hattn_prefill_workspace_size() bytes,
- *              overwritten with the rotated keys (dims 0..63 fp16, 64..191
- *              bf16); out and lse must not overlap q, k, v or it.
+ *              overwritten with the keys' rotated dims 0..63 as fp16
+ *              [total_tokens, hkv, 64] (dims 64..191 are read from k);
+ *              out and lse must not overlap q, k, v or it.
  * Queries and keys are rotated before the tensor-core products; the rotated
  * dims are carried as fp16 (see hattn_rope_kv_append), so |RoPE(x)| must stay
  * below 65504 on dims 0..63 (recorded as HATTN_ERR_INVALID_ARG otherwise).
@@ -117,6 +118,39 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
                              long total_tokens, int max_seqlen, int hq, int hkv, int dqk, int dv,
                              int rope_dim, float rope_base, int window, float softmax_scale,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One shard of a layer's prefill under context parallelism: a sequence is cut
+ * into consecutive shards, one per GPU, and shard r holds its tokens
+ * [pos0, pos0 + shard_tokens).  A query at position p of a window layer sees
+ * keys p - window + 1 .. p, so besides its own keys a shard needs only the
+ * last min(window - 1, pos0) keys before it -- the halo -- which an exchange
+ * step brings from the GPUs that hold them (plmsmile notes on the MiMo
+ * series, MiMo-V2.6, "DFlash and long-context system optimisation", training
+ * memory: SWA context parallelism exchanges only the window-reachable KV).
+ * A global layer (window 0) needs the whole history as its halo.  Same
+ * results as rows [pos0, pos0 + shard_tokens) of hattn_prefill() over the
+ * whole sequence.
+ *
+ *   q      bf16 [shard_tokens, hq, dqk]   the shard's queries, un-rotated
+ *   k      bf16 [halo + shard_tokens, hkv, dqk]: the halo's keys (positions
+ *          pos0 - halo .. pos0 - 1) followed by the shard's own, un-rotated
+ *   v      bf16 [halo + shard_tokens, hkv, dv], the same rows
+ *   out    bf16 [shard_tokens, hq, dv], lse fp32 [shard_tokens, hq] (or NULL)
+ *   halo   rows of k and v before the shard's own: at least
+ *          min(window - 1, pos0) for window > 0, exactly pos0 for window = 0,
+ *          and at most pos0 (else HATTN_ERR_INVALID_ARG)
+ *   pos0   absolute position of the shard's first token (RoPE positions are
+ *          absolute: the halo's keys rotate at pos0 - halo ..)
+ *   workspace  DEVICE scratch of >= hattn_prefill_workspace_size(halo +
+ *          shard_tokens, hkv, dqk) bytes
+ *   other arguments as for hattn_prefill().
+ */
+hattn_status_t hattn_prefill_shard(const void* q, const void* k, const void* v,
+                                   const float* sink, void* out, float* lse, long shard_tokens,
+                                   int halo, long pos0, int hq, int hkv, int dqk, int dv,
+                                   int rope_dim, float rope_base, int window, float softmax_scale,
+                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of workspace hattn_prefill_backward() needs: the rotated dims 0..63 of

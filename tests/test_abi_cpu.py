@@ -42,9 +42,10 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # rotated keys rounded to 256 bytes, then 256 bytes of work counter
-    assert ha.hattn_prefill_workspace_size(32768, 8, 192) == 32768 * 8 * 192 * 2 + 256
-    assert ha.hattn_prefill_workspace_size(3, 1, 192) == 1280 + 256  # 1152 rounded to 256
+    # the keys' rotated dims 0..63 (fp16) rounded to 256 bytes, then 256 bytes
+    # of work counter
+    assert ha.hattn_prefill_workspace_size(32768, 8, 192) == 32768 * 8 * 64 * 2 + 256
+    assert ha.hattn_prefill_workspace_size(3, 1, 192) == 512 + 256  # 384 rounded to 256
     # a ring window fits one chunk: no workspace
     assert ha.hattn_decode_workspace_size(64, 4, 64, 8, 128, 65536, 128, 131, 1) == 0
     # partial O and lse (each rounded to 256 bytes), then 256 bytes of work counter
@@ -203,6 +204,31 @@ def _decode_paged(**kw):
 ])
 def test_decode_paged_rejects_bad_arguments(lib, kw, code):
     assert _decode_paged(**kw) == code
+
+
+def _shard(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, sink=FAKE, out=FAKE, lse=FAKE, shard_tokens=1000,
+                halo=127, pos0=4000, hq=64, hkv=8, dqk=192, dv=128, rope_dim=64, rope_base=1e4,
+                window=128, softmax_scale=0.07, workspace=FAKE, workspace_bytes=1 << 30,
+                stream=0)
+    args.update(kw)
+    return ha.hattn_prefill_shard(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(halo=126), ha.HATTN_ERR_INVALID_ARG),               # the window needs 127 rows
+    (dict(halo=30, pos0=20), ha.HATTN_ERR_INVALID_ARG),       # more rows than positions
+    (dict(halo=20, pos0=30), ha.HATTN_ERR_INVALID_ARG),       # needs min(127, 30) = 30
+    (dict(window=0, halo=127), ha.HATTN_ERR_INVALID_ARG),     # global: the whole history
+    (dict(pos0=2**31 - 500), ha.HATTN_ERR_INVALID_ARG),       # positions past INT_MAX
+    (dict(shard_tokens=-1), ha.HATTN_ERR_INVALID_ARG),
+    (dict(dqk=128), ha.HATTN_ERR_UNSUPPORTED),
+    (dict(workspace_bytes=1000), ha.HATTN_ERR_WORKSPACE),
+    (dict(k=FAKE + 8), ha.HATTN_ERR_INVALID_ARG),
+    (dict(shard_tokens=0), ha.HATTN_OK),                      # nothing to do
+])
+def test_prefill_shard_rejects_bad_arguments(lib, kw, code):
+    assert _shard(**kw) == code
 
 
 def test_oracle_is_not_reachable_from_the_product():
