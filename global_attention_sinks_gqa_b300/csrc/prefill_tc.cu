@@ -123,6 +123,13 @@ struct Cfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= (ONE ? 256 : 128), "BN");
   static_assert(kSlot % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
   static_assert(NSLOT >= (ONE ? 5 : 8), "ring must hold a K and a V block (and room to prefetch)");
+  // Several key blocks per unit: the slots form KST stages of one K block
+  // (3 boxes each) and one stage of one V block (2 boxes, after them), each
+  // stage on its own full / empty barrier pair (kv_full[0..KST-1] for K,
+  // kv_full[KST] for V).  K_{j+1} can then load as soon as K_{j+1-KST} is
+  // released, a whole key block ahead of its S product.
+  static constexpr int KST = (NSLOT - 2) / 3;
+  static_assert(ONE || KST >= 2, "two K stages");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
 
@@ -525,6 +532,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pos;
         return true;
       };
+      // several key blocks per unit: whole K / V blocks into their stages
+      uint32_t kq = 0, vq = 0;  // K and V blocks loaded
+      auto load_k = [&](const UnitInfo& ui, int kpos) -> bool {
+        const uint32_t st = kq % C::KST, ph = (kq / C::KST) & 1u;
+        if (!mbar_wait(&bars->kv_empty[st], ph ^ 1u, a.ctl, abort)) return false;
+        mbar_arrive_expect_tx(&bars->kv_full[st], 3 * C::kSlot);
+        for (int i = 0; i < 3; ++i)
+          tma_load_3d(ring + (st * 3 + i) * C::kSlot, kmap(i), &bars->kv_full[st], 64 * i,
+                      kv_c1(ui, kpos), kv_c2(ui, kpos));
+        ++kq;
+        return true;
+      };
+      auto load_v = [&](const UnitInfo& ui, int vpos) -> bool {
+        if (!mbar_wait(&bars->kv_empty[C::KST], (vq & 1u) ^ 1u, a.ctl, abort)) return false;
+        mbar_arrive_expect_tx(&bars->kv_full[C::KST], 2 * C::kSlot);
+        for (int i = 0; i < 2; ++i)
+          tma_load_3d(ring + (C::KST * 3 + i) * C::kSlot, &mapV, &bars->kv_full[C::KST], 64 * i,
+                      kv_c1(ui, vpos), kv_c2(ui, vpos));
+        ++vq;
+        return true;
+      };
       uint32_t pn = 0;  // queue entries published
       while (ok) {
         // draw the next unit that holds a query, publish it (or the end)
@@ -543,14 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pn;
         if (u < 0) break;
         const int k0pos = ui.kstart;
-        // Several blocks: K_0 first (its slots free up while the previous
-        // unit finishes), then the two Q tiles, then V_0, K_1, V_1, ...  One
+        // Several blocks: K_0 first (its stage frees while the previous
+        // unit finishes), then the two Q tiles, then K_1, V_0, K_2, V_1, ...  One
         // block: the Q tiles first -- a tile's buffer frees with its S MMA of
         // the previous unit and its RoPE heads the tile's next chain -- then
         // K_0, V_0.
-        if constexpr (!ONE)
-          for (int i = 0; i < 3 && ok; ++i)
-            ok = load_box(kmap(i), 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+        if constexpr (!ONE) ok = load_k(ui, k0pos);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -566,24 +592,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ui.tok0 + ui.t0 + t * TQ);
           ++qf;
         }
-        if constexpr (ONE)
+        if constexpr (ONE) {
           for (int i = 0; i < 3 && ok; ++i)
             ok = load_box(kmap(i), 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
-        for (int j = 0; j < ui.nblk && ok; ++j) {
-          const int vpos = k0pos + j * BN;
           for (int i = 0; i < 2 && ok; ++i)
-            ok = load_box(&mapV, 64 * i, kv_c1(ui, vpos), kv_c2(ui, vpos));
-          if (j + 1 < ui.nblk)
-            for (int i = 0; i < 3 && ok; ++i)
-              ok = load_box(kmap(i), 64 * i, kv_c1(ui, vpos + BN), kv_c2(ui, vpos + BN));
+            ok = load_box(&mapV, 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+        } else {
+          // K_{j+1} (its stage frees when S of K_{j+1-KST} completes) before
+          // V_j (its stage frees when PV of V_{j-1} completes): the order in
+          // which the products release them
+          for (int j = 0; j < ui.nblk && ok; ++j) {
+            const int vpos = k0pos + j * BN;
+            if (j + 1 < ui.nblk) ok = load_k(ui, vpos + BN);
+            if (ok) ok = load_v(ui, vpos);
+          }
         }
       }
       // never leave with copies in flight into this CTA's shared memory
       if (qfills0) mbar_wait_drain(&bars->q_full[0], (qfills0 - 1) & 1u, a.ctl);
       if (qfills1) mbar_wait_drain(&bars->q_full[1], (qfills1 - 1) & 1u, a.ctl);
-      for (uint32_t sl = 0; sl < uint32_t(NSLOT); ++sl) {
-        const uint32_t fills = pos > sl ? (pos - sl + NSLOT - 1) / NSLOT : 0;
-        if (fills) mbar_wait_drain(&bars->kv_full[sl], (fills - 1) & 1u, a.ctl);
+      if constexpr (ONE) {
+        for (uint32_t sl = 0; sl < uint32_t(NSLOT); ++sl) {
+          const uint32_t fills = pos > sl ? (pos - sl + NSLOT - 1) / NSLOT : 0;
+          if (fills) mbar_wait_drain(&bars->kv_full[sl], (fills - 1) & 1u, a.ctl);
+        }
+      } else {
+        for (uint32_t st = 0; st < uint32_t(C::KST); ++st) {
+          const uint32_t fills = kq > st ? (kq - st + C::KST - 1) / C::KST : 0;
+          if (fills) mbar_wait_drain(&bars->kv_full[st], (fills - 1) & 1u, a.ctl);
+        }
+        if (vq) mbar_wait_drain(&bars->kv_full[C::KST], (vq - 1) & 1u, a.ctl);
       }
     }
     } else if (warp == 1) {
@@ -690,15 +728,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++uc;
         }
       } else {
+      // K blocks in KST stages (positions kc), V blocks in one stage (vc):
+      // the stage of block c is kc % KST; K stage s holds slots 3s .. 3s + 2,
+      // the V stage slots 3 KST, 3 KST + 1
+      uint32_t kc = 0, vc = 0;
+      auto wait_k = [&]() -> uint32_t {  // slot position of the next K block
+        const uint32_t st = kc % C::KST;
+        if (!mbar_wait(&bars->kv_full[st], (kc / C::KST) & 1u, a.ctl, abort)) return ~0u;
+        ++kc;
+        return 3 * st;
+      };
+      constexpr uint32_t kVPos = 3 * C::KST;
       uint32_t rn = 0;
       while (ok) {
         const int u = read_unit(rn, false);
         if (u < 0) break;
         UnitInfo ui;
         unit_info<G, BN, WIN>(u, a, cu, nut, ui);
-        const uint32_t k0 = pos;
-        pos += 3;
-        if (!wait_slots(k0, 3)) break;
+        const uint32_t k0 = wait_k();
+        if (k0 == ~0u) break;
         for (int t = 0; t < 2 && ok; ++t) {
           if (!mbar_wait(&bars->q_ready[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
           tc_fence_after();
@@ -707,14 +755,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ui.nblk == 1) umma_commit(&bars->q_empty[t]);
         }
         if (!ok) break;
-        release_slots(k0, 3);
+        umma_commit(&bars->kv_empty[k0 / 3]);  // K_0's stage frees once both S are done
         for (int j = 0; j < ui.nblk && ok; ++j, ++blk) {
-          const uint32_t vp = pos;
-          pos += 2;
           const bool more = j + 1 < ui.nblk;
-          const uint32_t kn = pos;
-          if (more) pos += 3;
-          if (!wait_slots(vp, 2)) { ok = false; break; }
+          if (!mbar_wait(&bars->kv_full[C::KST], vc & 1u, a.ctl, abort)) { ok = false; break; }
+          ++vc;
+          uint32_t kn = 0;
           for (int t = 0; t < 2; ++t) {
             if (!mbar_wait(&bars->p_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
             if (j == 0 && uc > 0 &&
@@ -723,15 +769,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            issue_pv(t, vp, j > 0);
+            issue_pv(t, kVPos, j > 0);
             if (!more) umma_commit(&bars->pv_done[t]);  // the unit's O_t is complete
-            if (t == 1) release_slots(vp, 2);
+            if (t == 1) umma_commit(&bars->kv_empty[C::KST]);  // V_j's stage
             if (more) {
-              if (t == 0 && !wait_slots(kn, 3)) { ok = false; break; }
+              if (t == 0) {
+                kn = wait_k();
+                if (kn == ~0u) { ok = false; break; }
+              }
               issue_qk(t, kn);
               umma_commit(&bars->s_full[t]);
               if (j + 2 == ui.nblk) umma_commit(&bars->q_empty[t]);
-              if (t == 1) release_slots(kn, 3);
+              if (t == 1) umma_commit(&bars->kv_empty[kn / 3]);  // K_{j+1}'s stage
             }
           }
         }
