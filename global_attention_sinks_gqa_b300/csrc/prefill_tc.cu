@@ -22,9 +22,14 @@
 // the other's softmax runs.
 //
 // CTA roles (384 threads, persistent over units):
-//   warp 0      TMA producer: Q tiles (3 boxes of 64 dims each) and a ring of
-//               NSLOT slots, each one [BN keys][64 dims] box of K or V, filled
-//               in the order K_0, V_0, K_1, V_1, ... (128-byte swizzle).
+//   warp 0      TMA producer: Q tiles (3 boxes of 64 dims each) and the key
+//               blocks, in slots of one [BN keys][64 dims] box (128-byte
+//               swizzle): a K block is 3 consecutive slots, a V block 2.
+//               Several blocks per unit: K in KST stages, V in one, each
+//               stage on one full / empty barrier pair, loaded K_0, K_1, V_0,
+//               K_2, V_1, ...  One block per unit: one K and one V stage whose
+//               release (and that of the Q tiles) the producer reads from the
+//               phases of the S and PV completion barriers.
 //   warp 1      TMEM allocator and single-thread MMA issuer, per key block j:
 //                 O_A += P_A,j V_j ; S_A = Q_A K_{j+1}^T ;
 //                 O_B += P_B,j V_j ; S_B = Q_B K_{j+1}^T
@@ -509,7 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t pos = 0;            // ring positions filled so far
       uint32_t qfills0 = 0, qfills1 = 0;  // Q loads issued into the tile A / B buffer
       bool ok = true;
       // K / V box of key position kpos of unit ui: packed keys [total, hkv, d]
@@ -523,15 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // box i of a key block: dims 64 i .. 64 i + 63, the rotated ones (i = 0)
       // through mapK0, the others through mapK12
       auto kmap = [&](int i) { return i == 0 ? &mapK0 : &mapK12; };
-      auto load_box = [&](const CUtensorMap* map, int dim0, int g, int row) -> bool {
-        const uint32_t slot = pos % NSLOT;
-        const uint32_t ph = (pos / NSLOT) & 1u;
-        if (!mbar_wait(&bars->kv_empty[slot], ph ^ 1u, a.ctl, abort)) return false;
-        mbar_arrive_expect_tx(&bars->kv_full[slot], C::kSlot);
-        tma_load_3d(ring + slot * C::kSlot, map, &bars->kv_full[slot], dim0, g, row);
-        ++pos;
-        return true;
-      };
+      uint32_t un = 0;  // one-block units whose K and V were loaded
       // several key blocks per unit: whole K / V blocks into their stages
       uint32_t kq = 0, vq = 0;  // K and V blocks loaded
       auto load_k = [&](const UnitInfo& ui, int kpos) -> bool {
@@ -581,7 +577,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
           uint32_t& qf = t ? qfills1 : qfills0;
-          if (!mbar_wait(&bars->q_empty[t], (qf & 1u) ^ 1u, a.ctl, abort)) {
+          // one-block units: Q_t is free once the previous unit's S_t is
+          // done (the phase of s_full[t]; the next phase needs this load, so
+          // the parity cannot alias); several blocks: its own barrier
+          const bool qfree =
+              ONE ? (qf == 0 || mbar_wait(&bars->s_full[t], (qf - 1) & 1u, a.ctl, abort))
+                  : mbar_wait(&bars->q_empty[t], (qf & 1u) ^ 1u, a.ctl, abort);
+          if (!qfree) {
             ok = false;
             break;
           }
@@ -593,10 +595,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++qf;
         }
         if constexpr (ONE) {
-          for (int i = 0; i < 3 && ok; ++i)
-            ok = load_box(kmap(i), 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
-          for (int i = 0; i < 2 && ok; ++i)
-            ok = load_box(&mapV, 64 * i, kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+          // the unit's K block (slots 0-2) once the previous unit's S_B is
+          // done, its V block (slots 3-4) once its PV_B is: the phases of
+          // s_full[1] and pv_done[1] (products complete in issue order)
+          if (ok && un > 0)
+            ok = mbar_wait(&bars->s_full[1], (un - 1) & 1u, a.ctl, abort);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars->kv_full[0], 3 * C::kSlot);
+            for (int i = 0; i < 3; ++i)
+              tma_load_3d(ring + i * C::kSlot, kmap(i), &bars->kv_full[0], 64 * i,
+                          kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+          }
+          if (ok && un > 0)
+            ok = mbar_wait(&bars->pv_done[1], (un - 1) & 1u, a.ctl, abort);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars->kv_full[1], 2 * C::kSlot);
+            for (int i = 0; i < 2; ++i)
+              tma_load_3d(ring + (3 + i) * C::kSlot, &mapV, &bars->kv_full[1], 64 * i,
+                          kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+            ++un;
+          }
         } else {
           // K_{j+1} (its stage frees when S of K_{j+1-KST} completes) before
           // V_j (its stage frees when PV of V_{j-1} completes): the order in
@@ -612,9 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qfills0) mbar_wait_drain(&bars->q_full[0], (qfills0 - 1) & 1u, a.ctl);
       if (qfills1) mbar_wait_drain(&bars->q_full[1], (qfills1 - 1) & 1u, a.ctl);
       if constexpr (ONE) {
-        for (uint32_t sl = 0; sl < uint32_t(NSLOT); ++sl) {
-          const uint32_t fills = pos > sl ? (pos - sl + NSLOT - 1) / NSLOT : 0;
-          if (fills) mbar_wait_drain(&bars->kv_full[sl], (fills - 1) & 1u, a.ctl);
+        if (un) {
+          mbar_wait_drain(&bars->kv_full[0], (un - 1) & 1u, a.ctl);
+          mbar_wait_drain(&bars->kv_full[1], (un - 1) & 1u, a.ctl);
         }
       } else {
         for (uint32_t st = 0; st < uint32_t(C::KST); ++st) {
@@ -630,77 +648,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_rot = make_idesc_f16(128, BN, 0, 0);   // dims 0..63
       constexpr uint32_t idesc_s = make_idesc_bf16(128, BN, 0, 0);    // dims 64..191
       constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, 0, 1);
-      constexpr uint32_t idesc_o64 = make_idesc_bf16(128, 64, 0, 1);
       const uint32_t qbase = smem_u32(smem + C::kOffQ);
       const uint32_t rbase = smem_u32(ring);
-      uint32_t pos = 0;   // ring positions consumed (same sequence as the producer)
       uint32_t blk = 0;   // key blocks completed by both tiles so far
       uint32_t uc = 0;    // units started
       bool ok = true;
-      auto wait_slots = [&](uint32_t p0, int n) -> bool {
-        for (int i = 0; i < n; ++i) {
-          const uint32_t p = p0 + i;
-          if (!mbar_wait(&bars->kv_full[p % NSLOT], (p / NSLOT) & 1u, a.ctl, abort)) return false;
-        }
-        return true;
-      };
-      auto release_slots = [&](uint32_t p0, int n) {
-        for (int i = 0; i < n; ++i) umma_commit(&bars->kv_empty[(p0 + i) % NSLOT]);
-      };
       // Shared-memory descriptors are built once; a k-step or slot only adds
       // its byte offset / 16 to the start-address field (addresses stay below
       // 256 KB, so the 14-bit field never carries).
       const uint64_t qdesc0 = make_sdesc_sw128(qbase, 16, 1024);
       const uint64_t kdesc0 = make_sdesc_sw128(rbase, 16, 1024);
       const uint64_t vdesc0 = make_sdesc_sw128(rbase, C::kSlot, 1024);
-      auto issue_qk = [&](int t, uint32_t kpos) {
+      // a K block sits in 3 consecutive slots from kslot, a V block in 2 from
+      // vslot (dims 0..63 then 64..127: one N=128 MMA per k-step spans both)
+      auto issue_qk = [&](int t, uint32_t kslot) {
         const uint64_t qd = qdesc0 + uint64_t((t * C::kQBytes) >> 4);
-        const uint32_t ks0 = kpos % NSLOT;
-        const uint32_t ks1 = ks0 + 1 == uint32_t(NSLOT) ? 0u : ks0 + 1;
-        const uint32_t ks2 = ks1 + 1 == uint32_t(NSLOT) ? 0u : ks1 + 1;
-        const uint64_t kd[3] = {kdesc0 + uint64_t((ks0 * C::kSlot) >> 4),
-                                kdesc0 + uint64_t((ks1 * C::kSlot) >> 4),
-                                kdesc0 + uint64_t((ks2 * C::kSlot) >> 4)};
+        const uint64_t kd = kdesc0 + uint64_t((kslot * C::kSlot) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk)
           umma_ss(tmem + s_col<ONE>(t), qd + uint64_t(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4),
-                  kd[kk >> 2] + uint64_t(((kk & 3) * 32) >> 4), kk < 4 ? idesc_rot : idesc_s,
-                  kk > 0 ? 1u : 0u);
+                  kd + uint64_t(((kk >> 2) * C::kSlot + (kk & 3) * 32) >> 4),
+                  kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
       };
-      auto issue_pv = [&](int t, uint32_t vpos, bool acc) {
-        const uint32_t s0 = vpos % NSLOT;
-        const uint32_t s1 = s0 + 1 == uint32_t(NSLOT) ? 0u : s0 + 1;
-        const uint64_t vd0 = vdesc0 + uint64_t((s0 * C::kSlot) >> 4);
-        const uint64_t vd1 = vdesc0 + uint64_t((s1 * C::kSlot) >> 4);
+      auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+        const uint64_t vd = vdesc0 + uint64_t((vslot * C::kSlot) >> 4);
         const uint32_t p_tmem = tmem + s_col<ONE>(t);
-        if (s1 == s0 + 1) {  // the two 64-dim halves of V are adjacent: one N=128 MMA per k-step
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            umma_ts(tmem + o_col<ONE>(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o,
-                    (acc || kk > 0) ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            umma_ts(tmem + o_col<ONE>(t), p_tmem + kk * 8, vd0 + uint64_t((kk * 2048) >> 4), idesc_o64,
-                    (acc || kk > 0) ? 1u : 0u);
-            umma_ts(tmem + o_col<ONE>(t) + 64, p_tmem + kk * 8, vd1 + uint64_t((kk * 2048) >> 4),
-                    idesc_o64, (acc || kk > 0) ? 1u : 0u);
-          }
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts(tmem + o_col<ONE>(t), p_tmem + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_o,
+                  (acc || kk > 0) ? 1u : 0u);
       };
       if constexpr (ONE) {
         // one key block per unit: S_t = Q_t K^T once O_t (over S_t's upper
         // columns) has been read by the previous unit's epilogue, then
         // O_t = P_t V
+        // (the producer takes the release of Q_t, K and V from the phases of
+        // s_full[t], s_full[1] and pv_done[1]: no commits of their own)
         uint32_t rn = 0;
         while (ok) {
           const int u = read_unit(rn, false);
           if (u < 0) break;
-          UnitInfo ui;
-          unit_info<G, BN, WIN>(u, a, cu, nut, ui);
-          const uint32_t k0 = pos;
-          pos += 3;
-          if (!wait_slots(k0, 3)) break;
+          if (!mbar_wait(&bars->kv_full[0], uc & 1u, a.ctl, abort)) break;
           for (int t = 0; t < 2 && ok; ++t) {
             if (!mbar_wait(&bars->q_ready[t], uc & 1u, a.ctl, abort) ||
                 (uc > 0 && !mbar_wait(&bars->o_free[t], (uc - 1) & 1u, a.ctl, abort))) {
@@ -708,23 +696,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            issue_qk(t, k0);
+            issue_qk(t, 0);
             umma_commit(&bars->s_full[t]);
-            umma_commit(&bars->q_empty[t]);
           }
           if (!ok) break;
-          release_slots(k0, 3);
-          const uint32_t vp = pos;
-          pos += 2;
-          if (!wait_slots(vp, 2)) break;
+          if (!mbar_wait(&bars->kv_full[1], uc & 1u, a.ctl, abort)) break;
           for (int t = 0; t < 2 && ok; ++t) {
             if (!mbar_wait(&bars->p_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
             tc_fence_after();
-            issue_pv(t, vp, false);
+            issue_pv(t, 3, false);
             umma_commit(&bars->pv_done[t]);
           }
           if (!ok) break;
-          release_slots(vp, 2);
           ++uc;
         }
       } else {
