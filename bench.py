@@ -209,7 +209,8 @@ def step_config(world: int = 1):
             "ga_prefill": "seq 32768, 64q/4kv, global, rope 64 @5e6",
             "decode": "batch 64 x 4 verify tokens; 5 swa layers (8kv ring 131 each) + 1 ga "
                       "layer (4kv, L~U[8192,65536])",
-            "l2": "inputs larger than L2 (no flush needed)",
+            "l2": "inputs larger than L2 (no flush needed); parts' alone_ms: each part's "
+                  "calls repeated on their own, L2 flushed between repetitions",
             "parallelism": f"replicas x{world}"}
 
 
@@ -374,6 +375,33 @@ def run_cuda(args, rank, world):
     part_ms = {k: statistics.mean(e[k][0].elapsed_time(e[k][1]) for e in ev) for k in keys}
     wl.ha.check_device_status()
 
+    # Each part alone as well (its calls back to back, same inputs), outside
+    # the step: inside the step every part runs under the SM clock the
+    # power-capped global prefill leaves behind; alone, the short parts run
+    # at their own clock.  The step's numbers above stay the reported ones.
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # twice the L2
+
+    def alone(fn, reps):
+        fn()
+        ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(reps)]
+        for a0, a1 in ev_a:
+            flush.zero_()  # L2 flushed between repetitions, outside the timed calls
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a0.elapsed_time(a1) for a0, a1 in ev_a)
+
+    alone_ms = {
+        "p0": alone(lambda: wl.run_prefill(wl.layers[0], sptr), 20),
+        "d_swa": alone(lambda: [wl.run_decode(dd, sptr) for dd in wl.dec if dd["kind"] == "swa"],
+                       20),
+        "d_ga": alone(lambda: [wl.run_decode(dd, sptr) for dd in wl.dec if dd["kind"] == "ga"],
+                      10),
+    }
+    wl.ha.check_device_status()
+
     # ---- end to end: per step, inputs from pinned host memory, outputs back
     e2e = run_e2e(wl, args, stream, sptr)
 
@@ -390,6 +418,12 @@ def run_cuda(args, rank, world):
                                   roofline_frac=max(bound_f, bound_b) / t,
                                   bound="tensor" if bound_f > bound_b else "hbm",
                                   peak="hbm_gbs" if bound_b > bound_f else tf_name)
+        if f"p{i}" in alone_ms:
+            ta = alone_ms[f"p{i}"] / 1e3
+            parts[lay["name"]].update(alone_ms=ta * 1e3,
+                                      alone_roofline_frac=max(bound_f, bound_b) / ta)
+        tr, _ = recorded_traffic("prefill_" + lay["name"].split("_")[0] + "_32k")
+        parts[lay["name"]]["traffic"] = tr
     for kind in ("swa", "ga"):
         lays = [dd for dd in wl.dec if dd["kind"] == kind]
         t = part_ms[f"d_{kind}"] / 1e3 / len(lays)  # per layer
@@ -399,7 +433,9 @@ def run_cuda(args, rank, world):
             ms=t * 1e3, tflops=dd["flops"] / t / 1e12, gbs=byts / t / 1e9,
             roofline_frac=byts / (hbm * 1e9) / t, bound="hbm", peak="hbm_gbs",
             verify_tokens_per_s=wl.B * wl.T / t, layers=len(lays),
-            timing="per layer: one event pair around the layers' calls back to back")
+            timing="per layer: one event pair around the layers' calls back to back",
+            alone_ms=alone_ms[f"d_{kind}"] / len(lays),
+            alone_roofline_frac=byts / (hbm * 1e9) / (alone_ms[f"d_{kind}"] / len(lays) / 1e3))
     ga = wl.layers[1]
     ga_s = part_ms["p1"] / 1e3
     ga_tf, ga_tf_name = tensor_peak(ga_s, tf_burst, tf_sust)
@@ -521,10 +557,35 @@ def run_e2e(wl, args, stream, sptr):
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / n
+
+    # the same copies alone (no layer calls), for the floor they set
+    def copies():
+        with torch.cuda.stream(up):
+            for i in range(nparts):
+                for h, d in zip(host_in[i], dev_in[i]):
+                    d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(down):
+            for i in range(nparts):
+                for o, h in zip(part_outs[i], part_host[i]):
+                    h.copy_(o, non_blocking=True)
+
+    copies()
+    torch.cuda.synchronize()
+    start.record(stream)
+    up.wait_event(start)
+    down.wait_event(start)
+    for _ in range(n):
+        copies()
+    stream.wait_stream(up)
+    stream.wait_stream(down)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    copy_ms = start.elapsed_time(stop) / n
     return {"value": round(wl.flops() / (ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h),
-            "copies": "uploads and read-backs on two copy streams, overlapping the layers"}
+            "copies": "uploads and read-backs on two copy streams, overlapping the layers",
+            "copies_alone_ms": round(copy_ms, 3)}
 
 
 # --------------------------------------------------------------------- CPU oracle arm
