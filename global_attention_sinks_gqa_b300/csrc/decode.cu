@@ -1070,7 +1070,10 @@ static_assert(kRingTcH0 + kRingTcH1 == kRingTcMaxCap, "halves cover the ring");
 __host__ __device__ constexpr int ring_tc_rows(int cap) { return (cap + 15) & ~15; }
 
 struct RingTcBars {
-  uint64_t q_full[2], k_full[2], v_full[2], qk_empty[2], v_empty[2], s_full[2], pv_done[2];
+  // a buffer's Q/K may be refilled once its S product is done and its V
+  // once its PV product is: the producer reads both from the phases of
+  // s_full and pv_done (the next phase needs the very load being waited for)
+  uint64_t q_full[2], k_full[2], v_full[2], s_full[2], pv_done[2];
   uint64_t drain[2], pair[2];  // the two warps of a worker meet here (one arrival per warp)
   uint32_t tmem_base;
   int abort;
@@ -1179,8 +1182,6 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       mbar_init(&bars->q_full[j], 1);
       mbar_init(&bars->k_full[j], 1);
       mbar_init(&bars->v_full[j], 1);
-      mbar_init(&bars->qk_empty[j], 1);
-      mbar_init(&bars->v_empty[j], 1);
       mbar_init(&bars->s_full[j], 1);
       mbar_init(&bars->pv_done[j], 1);
       mbar_init(&bars->drain[j], 1);
@@ -1234,7 +1235,7 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
         bool prog = false;
         if (iq < nmine && iq < iv + 2) {
           const int j = iq & 1, use = iq >> 1;
-          if (mbar_test_wait(&bars->qk_empty[j], (use - 1) & 1u)) {
+          if (mbar_test_wait(&bars->s_full[j], (use - 1) & 1u)) {
             load_qk(iq);
             qk_uses[j] = use + 1;
             ++iq;
@@ -1244,7 +1245,7 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
         if (iv < iq) {
           const int j = iv & 1, use = iv >> 1;
           if (mbar_test_wait(&bars->k_full[j], use & 1u) &&
-              (use == 0 || mbar_test_wait(&bars->v_empty[j], (use - 1) & 1u))) {
+              (use == 0 || mbar_test_wait(&bars->pv_done[j], (use - 1) & 1u))) {
             const int v = blockIdx.x + iv * gridDim.x;
             uint8_t* buf = smem + j * kRingTcBuf;
             mbar_arrive_expect_tx(&bars->v_full[j], uint32_t(2 * a.cap * 128));
@@ -1293,7 +1294,7 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
     const uint32_t d_s = tmem + 256u * w;  // MMA accumulator (lane field 0)
     uint32_t pph = 0;                      // phase of this worker's pair barrier
     bool issued = false;
-    uint32_t nv = 0;  // items this worker computed: phases of s_full and pv_done
+    uint32_t nv = 0;  // items this worker took (computed or skipped): phases of s_full, pv_done
     // the sequence length and this row's sink logit of the worker's next
     // item are loaded one item ahead: their latency hides behind the
     // current item instead of stalling its start and its epilogue
@@ -1430,12 +1431,14 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       tc_fence_before();
       if (!pair_sync(&bars->pair[w], pph, lane, a, abort)) break;
       if (!valid) {
-        // nothing to compute: hand the buffer back once V has landed too
+        // nothing to compute: hand the buffer back once V has landed too,
+        // completing the phases of s_full and pv_done the products would have
         const bool ok = warp_wait(&bars->v_full[w], ph, a.ctl, abort);
         if (issuer) {
-          mbar_arrive(&bars->qk_empty[w]);
-          mbar_arrive(&bars->v_empty[w]);
+          mbar_arrive(&bars->s_full[w]);
+          mbar_arrive(&bars->pv_done[w]);
         }
+        ++nv;
         if (!ok) break;
         continue;
       }
@@ -1451,7 +1454,6 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
                   kd + uint64_t(((kk >> 2) * kRingTcKBox + (kk & 3) * 32) >> 4),
                   kk < 4 ? idesc_rot : idesc_s, kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full[w]);
-        umma_commit(&bars->qk_empty[w]);  // Q and K of the buffer may be refilled
       }
       issued = true;
       // visible positions [lo, p] sit in the cyclic slot interval starting at
@@ -1518,7 +1520,6 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
           umma_ts(d_s + 128, d_s + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_o,
                   kk > 0 ? 1u : 0u);
         umma_commit(&bars->pv_done[w]);
-        umma_commit(&bars->v_empty[w]);  // V of the buffer may be refilled
       }
       const float l = red[32 + lane] + red[96 + lane];
       if (!warp_wait(&bars->pv_done[w], phc, a.ctl, abort)) break;
@@ -1584,8 +1585,12 @@ cudaError_t launch_ring_tc(const DecodeArgs& a, cudaStream_t s) {
       !make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, a.cap, 1) ||
       !make_map(&mv, a.v_cache, long(a.B) * a.hkv, a.cap, kDv, a.cap, 1))
     return cudaErrorInvalidValue;
+  // as many CTAs as give each the same number of items (512 items over a
+  // 148-SM part: 128 CTAs of 4, two per worker, rather than 148 CTAs of 3 or
+  // 4, where the CTAs with 4 set the step's time)
   const long items = long(a.B) * a.hkv;
-  const int grid = int(items < num_sms() ? items : num_sms());
+  const long per = (items + num_sms() - 1) / num_sms();
+  const int grid = int((items + per - 1) / per);
   // programmatic dependent launch: the CTAs' setup overlaps the tail of the
   // kernel before them; every global read waits for it (grid_dep_wait)
   cudaLaunchConfig_t cfg = {};
