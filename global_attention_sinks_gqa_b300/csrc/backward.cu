@@ -529,7 +529,9 @@ constexpr int kDqSmem = kDqOffBar + 256 + 1024;
 static_assert(kDqSmem <= 232448, "shared memory");
 
 struct DqBars {
-  uint64_t fixed_full, fixed_empty, k_full[2], k_empty[2], v_full, v_empty;
+  // V(it) is free once dP(it) is done: the producer reads that from the
+  // phase of s_full (committed with it; the next phase needs V(it + 1))
+  uint64_t fixed_full, fixed_empty, k_full[2], k_empty[2], v_full;
   uint64_t s_full, s_free, p_full, acc_done, acc_free, drain;
   uint32_t tmem_base;
   int abort;
@@ -590,7 +592,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bars->k_empty[j], 1);
     }
     mbar_init(&bars->v_full, 1);
-    mbar_init(&bars->v_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 4);
     mbar_init(&bars->p_full, 4);
@@ -646,7 +647,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(kb + kBoxBytes128, &mK, &bars->k_full[j], 64, du.g, kr0);
           tma_load_3d(kb + 2 * kBoxBytes128, &mK, &bars->k_full[j], 128, du.g, kr0);
           ++kfill;
-          if (it >= 1 && !mbar_wait(&bars->v_empty, (it - 1) & 1, a.ctl, abort)) {
+          if (it >= 1 && !mbar_wait(&bars->s_full, (it - 1) & 1, a.ctl, abort)) {
             ok = false;
             break;
           }
@@ -694,7 +695,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + BN, ga + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4),
                   vd + uint64_t(((kk >> 2) * kBoxBytes128 + (kk & 3) * 32) >> 4), id_s, kk > 0);
-        umma_commit(&bars->v_empty);
         umma_commit(&bars->s_full);
         if (last) umma_commit(&bars->fixed_empty);
       }
