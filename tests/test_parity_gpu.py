@@ -307,6 +307,63 @@ def test_decode_append_is_append_then_decode(cap, window, T, G, lens):
     compare(out, lse, o_ref, l_ref, f"decode_append cap={cap} T={T} G={G}")
 
 
+def test_decode_steps_back_to_back_same_layer():
+    """Three decode steps of one window layer issued back to back, no
+    synchronisation between them: the window-ring kernel is launched as a
+    programmatic dependent and may start while the step before it runs, yet
+    every step must read the tokens the previous step appended to the ring."""
+    dev = torch.device("cuda")
+    T, G, hkv, cap, window, base, nsteps = 4, 8, 8, 131, 128, 1e4, 3
+    rs = np.random.RandomState(1600)
+    lens = [int(x) for x in rs.randint(3 * T, 900, size=32)] + [3 * T, 131 + 3 * T]
+    d = synth.decode_case(lens, T, G * hkv, hkv, window=window, rope_base=base, seed=1601)
+    kc, vc = fill_cache(d, cap, True, upto=[L - nsteps * T for L in lens])
+    g = synth._gen(1602, "cpu")
+    qs = [synth.randn_bf16((len(lens), T, G * hkv, synth.D_QK), g, "cpu") for _ in range(nsteps)]
+    sink = d.sink.to(dev)
+    outs = []
+    for s in range(nsteps):  # step s appends positions L - (nsteps - s) T ..
+        Ls = [L - (nsteps - 1 - s) * T for L in lens]
+        k_new = torch.stack([d.k_hist[b, L - T:L] for b, L in enumerate(Ls)]).to(dev)
+        v_new = torch.stack([d.v_hist[b, L - T:L] for b, L in enumerate(Ls)]).to(dev)
+        outs.append((Ls, ha.decode_append(qs[s].to(dev), k_new.contiguous(), v_new.contiguous(),
+                                          kc, vc, torch.tensor(Ls, dtype=torch.int32, device=dev),
+                                          sink, max_seqlen_k=max(lens), window=window,
+                                          is_ring=True, rope_base=base, softmax_scale=d.scale)))
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    for s, (Ls, (out, lse)) in enumerate(outs):
+        o_ref, l_ref = oracle.decode(qs[s], d.k_hist, d.v_hist, Ls, d.sink, window=window,
+                                     rope_base=base, scale=d.scale)
+        compare(out, lse, o_ref, l_ref, f"back-to-back step {s}")
+
+
+def test_decode_layers_back_to_back():
+    """The decode step of three window layers and a global layer (separate
+    caches) issued back to back, as a hybrid block runs them."""
+    dev = torch.device("cuda")
+    T = 4
+    rs = np.random.RandomState(1610)
+    lens = [int(x) for x in rs.randint(T, 3000, size=24)]
+    layers = []
+    for li, (window, hkv, base) in enumerate([(128, 8, 1e4)] * 3 + [(0, 4, 5e6)]):
+        d = synth.decode_case(lens, T, 64, hkv, window=window, rope_base=base, seed=1611 + li)
+        cap = 131 if window else max(lens) + 5
+        kc, vc, k_new, v_new, sl = _append_step(d, cap, window > 0)
+        layers.append((d, window, base, kc, vc, k_new, v_new, sl))
+    res = []
+    for d, window, base, kc, vc, k_new, v_new, sl in layers:
+        res.append(ha.decode_append(d.q.to(dev), k_new, v_new, kc, vc, sl, d.sink.to(dev),
+                                    max_seqlen_k=max(lens), window=window, is_ring=window > 0,
+                                    rope_base=base, softmax_scale=d.scale))
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    for (d, window, base, *_), (out, lse) in zip(layers, res):
+        o_ref, l_ref = oracle.decode(d.q, d.k_hist, d.v_hist, lens, d.sink, window=window,
+                                     rope_base=base, scale=d.scale)
+        compare(out, lse, o_ref, l_ref, f"layer chain W={window}")
+
+
 def test_decode_append_unwritten_slots_hold_nan():
     """The fused append over a ring whose never-written slots hold NaN."""
     lens, T, cap = [4, 9, 60, 130, 131, 700], 4, 131
