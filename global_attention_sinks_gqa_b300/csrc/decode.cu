@@ -1061,7 +1061,12 @@ constexpr int kRingTcBuf = kRingTcOffV + 2 * kRingTcKBox;
 constexpr int kRingTcOffCs = 2 * kRingTcBuf;     // (cos, sin) of the item's tokens, per worker
 constexpr int kRingTcCsRow = 32 * 8 + 16;        // one token's 32 pairs (+16: no bank clash)
 constexpr int kRingTcOffRed = kRingTcOffCs + 2 * 4 * kRingTcCsRow;  // [worker][half][max|sum][32]
-constexpr int kRingTcOffBar = kRingTcOffRed + 2 * 2 * 2 * 32 * 4;
+// the T <= 4 new tokens' K (3 boxes of [T rows][64 dims]) and V (2 boxes) of a
+// worker's item, loaded with its Q (the fused append reads them from here)
+constexpr int kRingTcNewBox = 1024;
+constexpr int kRingTcNewBytes = 5 * kRingTcNewBox;  // per worker
+constexpr int kRingTcOffNew = (kRingTcOffRed + 2 * 2 * 2 * 32 * 4 + 1023) / 1024 * 1024;
+constexpr int kRingTcOffBar = kRingTcOffNew + 2 * kRingTcNewBytes;
 constexpr int kRingTcSmem = kRingTcOffBar + 256 + 1024;  // + barriers + alignment slack
 constexpr int kRingTcThreads = 192;
 static_assert(kRingTcBuf % 1024 == 0 && kRingTcKBox % 1024 == 0, "swizzle atoms");
@@ -1153,7 +1158,9 @@ template <int G>
 __global__ void __launch_bounds__(kRingTcThreads, 1)
     decode_ring_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                           const __grid_constant__ CUtensorMap mapK,
-                          const __grid_constant__ CUtensorMap mapV, const DecodeArgs a) {
+                          const __grid_constant__ CUtensorMap mapV,
+                          const __grid_constant__ CUtensorMap mapKN,
+                          const __grid_constant__ CUtensorMap mapVN, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1163,15 +1170,24 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
   const int RR = ring_tc_rows(a.cap);
   RingTcBars* bars = reinterpret_cast<RingTcBars*>(smem + kRingTcOffBar);
   volatile int* abort = &bars->abort;
-  // Q (3 boxes of [G*T rows][64 dims]) on q_full, K (3 boxes of [cap slots]
-  // [64 dims]) on k_full of buffer j = i % 2
+  // Q (3 boxes of [G*T rows][64 dims]) -- and with a fused append the new
+  // tokens' K and V (5 boxes of [T rows][64 dims]) -- on q_full, K (3 boxes
+  // of [cap slots][64 dims]) on k_full of buffer j = i % 2
+  const bool fused = a.k_new != nullptr;
   auto load_qk = [&](int i) {
     const int v = blockIdx.x + i * gridDim.x;
     const int b = v / a.hkv, kvh = v - b * a.hkv, j = i & 1;
     uint8_t* buf = smem + j * kRingTcBuf;
-    mbar_arrive_expect_tx(&bars->q_full[j], uint32_t(3 * rows * 128));
+    mbar_arrive_expect_tx(&bars->q_full[j], uint32_t((3 * rows + (fused ? 5 * T : 0)) * 128));
     for (int k = 0; k < 3; ++k)
       tma_load_3d(buf + k * kRingTcQBox, &mapQ, &bars->q_full[j], 64 * k, kvh * G, b * T);
+    if (fused) {
+      uint8_t* nb = smem + kRingTcOffNew + j * kRingTcNewBytes;
+      for (int k = 0; k < 3; ++k)
+        tma_load_3d(nb + k * kRingTcNewBox, &mapKN, &bars->q_full[j], 64 * k, kvh, b * T);
+      for (int k = 0; k < 2; ++k)
+        tma_load_3d(nb + (3 + k) * kRingTcNewBox, &mapVN, &bars->q_full[j], 64 * k, kvh, b * T);
+    }
     mbar_arrive_expect_tx(&bars->k_full[j], uint32_t(3 * a.cap * 128));
     for (int k = 0; k < 3; ++k)
       tma_load_3d(buf + kRingTcOffK + k * kRingTcKBox, &mapK, &bars->k_full[j], 64 * k, 0, v);
@@ -1193,6 +1209,10 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
     tma_prefetch_map(&mapQ);
     tma_prefetch_map(&mapK);
     tma_prefetch_map(&mapV);
+    if (fused) {
+      tma_prefetch_map(&mapKN);
+      tma_prefetch_map(&mapVN);
+    }
   }
   if (warp == 2) {
     __syncwarp();
@@ -1318,30 +1338,16 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       L_next = item_len(i + 2);
       sink_next = item_sink(i + 2);
       const bool valid = length_ok(L, a);
-      // fused append: this lane's share of the T new tokens' K and V, read
-      // now so that the loads overlap the wait for the ring.  K pairs of
-      // chunks (c, c + 4), c in this half's two rotated chunks: lanes < 2T;
-      // the other 16 K chunks and the 16 V chunks of each token: task
-      // e = 32 hf + lane < 16 T.
+      // fused append: this lane's share of the T new tokens' K and V, which
+      // land with Q (read into registers once Q has, before the S product
+      // lets the producer refill the buffer).  K pairs of chunks (c, c + 4),
+      // c in this half's two rotated chunks: lanes < 2T; the other 16 K
+      // chunks and the 16 V chunks of each token: task e = 32 hf + lane < 16 T.
       const bool fuse = a.k_new != nullptr && valid;
       const int e_task = 32 * hf + lane;
       const int kp_t = lane >> 1, kp_c = 2 * hf + (lane & 1);
       const int pl_t = e_task >> 4, pl_c = 8 + (e_task & 15), v_c = e_task & 15;
       uint4 kp_x = make_uint4(0u, 0u, 0u, 0u), kp_y = kp_x, kpl = kp_x, vpl = kp_x;
-      if (fuse) {
-        const uint4* kn = static_cast<const uint4*>(a.k_new);
-        const uint4* vn = static_cast<const uint4*>(a.v_new);
-        if (lane < 2 * T) {
-          const long row = (long(b) * T + kp_t) * a.hkv + kvh;
-          kp_x = __ldg(kn + row * 24 + kp_c);
-          kp_y = __ldg(kn + row * 24 + kp_c + 4);
-        }
-        if (e_task < 16 * T) {
-          const long row = (long(b) * T + pl_t) * a.hkv + kvh;
-          kpl = __ldg(kn + row * 24 + pl_c);
-          vpl = __ldg(vn + row * 16 + v_c);
-        }
-      }
       if (valid) {
         // (cos, sin) of the 16 frequencies this half rotates, at each of the
         // T query positions
@@ -1352,6 +1358,20 @@ __global__ void __launch_bounds__(kRingTcThreads, 1)
       }
       __syncwarp();
       if (!warp_wait(&bars->q_full[w], ph, a.ctl, abort)) break;
+      if (fuse) {
+        // rows of 128 bytes, 16-byte chunks swizzled by row (boxes 1 KB-aligned)
+        const uint8_t* nb = smem + kRingTcOffNew + w * kRingTcNewBytes;
+        if (lane < 2 * T) {
+          kp_x = *reinterpret_cast<const uint4*>(nb + kp_t * 128 + ((kp_c ^ kp_t) << 4));
+          kp_y = *reinterpret_cast<const uint4*>(nb + kp_t * 128 + (((kp_c + 4) ^ kp_t) << 4));
+        }
+        if (e_task < 16 * T) {
+          kpl = *reinterpret_cast<const uint4*>(nb + (pl_c >> 3) * kRingTcNewBox + pl_t * 128 +
+                                                (((pl_c & 7) ^ pl_t) << 4));
+          vpl = *reinterpret_cast<const uint4*>(nb + (3 + (v_c >> 3)) * kRingTcNewBox +
+                                                pl_t * 128 + (((v_c & 7) ^ pl_t) << 4));
+        }
+      }
       const int p = L - T + t;  // this row's query position
       if (valid) {
         // RoPE of this row's dim pairs (f, f + 32), f in this half's 16:
@@ -1580,11 +1600,20 @@ cudaError_t launch_ring_tc(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mkn, mvn;
   if (!make_map(&mq, a.q, long(a.B) * a.T, a.hq, kDqk, G, a.T) ||
       !make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, a.cap, 1) ||
       !make_map(&mv, a.v_cache, long(a.B) * a.hkv, a.cap, kDv, a.cap, 1))
     return cudaErrorInvalidValue;
+  // the new tokens' K / V [B, T, hkv, d]: boxes of one KV head's T rows
+  if (a.k_new != nullptr) {
+    if (!make_map(&mkn, a.k_new, long(a.B) * a.T, a.hkv, kDqk, 1, a.T) ||
+        !make_map(&mvn, a.v_new, long(a.B) * a.T, a.hkv, kDv, 1, a.T))
+      return cudaErrorInvalidValue;
+  } else {
+    mkn = mq;  // not read
+    mvn = mq;
+  }
   // as many CTAs as give each the same number of items (512 items over a
   // 148-SM part: 128 CTAs of 4, two per worker, rather than 148 CTAs of 3 or
   // 4, where the CTAs with 4 set the step's time)
@@ -1603,7 +1632,7 @@ cudaError_t launch_ring_tc(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_ring_tc_kernel<G>, mq, mk, mv, a);
+  return cudaLaunchKernelEx(&cfg, decode_ring_tc_kernel<G>, mq, mk, mv, mkn, mvn, a);
 }
 
 cudaError_t launch_decode_kernel(const DecodeArgs& a, cudaStream_t s) {
