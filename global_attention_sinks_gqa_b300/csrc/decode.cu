@@ -649,384 +649,6 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Small rings (cap <= 256 slots, one chunk): one CTA per (sequence, KV head)
-// loads the whole ring with one TMA round (K: 3 boxes, V: 2 boxes of
-// [cap slots][64 dims]) while its warps fetch their Q fragments, then 4 warps
-// (MT 16-row m-tiles x KW slot groups) run QK^T and PV on mma.sync over the
-// resident ring and merge by log-sum-exp.  At W = 128 an item is 32 rows x
-// 131 slots: far too little multiply to pay for tensor-memory round trips,
-// and two such CTAs fit one SM, so loads of one overlap the math of the other.
-// ---------------------------------------------------------------------------
-constexpr int kRingMaxCap = 256;
-constexpr int kRingThreads = 128;
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                          uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                        uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// Byte offset of 16-byte chunk c (0..7) of row `row` in a [rows][64] bf16 box
-// written by TMA with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t sw128(int row, int c) {
-  return uint32_t(row * 128 + ((c ^ (row & 7)) << 4));
-}
-
-// Rows of one ring box in shared memory: cap rounded up to whole 16-slot
-// k-steps (rows past cap are never written by TMA; V rows there are zeroed).
-// After the math the K boxes hold the merge scratch (partial O of up to 3
-// warps + their m, l, lr), so the boxes span at least that much; the mbarrier
-// sits past both.
-constexpr int kRingScratch = 3 * 16 * 128 * 4 + 4 * 48 * 4;
-__host__ __device__ constexpr int ring_rows(int cap) { return (cap + 15) & ~15; }
-__host__ __device__ constexpr int ring_bar_offset(int cap) {
-  return 5 * ring_rows(cap) * 128 > kRingScratch ? 5 * ring_rows(cap) * 128
-                                                : ((kRingScratch + 63) & ~63);
-}
-__host__ __device__ constexpr int ring_smem_bytes(int cap) {
-  return ring_bar_offset(cap) + 64 + 1024;  // + barrier + alignment slack
-}
-
-template <int MT>
-__global__ void __launch_bounds__(kRingThreads)
-    decode_ring_kernel(const __grid_constant__ CUtensorMap mapK,
-                       const __grid_constant__ CUtensorMap mapV, const DecodeArgs a) {
-  constexpr int KW = 4 / MT;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int mt = warp % MT, kg = warp / MT;
-  const int G = a.hq / a.hkv, T = a.T, rows = G * T;
-  const int b = blockIdx.x / a.hkv, kvh = blockIdx.x - b * a.hkv;
-  const int RR = ring_rows(a.cap);
-  const int box = RR * 128;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + ring_bar_offset(a.cap));
-  int* abort = reinterpret_cast<int*>(smem + ring_bar_offset(a.cap) + 8);
-  const int L = __ldg(a.seqlens + b);
-  if (!length_ok(L, a)) {
-    if (threadIdx.x == 0 && kvh == 0) record_status(a.ctl, HATTN_ERR_INVALID_ARG);
-    return;
-  }
-  const int nslots = min(L, a.cap);  // slots written so far
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    *abort = 0;
-    mbar_fence_init();
-  }
-  // V rows past cap are read by the last k-step: make them zero
-  for (int e = threadIdx.x; e < (RR - a.cap) * 16; e += kRingThreads) {
-    const int rr = a.cap + (e >> 4), c16 = e & 15;
-    *reinterpret_cast<uint4*>(smem + (3 + (c16 >> 3)) * box + rr * 128 + (c16 & 7) * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    tma_prefetch_map(&mapK);
-    tma_prefetch_map(&mapV);
-    mbar_arrive_expect_tx(bar, uint32_t(5 * a.cap * 128));
-    const int plane = b * a.hkv + kvh;
-    for (int i = 0; i < 3; ++i) tma_load_3d(smem + i * box, &mapK, bar, 64 * i, 0, plane);
-    for (int i = 0; i < 2; ++i) tma_load_3d(smem + (3 + i) * box, &mapV, bar, 64 * i, 0, plane);
-  }
-
-  // ---- this warp's 16 query rows (r = t * G + hh) while the ring streams in
-  const int r0 = mt * 16 + gid, r1 = r0 + 8;
-  const bool v0 = r0 < rows, v1 = r1 < rows;
-  const int t0r = v0 ? r0 / G : T - 1, t1r = v1 ? r1 / G : T - 1;
-  const int p0 = L - T + t0r, p1 = L - T + t1r;  // query positions
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  const long q0 = ((long(b) * T + t0r) * a.hq + kvh * G + (v0 ? r0 % G : 0)) * kDqk;
-  const long q1 = ((long(b) * T + t1r) * a.hq + kvh * G + (v1 ? r1 % G : 0)) * kDqk;
-  uint32_t qa[12][4];
-#pragma unroll
-  for (int kk = 0; kk < 12; ++kk) {
-    const int c = kk * 16 + 2 * tig;
-    qa[kk][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q + q0 + c)) : 0u;
-    qa[kk][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q + q1 + c)) : 0u;
-    qa[kk][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(q + q0 + c + 8)) : 0u;
-    qa[kk][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q + q1 + c + 8)) : 0u;
-  }
-  // RoPE on dims 0..63: dim d (k-step d/16) pairs with d + 32 (k-step + 2),
-  // which this thread holds in the same register slot.
-#pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-    for (int reg = 0; reg < 4; ++reg) {
-      const int d = kk * 16 + ((reg & 2) ? 8 : 0) + 2 * tig;
-      const int pos = (reg & 1) ? p1 : p0;
-      const float2 x = unpack_bf16x2(qa[kk][reg]);
-      const float2 y = unpack_bf16x2(qa[kk + 2][reg]);
-      const float2 c0 = rope_cos_sin(pos, a.freqs.hi[d], a.freqs.lo[d]);
-      const float2 c1 = rope_cos_sin(pos, a.freqs.hi[d + 1], a.freqs.lo[d + 1]);
-      const float a0 = x.x * c0.x - y.x * c0.y, a1 = x.y * c1.x - y.y * c1.y;
-      const float b0 = y.x * c0.x + x.x * c0.y, b1 = y.y * c1.x + x.y * c1.y;
-      if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
-        record_status(a.ctl, HATTN_ERR_INVALID_ARG);
-      qa[kk][reg] = pack_f16x2(a0, a1);  // rotated dims are fp16 operands
-      qa[kk + 2][reg] = pack_f16x2(b0, b1);
-    }
-  }
-  // the ring keeps positions [L - cap, L): slot s holds the one congruent to s
-  const int base = L - a.cap;
-  int ring_r = base % a.cap;
-  if (ring_r < 0) ring_r += a.cap;
-  const int ring_off = base - ring_r;
-
-  const bool ok = mbar_wait(bar, 0, a.ctl, reinterpret_cast<volatile int*>(abort));
-  if (!ok) {  // never leave with the ring copies still in flight
-    if (threadIdx.x == 0) mbar_wait_drain(bar, 0, a.ctl);
-    return;
-  }
-  if (nslots < a.cap) {
-    // slots not written yet (sequence shorter than the ring): their weights
-    // are 0, but 0 * NaN is not, so zero those V rows
-    for (int e = threadIdx.x; e < (a.cap - nslots) * 16; e += kRingThreads) {
-      const int rr = nslots + (e >> 4), c16 = e & 15;
-      *reinterpret_cast<uint4*>(smem + (3 + (c16 >> 3)) * box + rr * 128 + (c16 & 7) * 16) =
-          make_uint4(0u, 0u, 0u, 0u);
-    }
-    __syncthreads();
-  }
-  // this warp's k-steps (16 slots each) of the RR / 16 the ring spans
-  const int nks = RR / 16;
-  const int ks_lo = kg * nks / KW, ks_hi = (kg + 1) * nks / KW;
-  const uint32_t sbase = smem_u32(smem);
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  // running max (exact: every chunk rescales) and sum of 2^(x - m), per row
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  {
-    for (int kc = ks_lo; kc < ks_hi; kc += 4) {  // chunks of up to 4 k-steps (64 slots)
-      const int nk = min(4, ks_hi - kc);
-      float s[8][4];
-#pragma unroll
-      for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 12; ++kk) {
-#pragma unroll
-        for (int n = 0; n < 8; n += 2) {
-          if (n / 2 < nk) {
-            const int mi = lane >> 3, rr = lane & 7;
-            const int key = (kc + n / 2) * 16 + (mi >> 1) * 8 + rr;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(sbase + (kk >> 2) * box + sw128(key, (kk & 3) * 2 + (mi & 1)), b0, b1, b2,
-                    b3);
-            if (kk < 4) {  // rotated dims: fp16 x fp16
-              mma_f16(s[n], qa[kk], b0, b1);
-              mma_f16(s[n + 1], qa[kk], b2, b3);
-            } else {
-              mma_bf16(s[n], qa[kk], b0, b1);
-              mma_bf16(s[n + 1], qa[kk], b2, b3);
-            }
-          }
-        }
-      }
-      // mask by key position, chunk max, online update (base 2)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int sl = kc * 16 + n * 8 + 2 * tig + e;
-          const int kp = sl + ring_off + (sl < ring_r ? a.cap : 0);
-          const bool in = n / 2 < nk && sl < nslots;
-          const bool vis0 = in && kp <= p0 && p0 - kp < a.window;
-          const bool vis1 = in && kp <= p1 && p1 - kp < a.window;
-          s[n][e] = vis0 ? s[n][e] * a.scale_log2 : -INFINITY;
-          s[n][2 + e] = vis1 ? s[n][2 + e] * a.scale_log2 : -INFINITY;
-          mx0 = fmaxf(mx0, s[n][e]);
-          mx1 = fmaxf(mx1, s[n][2 + e]);
-        }
-      }
-#pragma unroll
-      for (int off = 1; off <= 2; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
-      m0 = mn0;
-      m1 = mn1;
-      float rs0 = 0.f, rs1 = 0.f;
-      uint32_t pa[4][4];
-#pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        const float e0 = fast_exp2(s[n][0] - ms0), e1 = fast_exp2(s[n][1] - ms0);
-        const float e2 = fast_exp2(s[n][2] - ms1), e3 = fast_exp2(s[n][3] - ms1);
-        rs0 += e0 + e1;
-        rs1 += e2 + e3;
-        pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16x2(e0, e1);
-        pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16x2(e2, e3);
-      }
-      l0 = l0 * al0 + rs0;
-      l1 = l1 * al1 + rs1;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= al0;
-        o[n][1] *= al0;
-        o[n][2] *= al1;
-        o[n][3] *= al1;
-      }
-      // O += P V (V box np/4 holds dims 64*(np/4) .. +63)
-#pragma unroll
-      for (int j2 = 0; j2 < 4; ++j2) {
-        if (j2 < nk) {
-          const uint32_t afr[4] = {pa[j2][0], pa[j2][1], pa[j2][2], pa[j2][3]};
-          const int k0 = (kc + j2) * 16;
-#pragma unroll
-          for (int np = 0; np < 8; ++np) {
-            const int mi = lane >> 3, rr = lane & 7;
-            const int key = k0 + (mi & 1) * 8 + rr;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sbase + (3 + (np >> 2)) * box + sw128(key, (np & 3) * 2 + (mi >> 1)), b0,
-                      b1, b2, b3);
-            mma_bf16(o[2 * np], afr, b0, b1);
-            mma_bf16(o[2 * np + 1], afr, b2, b3);
-          }
-        }
-      }
-    }
-  }
-  // ---- row sums over the quad, then merge the KW slot groups through the
-  // (no longer needed) K boxes
-#pragma unroll
-  for (int off = 1; off <= 2; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  __syncthreads();
-  if (KW > 1) {
-    float* red = reinterpret_cast<float*>(smem);
-    float* mlred = red + 3 * 16 * 128;
-    if (kg != 0) {
-      float* ow = red + ((kg - 1) * MT + mt) * (16 * 128);
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const int c = n * 8 + 2 * tig;
-        *reinterpret_cast<float2*>(ow + gid * 128 + c) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(ow + (gid + 8) * 128 + c) = make_float2(o[n][2], o[n][3]);
-      }
-      float* ml = mlred + warp * 48;
-      if (tig == 0) {
-        ml[gid] = m0;
-        ml[gid + 8] = m1;
-        ml[16 + gid] = l0;
-        ml[16 + gid + 8] = l1;
-      }
-    }
-    __syncthreads();
-    if (kg == 0) {
-      float mm0 = m0, mm1 = m1;
-      for (int w = 1; w < KW; ++w) {
-        const float* mlw = mlred + (w * MT + mt) * 48;
-        mm0 = fmaxf(mm0, mlw[gid]);
-        mm1 = fmaxf(mm1, mlw[gid + 8]);
-      }
-      const float ms0 = mm0 == -INFINITY ? 0.f : mm0, ms1 = mm1 == -INFINITY ? 0.f : mm1;
-      const float f0 = fast_exp2(m0 - ms0), f1 = fast_exp2(m1 - ms1);
-      l0 *= f0;
-      l1 *= f1;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= f0;
-        o[n][1] *= f0;
-        o[n][2] *= f1;
-        o[n][3] *= f1;
-      }
-      for (int w = 1; w < KW; ++w) {
-        const float* mlw = mlred + (w * MT + mt) * 48;
-        const float g0 = fast_exp2(mlw[gid] - ms0), g1 = fast_exp2(mlw[gid + 8] - ms1);
-        l0 += mlw[16 + gid] * g0;
-        l1 += mlw[16 + gid + 8] * g1;
-        const float* ow2 = red + ((w - 1) * MT + mt) * (16 * 128);
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          const int c = n * 8 + 2 * tig;
-          const float2 x0 = *reinterpret_cast<const float2*>(ow2 + gid * 128 + c);
-          const float2 x1 = *reinterpret_cast<const float2*>(ow2 + (gid + 8) * 128 + c);
-          o[n][0] += x0.x * g0;
-          o[n][1] += x0.y * g0;
-          o[n][2] += x1.x * g1;
-          o[n][3] += x1.y * g1;
-        }
-      }
-      m0 = mm0;
-      m1 = mm1;
-    }
-  }
-  if (kg != 0) return;
-  // ---- add the sink and finish the rows
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const bool valid = half ? v1 : v0;
-    const int r = half ? r1 : r0;
-    const float m = half ? m1 : m0;
-    const float l = half ? l1 : l0;
-    if (!valid) continue;
-    const int t = r / G, h = kvh * G + r % G;
-    const float sl2 = __ldg(a.sink + h) * kLog2e;
-    const float mt_ = fmaxf(m, sl2);
-    const float msub = mt_ == -INFINITY ? 0.f : mt_;
-    const float fo = fast_exp2(m - msub);
-    const float sw = fast_exp2(sl2 - msub);
-    const float sc = fo / (l * fo + sw);
-    const long orow = (long(b) * T + t) * a.hq + h;
-    uint32_t* op = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDv);
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int c = n * 8 + 2 * tig;
-      op[c >> 1] = pack_bf16x2(o[n][half * 2] * sc, o[n][half * 2 + 1] * sc);
-    }
-    if (tig == 0 && a.lse) a.lse[orow] = (msub + log2f(l * fo + sw)) * kLn2;
-  }
-}
-
-template <int MT>
-cudaError_t launch_ring(const DecodeArgs& a, cudaStream_t s) {
-  const int smem = ring_smem_bytes(kRingMaxCap);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_ring_kernel<MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  CUtensorMap mk, mv;
-  if (!make_map(&mk, a.k_cache, long(a.B) * a.hkv, a.cap, kDqk, a.cap, 1) ||
-      !make_map(&mv, a.v_cache, long(a.B) * a.hkv, a.cap, kDv, a.cap, 1))
-    return cudaErrorInvalidValue;
-  decode_ring_kernel<MT><<<unsigned(long(a.B) * a.hkv), kRingThreads, ring_smem_bytes(a.cap), s>>>(
-      mk, mv, a);
-  return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
 // Rings of at most 144 slots with at most 32 query rows (the window layer at
 // W = 128, T <= 4, G <= 8) on the tensor cores.  Persistent: one CTA per SM
 // walks the items (sequence, KV head) v = blockIdx.x + i * gridDim.x.  Two
@@ -1721,13 +1343,6 @@ cudaError_t launch_decode(const DecodeArgs& a_in, cudaStream_t s) {
       case 8: return launch_ring_tc<8>(a, s);
       default: break;
     }
-  }
-  // a ring small enough to sit in shared memory whole: one CTA per item
-  if (a.is_ring && a.cap <= kRingMaxCap && a.nsplit == 1 && G * a.T <= 64) {
-    const int rows = G * a.T;
-    if (rows <= 16) return launch_ring<1>(a, s);
-    if (rows <= 32) return launch_ring<2>(a, s);
-    return launch_ring<4>(a, s);
   }
   return launch_decode_kernel(a, s);
 }
