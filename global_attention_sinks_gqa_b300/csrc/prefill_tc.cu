@@ -130,9 +130,10 @@ struct Cfg {
   static_assert(NSLOT >= (ONE ? 5 : 8), "ring must hold a K and a V block (and room to prefetch)");
   // Several key blocks per unit: the slots form KST stages of one K block
   // (3 boxes each) and one stage of one V block (2 boxes, after them), each
-  // stage on its own full / empty barrier pair (kv_full[0..KST-1] for K,
-  // kv_full[KST] for V).  K_{j+1} can then load as soon as K_{j+1-KST} is
-  // released, a whole key block ahead of its S product.
+  // stage with its own empty barrier (kv_empty[0..KST-1] for K, kv_empty[KST]
+  // for V); the blocks land on k0_full (K_0) or tile A's p_full (the rest).
+  // K_{j+1} can then load as soon as K_{j+1-KST} is released and P_A(j - 1)
+  // is done, about a key block ahead of its S product.
   static constexpr int KST = (NSLOT - 2) / 3;
   static_assert(ONE || KST >= 2, "two K stages");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
@@ -180,6 +181,7 @@ struct Bars {
   uint64_t q_full[2], q_ready[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+  uint64_t k0_full;  // several key blocks per unit: K_0 of each unit
   uint64_t unit_full[kUnitQueue], unit_empty[kUnitQueue];
   uint64_t drain;
   uint32_t tmem_base;
@@ -451,7 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_ready[t], 128);
       mbar_init(&bars->q_empty[t], 1);
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      // several key blocks per unit: tile A's P barrier also takes the
+      // producer's V_j and K_{j+1} (or the softmax's stand-in on a unit's
+      // last block)
+      mbar_init(&bars->p_full[t], (!ONE && t == 0) ? 130 : 128);
       mbar_init(&bars->pv_done[t], 1);
       mbar_init(&bars->o_free[t], 128);
     }
@@ -463,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->unit_full[i], 1);
       mbar_init(&bars->unit_empty[i], kUnitReaders);
     }
+    mbar_init(&bars->k0_full, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -528,23 +534,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // through mapK0, the others through mapK12
       auto kmap = [&](int i) { return i == 0 ? &mapK0 : &mapK12; };
       uint32_t un = 0;  // one-block units whose K and V were loaded
-      // several key blocks per unit: whole K / V blocks into their stages
-      uint32_t kq = 0, vq = 0;  // K and V blocks loaded
-      auto load_k = [&](const UnitInfo& ui, int kpos) -> bool {
+      // several key blocks per unit: whole K / V blocks into their stages.
+      // K_0 of a unit completes k0_full.  K_{j+1} and V_j instead complete
+      // phase j of tile A's p_full together with the softmax's P_A(j), so
+      // that one wait of the MMA issuer covers PV_A(j) and S(j + 1).  Each
+      // arrives (with its bytes) only once phase j - 1 is complete: K_{j+1}
+      // waits for it here; V_j loads into a stage that PV_B(j - 1) released,
+      // and PV_B(j - 1) was issued after that phase.  Phase j cannot complete
+      // without these arrivals, so the parity waited on cannot alias.
+      uint32_t kq = 0, vq = 0;  // K and V blocks loaded (vq: p_full[0] phases joined)
+      uint32_t k0n = 0;         // phases of k0_full (units started)
+      auto load_k = [&](const UnitInfo& ui, int kpos, bool first) -> bool {
         const uint32_t st = kq % C::KST, ph = (kq / C::KST) & 1u;
         if (!mbar_wait(&bars->kv_empty[st], ph ^ 1u, a.ctl, abort)) return false;
-        mbar_arrive_expect_tx(&bars->kv_full[st], 3 * C::kSlot);
+        if (!first && vq > 0 && !mbar_wait(&bars->p_full[0], (vq - 1) & 1u, a.ctl, abort))
+          return false;
+        uint64_t* full = first ? &bars->k0_full : &bars->p_full[0];
+        mbar_arrive_expect_tx(full, 3 * C::kSlot);
         for (int i = 0; i < 3; ++i)
-          tma_load_3d(ring + (st * 3 + i) * C::kSlot, kmap(i), &bars->kv_full[st], 64 * i,
-                      kv_c1(ui, kpos), kv_c2(ui, kpos));
+          tma_load_3d(ring + (st * 3 + i) * C::kSlot, kmap(i), full, 64 * i, kv_c1(ui, kpos),
+                      kv_c2(ui, kpos));
         ++kq;
+        if (first) ++k0n;
         return true;
       };
       auto load_v = [&](const UnitInfo& ui, int vpos) -> bool {
         if (!mbar_wait(&bars->kv_empty[C::KST], (vq & 1u) ^ 1u, a.ctl, abort)) return false;
-        mbar_arrive_expect_tx(&bars->kv_full[C::KST], 2 * C::kSlot);
+        mbar_arrive_expect_tx(&bars->p_full[0], 2 * C::kSlot);
         for (int i = 0; i < 2; ++i)
-          tma_load_3d(ring + (C::KST * 3 + i) * C::kSlot, &mapV, &bars->kv_full[C::KST], 64 * i,
+          tma_load_3d(ring + (C::KST * 3 + i) * C::kSlot, &mapV, &bars->p_full[0], 64 * i,
                       kv_c1(ui, vpos), kv_c2(ui, vpos));
         ++vq;
         return true;
@@ -572,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block: the Q tiles first -- a tile's buffer frees with its S MMA of
         // the previous unit and its RoPE heads the tile's next chain -- then
         // K_0, V_0.
-        if constexpr (!ONE) ok = load_k(ui, k0pos);
+        if constexpr (!ONE) ok = load_k(ui, k0pos, true);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -621,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // which the products release them
           for (int j = 0; j < ui.nblk && ok; ++j) {
             const int vpos = k0pos + j * BN;
-            if (j + 1 < ui.nblk) ok = load_k(ui, vpos + BN);
+            if (j + 1 < ui.nblk) ok = load_k(ui, vpos + BN, false);
             if (ok) ok = load_v(ui, vpos);
           }
         }
@@ -635,11 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_drain(&bars->kv_full[1], (un - 1) & 1u, a.ctl);
         }
       } else {
-        for (uint32_t st = 0; st < uint32_t(C::KST); ++st) {
-          const uint32_t fills = kq > st ? (kq - st + C::KST - 1) / C::KST : 0;
-          if (fills) mbar_wait_drain(&bars->kv_full[st], (fills - 1) & 1u, a.ctl);
-        }
-        if (vq) mbar_wait_drain(&bars->kv_full[C::KST], (vq - 1) & 1u, a.ctl);
+        if (k0n) mbar_wait_drain(&bars->k0_full, (k0n - 1) & 1u, a.ctl);
+        if (vq) mbar_wait_drain(&bars->p_full[0], (vq - 1) & 1u, a.ctl);
       }
     }
     } else if (warp == 1) {
@@ -711,13 +726,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++uc;
         }
       } else {
-      // K blocks in KST stages (positions kc), V blocks in one stage (vc):
-      // the stage of block c is kc % KST; K stage s holds slots 3s .. 3s + 2,
-      // the V stage slots 3 KST, 3 KST + 1
-      uint32_t kc = 0, vc = 0;
-      auto wait_k = [&]() -> uint32_t {  // slot position of the next K block
+      // K blocks in KST stages (the stage of the c-th K block is c % KST;
+      // K stage s holds slots 3s .. 3s + 2), V blocks in one stage (slots
+      // 3 KST, 3 KST + 1).  This thread waits on K_0 of a unit (k0_full)
+      // and then, per key block j, only on P_A(j) -- whose barrier also
+      // carries V_j and K_{j+1} -- and P_B(j); the softmax of tile B
+      // releases each K stage once it has seen S_B of that block.  Every
+      // wait and commit costs this thread hundreds of cycles while the
+      // products stream operands out of shared memory, so it makes three
+      // commits and two waits per block.
+      uint32_t kc = 0;
+      auto next_kslot = [&]() -> uint32_t {
         const uint32_t st = kc % C::KST;
-        if (!mbar_wait(&bars->kv_full[st], (kc / C::KST) & 1u, a.ctl, abort)) return ~0u;
         ++kc;
         return 3 * st;
       };
@@ -728,8 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u < 0) break;
         UnitInfo ui;
         unit_info<G, BN, WIN>(u, a, cu, nut, ui);
-        const uint32_t k0 = wait_k();
-        if (k0 == ~0u) break;
+        if (!mbar_wait(&bars->k0_full, uc & 1u, a.ctl, abort)) break;
+        const uint32_t k0 = next_kslot();
         for (int t = 0; t < 2 && ok; ++t) {
           if (!mbar_wait(&bars->q_ready[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
           tc_fence_after();
@@ -738,13 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ui.nblk == 1) umma_commit(&bars->q_empty[t]);
         }
         if (!ok) break;
-        umma_commit(&bars->kv_empty[k0 / 3]);  // K_0's stage frees once both S are done
         for (int j = 0; j < ui.nblk && ok; ++j, ++blk) {
           const bool more = j + 1 < ui.nblk;
-          if (!mbar_wait(&bars->kv_full[C::KST], vc & 1u, a.ctl, abort)) { ok = false; break; }
-          ++vc;
           uint32_t kn = 0;
           for (int t = 0; t < 2; ++t) {
+            // t = 0: P_A(j), V_j and (more) K_{j+1} have landed
             if (!mbar_wait(&bars->p_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
             if (j == 0 && uc > 0 &&
                 !mbar_wait(&bars->o_free[t], (uc - 1) & 1u, a.ctl, abort)) {
@@ -756,14 +774,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!more) umma_commit(&bars->pv_done[t]);  // the unit's O_t is complete
             if (t == 1) umma_commit(&bars->kv_empty[C::KST]);  // V_j's stage
             if (more) {
-              if (t == 0) {
-                kn = wait_k();
-                if (kn == ~0u) { ok = false; break; }
-              }
+              if (t == 0) kn = next_kslot();
               issue_qk(t, kn);
               umma_commit(&bars->s_full[t]);
               if (j + 2 == ui.nblk) umma_commit(&bars->q_empty[t]);
-              if (t == 1) umma_commit(&bars->kv_empty[kn / 3]);  // K_{j+1}'s stage
             }
           }
         }
@@ -914,6 +928,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else
       for (int j = 0; j < ui.nblk; ++j, ++blk) {
         if (!warp_wait(&bars->s_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
+        // S_B of this block is done, and S_A before it: K_j's stage is free
+        // (the blk-th K block of this CTA)
+        if (t == 1 && r == 0) mbar_arrive(&bars->kv_empty[blk % C::KST]);
         tc_fence_after();
         const int kb = ui.kstart + j * BN;  // position of column 0
         uint32_t s[BN];
@@ -927,6 +944,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
+        // a unit's last block has no K_{j+1}: one softmax thread arrives in
+        // its place
+        if (t == 0 && r == 0 && j + 1 == ui.nblk) mbar_arrive(&bars->p_full[0]);
       }
       if (!ok) break;
       have_prev = true;
