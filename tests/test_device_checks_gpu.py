@@ -144,3 +144,33 @@ def test_prefill_cached_skips_and_reports_prefix_past_the_cache():
     o, l = oracle.decode(q_new[0][None], d.k_hist[0:1], d.v_hist[0:1], [prefixes[0] + news[0]],
                          d.sink, window=window, rope_base=base, scale=d.scale)
     compare(out_full[:news[0]], lse_full[:news[0]], o[0], l[0], "valid cached sequence")
+
+
+# (G, window, base): one-block window units (G = 8 and 16 at W = 128), a
+# window whose band needs several key blocks (G = 4) and a global layer
+@pytest.mark.parametrize("G,window,base", [(8, 128, 1e4), (16, 128, 1e4), (4, 128, 1e4),
+                                           (8, 0, 5e6)])
+def test_prefill_reports_rotated_keys_past_fp16(G, window, base):
+    """Rotated key dims are stored as fp16; a key whose rotation leaves the
+    fp16 range is reported as HATTN_ERR_INVALID_ARG.  x = y = 6e4 in the
+    pair (0, 32): the rotated values reach 6e4 * sqrt(2) at positions whose
+    angle (pos radians for frequency 0) is near pi/4 + k pi/2."""
+    dev = torch.device("cuda")
+    total = 300
+    c = synth.prefill_case([total], 2 * G, 2, window=window, rope_base=base, seed=907)
+    q, v, sink = c.q.to(dev), c.v.to(dev), c.sink.to(dev)
+    cu = c.cu_seqlens.to(dev)
+    k_big = c.k.clone()
+    k_big[:, :, 0] = 6e4
+    k_big[:, :, 32] = 6e4
+    ha.prefill(q, k_big.to(dev), v, sink, cu, max_seqlen=total, window=window, rope_base=base)
+    torch.cuda.synchronize()
+    assert ha.hattn_check_device_status() == ha.HATTN_ERR_INVALID_ARG
+    # keys within range: no report, and the result matches the oracle
+    out, lse = ha.prefill(q, c.k.to(dev), v, sink, cu, max_seqlen=total, window=window,
+                          rope_base=base)
+    torch.cuda.synchronize()
+    assert ha.hattn_check_device_status() == ha.HATTN_OK
+    o_ref, l_ref = oracle.prefill(c.q, c.k, c.v, c.sink, [0, total], window=window,
+                                  rope_base=base, scale=c.scale)
+    compare(out, lse, o_ref, l_ref, f"G {G} window {window}")
