@@ -145,6 +145,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def copy_note(copy_ms, alone_ms, nbytes, hbm):
+    """A part against a device-to-device copy moving the same bytes: the
+    copy's time and fraction of the HBM peak, and the part's time (alone)
+    over the copy's."""
+    return {"ms": round(copy_ms, 5), "frac_of_hbm_peak": round(nbytes / copy_ms / 1e6 / hbm, 4),
+            "part_alone_over_copy": round(alone_ms / copy_ms, 3)}
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -402,6 +410,23 @@ def run_cuda(args, rank, world):
     }
     wl.ha.check_device_status()
 
+    # The HBM peak is a device-to-device copy of 2 GiB each way; at the size
+    # of a short HBM-bound part the same copy reaches much less of it (ramp
+    # and tail).  So the HBM-bound parts also get a copy moving their own
+    # bytes (half read, half written), chained like their calls (the window
+    # decode: five layers, five buffers), L2 flushed before each repetition.
+    def copy_of(nbytes, chain):
+        n = int(nbytes) // 2 // 16 * 16  # bytes each way
+        src = [torch.zeros(n, dtype=torch.uint8, device=dev) for _ in range(chain)]
+        dst = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(chain)]
+        t = alone(lambda: [d.copy_(x) for x, d in zip(src, dst)], 20)
+        del src, dst
+        return t / chain
+
+    swa_dec = [dd for dd in wl.dec if dd["kind"] == "swa"]
+    copy_ms = {"p0": copy_of(wl.layers[0]["bytes"], 1),
+               "d_swa": copy_of(swa_dec[0]["bytes"] + swa_dec[0]["abytes"], len(swa_dec))}
+
     # ---- end to end: per step, inputs from pinned host memory, outputs back
     e2e = run_e2e(wl, args, stream, sptr)
 
@@ -422,6 +447,9 @@ def run_cuda(args, rank, world):
             ta = alone_ms[f"p{i}"] / 1e3
             parts[lay["name"]].update(alone_ms=ta * 1e3,
                                       alone_roofline_frac=max(bound_f, bound_b) / ta)
+        if f"p{i}" in copy_ms:
+            parts[lay["name"]]["same_bytes_copy"] = copy_note(
+                copy_ms[f"p{i}"], alone_ms[f"p{i}"], lay["bytes"], hbm)
         tr, _ = recorded_traffic("prefill_" + lay["name"].split("_")[0] + "_32k")
         parts[lay["name"]]["traffic"] = tr
     for kind in ("swa", "ga"):
@@ -436,6 +464,9 @@ def run_cuda(args, rank, world):
             timing="per layer: one event pair around the layers' calls back to back",
             alone_ms=alone_ms[f"d_{kind}"] / len(lays),
             alone_roofline_frac=byts / (hbm * 1e9) / (alone_ms[f"d_{kind}"] / len(lays) / 1e3))
+        if f"d_{kind}" in copy_ms:
+            parts[f"decode_{kind}_b64_t4"]["same_bytes_copy"] = copy_note(
+                copy_ms[f"d_{kind}"], alone_ms[f"d_{kind}"] / len(lays), byts, hbm)
     ga = wl.layers[1]
     ga_s = part_ms["p1"] / 1e3
     ga_tf, ga_tf_name = tensor_peak(ga_s, tf_burst, tf_sust)
