@@ -327,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + kOCol, p + kk * 8, make_sdesc_sw128(vbase + kk * 2048, kBox, 1024),
                   idesc_o, (!first || kk > 0) ? 1u : 0u);
         umma_commit(&bars->pv_done);
-        umma_commit(&bars->empty[st]);  // K and V of this block are consumed
+        // (the stage is released by a softmax thread once S of block
+        // blk_global + 2 is done: that QK^T was issued after this PV)
         return true;
       };
       uint32_t rn = 0;
@@ -499,6 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nb; ++j, ++blk) {
         const uint32_t sb = blk & 1u;
         if (!warp_wait(&bars->s_full[sb], (blk >> 1) & 1u, a.ctl, abort)) { ok = false; break; }
+        // QK^T of block blk was issued after PV of block blk - 2 (within an
+        // item QK_{j} follows PV_{j-2}; an item's first QK^T follows the last
+        // PV of the item before), so that block's K / V stage is free now
+        if (blk >= 2 && quad == 0 && lane == 0) mbar_arrive(&bars->empty[(blk - 2) % kStages]);
         tc_fence_after();
         const int sbase_slot = it.s_beg + j * kBK;
         const int valid_rows = it.s_end - sbase_slot;
