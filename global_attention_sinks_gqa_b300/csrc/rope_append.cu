@@ -70,60 +70,99 @@ __device__ __forceinline__ bool rope_key_row(const uint4* src, uint4* dst, int p
 
 constexpr int kRowsPerBlock = 8;  // one warp per row
 
-// Rotated-key pre-pass of prefill: one warp per token, all hkv heads of it.
-// Only the rotated dims 0..63 of each key row are read and written (as fp16,
-// into k_rot [total, hkv, 64]); the attention kernel reads dims 64..191
-// straight from k.  The token's 32 (cos, sin) pairs are computed once (lane i:
-// frequency i) and shared through shared memory by every head.  A task is one
-// head's pair of 16-byte chunks (c, c + 4), c < 4 -- the dims i and i + 32 a
-// rotation mixes -- so a warp covers 8 heads per pass with 64-byte pieces of
-// each 384-byte source row and whole 128-byte destination rows.
-constexpr int kTokWarps = 8;
+// Rotated-key pre-pass of prefill.  Only the rotated dims 0..63 of each key
+// row are read and written (as fp16, into k_rot [total, hkv, 64]); the
+// attention kernel reads dims 64..191 straight from k.  A task is one head's
+// pair of 16-byte chunks (c, c + 4), c < 4 -- the dims i and i + 32 a rotation
+// mixes; a block takes the 4 hkv tasks of each of its tokens (at most
+// kPassMaxTok of them), TPT tasks per thread.  Each thread first issues all
+// its tasks' loads; while they are in flight the block evaluates its tokens'
+// 32 (cos, sin) pairs into shared memory, each pair once for all the heads.
+// (One warp per token, with a token's loads issued only after its angles,
+// took 22-23 us for 32768 tokens whatever the head count; this layout takes
+// 18 us for 8 KV heads and 12 us for 4.)
+constexpr int kPassThreads = 256;
+constexpr int kPassMaxTok = 128;
+constexpr int kPassTasks = 8;  // tasks per thread
 
-__global__ void __launch_bounds__(256) rope_keys_packed_kernel(
+template <int TPT>
+__host__ __device__ inline int pass_tokens(int hkv) {
+  const int t = TPT * kPassThreads / (4 * hkv);
+  return t < 1 ? 1 : (t > kPassMaxTok ? kPassMaxTok : t);
+}
+
+template <int TPT>
+__global__ void __launch_bounds__(kPassThreads) rope_keys_packed_kernel(
     const uint4* __restrict__ k, uint4* __restrict__ k_rot, const int* __restrict__ cu_seqlens,
     int batch, long total, int hkv, const RopeFreqs f, const DeviceCtl ctl,
     unsigned int* __restrict__ unit_ctr, int pos_off) {
-  __shared__ float2 cs_tab[kTokWarps][32];
+  extern __shared__ float2 cs_tab[];  // [tokens of the block][32]
+  __shared__ int pos_tab[kPassMaxTok];
   if (unit_ctr != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *unit_ctr = 0u;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int ntask = hkv * 4;
+  const int ntok = pass_tokens<TPT>(hkv);
+  const long n0 = long(blockIdx.x) * ntok;
+  const int ntask = 4 * hkv * ntok;
   bool overflow = false;
-  for (long n = long(blockIdx.x) * kTokWarps + w; n < total; n += long(gridDim.x) * kTokWarps) {
-    int pos = int(n) + pos_off;
-    if (cu_seqlens != nullptr) {
-      // sequence holding packed token n: largest b with cu[b] <= n
-      int lo = 0, hi = batch;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu_seqlens + mid) <= n) lo = mid; else hi = mid - 1;
-      }
-      pos = int(n - __ldg(cu_seqlens + lo));
-    }
-    __syncwarp();
-    cs_tab[w][lane] = rope_cos_sin(pos, f.hi[lane], f.lo[lane]);
-    __syncwarp();
-    for (int task = lane; task < ntask; task += 32) {
-      const int h = task >> 2, c = task & 3;
-      const uint4* src = k + (n * hkv + h) * 24;
-      uint4* dst = k_rot + (n * hkv + h) * 8;
-      const uint4 x = __ldg(src + c), y = __ldg(src + c + 4);
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-      uint32_t a[4], b[4];
+  for (int base = 0; base < ntask; base += TPT * kPassThreads) {
+    uint4 x[TPT], y[TPT];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 8 * c + 2 * e;  // dims (i, i+1) pair with (i+32, i+33)
-        const float2 xv = unpack_bf16x2(xs[e]), yv = unpack_bf16x2(ys[e]);
-        const float2 cs0 = cs_tab[w][i], cs1 = cs_tab[w][i + 1];
-        const float a0 = xv.x * cs0.x - yv.x * cs0.y, a1 = xv.y * cs1.x - yv.y * cs1.y;
-        const float b0 = yv.x * cs0.x + xv.x * cs0.y, b1 = yv.y * cs1.x + xv.y * cs1.y;
-        if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
-          overflow = true;
-        a[e] = pack_f16x2(a0, a1);
-        b[e] = pack_f16x2(b0, b1);
+    for (int u = 0; u < TPT; ++u) {
+      const int task = base + u * kPassThreads + threadIdx.x;
+      const int tok = task / (4 * hkv), h = (task >> 2) % hkv, c = task & 3;
+      const long n = n0 + tok;
+      x[u] = make_uint4(0u, 0u, 0u, 0u);
+      y[u] = x[u];
+      if (task < ntask && n < total) {
+        const uint4* src = k + (n * hkv + h) * 24;
+        x[u] = __ldg(src + c);
+        y[u] = __ldg(src + c + 4);
       }
-      dst[c] = make_uint4(a[0], a[1], a[2], a[3]);
-      dst[c + 4] = make_uint4(b[0], b[1], b[2], b[3]);
+    }
+    if (base == 0) {
+      for (int t = threadIdx.x; t < ntok; t += kPassThreads) {
+        const long nt = n0 + t;
+        int pos = int(nt) + pos_off;
+        if (cu_seqlens != nullptr && nt < total) {
+          int lo = 0, hi = batch;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(cu_seqlens + mid) <= nt) lo = mid; else hi = mid - 1;
+          }
+          pos = int(nt - __ldg(cu_seqlens + lo));
+        }
+        pos_tab[t] = pos;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < 32 * ntok; e += kPassThreads)
+        cs_tab[e] = rope_cos_sin(pos_tab[e >> 5], f.hi[e & 31], f.lo[e & 31]);
+      __syncthreads();
+    }
+#pragma unroll
+    for (int u = 0; u < TPT; ++u) {
+      const int task = base + u * kPassThreads + threadIdx.x;
+      const int tok = task / (4 * hkv), h = (task >> 2) % hkv, c = task & 3;
+      const long n = n0 + tok;
+      if (task < ntask && n < total) {
+        const float2* cs = cs_tab + tok * 32;
+        const uint32_t xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+        const uint32_t ys[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+        uint32_t a[4], b[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 8 * c + 2 * e;
+          const float2 xv = unpack_bf16x2(xs[e]), yv = unpack_bf16x2(ys[e]);
+          const float2 cs0 = cs[i], cs1 = cs[i + 1];
+          const float a0 = xv.x * cs0.x - yv.x * cs0.y, a1 = xv.y * cs1.x - yv.y * cs1.y;
+          const float b0 = yv.x * cs0.x + xv.x * cs0.y, b1 = yv.y * cs1.x + xv.y * cs1.y;
+          if (fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))) > kF16Max)
+            overflow = true;
+          a[e] = pack_f16x2(a0, a1);
+          b[e] = pack_f16x2(b0, b1);
+        }
+        uint4* dst = k_rot + (n * hkv + h) * 8;
+        dst[c] = make_uint4(a[0], a[1], a[2], a[3]);
+        dst[c + 4] = make_uint4(b[0], b[1], b[2], b[3]);
+      }
     }
   }
   if (overflow) record_status(ctl, HATTN_ERR_INVALID_ARG);
@@ -229,10 +268,10 @@ cudaError_t launch_rope_keys_packed(const void* k, void* k_rot, const int* cu_se
                                     long total, int hkv, const RopeFreqs& f, const DeviceCtl& ctl,
                                     cudaStream_t s, unsigned int* unit_ctr, int pos_off) {
   if (total == 0) return cudaSuccess;
-  long blocks = (total + kTokWarps - 1) / kTokWarps;
-  const long cap_blocks = long(num_sms()) * 8;  // grid-stride beyond 8 blocks per SM
-  if (blocks > cap_blocks) blocks = cap_blocks;
-  rope_keys_packed_kernel<<<dim3(unsigned(blocks)), 256, 0, s>>>(
+  const int ntok = pass_tokens<kPassTasks>(hkv);
+  const long blocks = (total + ntok - 1) / ntok;
+  const size_t smem = size_t(ntok) * 32 * sizeof(float2);  // <= 32 KB
+  rope_keys_packed_kernel<kPassTasks><<<dim3(unsigned(blocks)), kPassThreads, smem, s>>>(
       static_cast<const uint4*>(k), static_cast<uint4*>(k_rot), cu_seqlens, batch, total, hkv, f,
       ctl, unit_ctr, pos_off);
   return cudaGetLastError();
