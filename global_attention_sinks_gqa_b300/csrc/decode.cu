@@ -75,7 +75,11 @@ constexpr int kItemReaders = 1 + 4;  // the MMA issuer and the four row warps
 struct Bars {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_ready[2], q_empty[2];
-  uint64_t s_full[2], p_full[2], pv_done, o_free, drain;
+  // pv_done: after every PV (the rescale of O waits for the previous
+  // block's); o_done: after an item's last PV (its epilogue waits on it:
+  // pv_done's parity could alias there, since the row warps reach the
+  // epilogue having seen only the PVs up to two blocks back complete)
+  uint64_t s_full[2], p_full[2], pv_done, o_done, o_free, drain;
   uint64_t item_full[kItemQueue], item_empty[kItemQueue];
   uint32_t tmem_base;
   int abort;
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[i], 128);
     }
     mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
     for (int i = 0; i < kItemQueue; ++i) {
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars->s_full[blk_global & 1u]);
         return true;
       };
-      auto issue_pv = [&](uint32_t blk_global, bool first) -> bool {
+      auto issue_pv = [&](uint32_t blk_global, bool first, bool last) -> bool {
         if (!mbar_wait(&bars->p_full[blk_global & 1u], (blk_global >> 1) & 1u, a.ctl, abort))
           return false;
         if (first && items > 0 && !mbar_wait(&bars->o_free, (items - 1) & 1u, a.ctl, abort))
@@ -327,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + kOCol, p + kk * 8, make_sdesc_sw128(vbase + kk * 2048, kBox, 1024),
                   idesc_o, (!first || kk > 0) ? 1u : 0u);
         umma_commit(&bars->pv_done);
+        if (last) umma_commit(&bars->o_done);  // the item's O is complete
         // (the stage is released by a softmax thread once S of block
         // blk_global + 2 is done: that QK^T was issued after this PV)
         return true;
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++qk;
             if (j + 2 == nb) umma_commit(&bars->q_empty[qb]);
           }
-          if (!issue_pv(b0 + j, j == 0)) { ok = false; break; }
+          if (!issue_pv(b0 + j, j == 0, j + 1 == nb)) { ok = false; break; }
           ++pv;
         }
         ++items;
@@ -380,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     auto epilogue = [&]() -> bool {
-      if (!warp_wait(&bars->pv_done, (blk - 1) & 1u, a.ctl, abort)) return false;
+      // the item's last PV (items: items finished, the previous one included)
+      if (!warp_wait(&bars->o_done, (items - 1) & 1u, a.ctl, abort)) return false;
       tc_fence_after();
       if (active) {
         const uint32_t t_o = tmem + lane_addr + kOCol;

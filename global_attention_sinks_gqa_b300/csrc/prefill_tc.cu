@@ -131,11 +131,13 @@ struct Cfg {
   // Several key blocks per unit: the slots form KST stages of one K block
   // (3 boxes each) and one stage of one V block (2 boxes, after them), each
   // stage with its own empty barrier (kv_empty[0..KST-1] for K, kv_empty[KST]
-  // for V); the blocks land on k0_full (K_0) or tile A's p_full (the rest).
+  // for V); the blocks land on k0_full[stage] (K_0) or tile A's p_full (the
+  // rest).
   // K_{j+1} can then load as soon as K_{j+1-KST} is released and P_A(j - 1)
   // is done, about a key block ahead of its S product.
   static constexpr int KST = (NSLOT - 2) / 3;
   static_assert(ONE || KST >= 2, "two K stages");
+  static_assert(KST <= 4, "one K_0 barrier per K stage");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
 
@@ -181,7 +183,10 @@ struct Bars {
   uint64_t q_full[2], q_ready[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
   uint64_t kv_full[NSLOT], kv_empty[NSLOT];
-  uint64_t k0_full;  // several key blocks per unit: K_0 of each unit
+  // several key blocks per unit: K_0 of each unit, one barrier per K stage
+  // (a unit of one block may start loading the next unit's K_0 before its
+  // own K_0 has landed; per stage, the stage's previous K_0 was consumed)
+  uint64_t k0_full[4];
   uint64_t unit_full[kUnitQueue], unit_empty[kUnitQueue];
   uint64_t drain;
   uint32_t tmem_base;
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->unit_full[i], 1);
       mbar_init(&bars->unit_empty[i], kUnitReaders);
     }
-    mbar_init(&bars->k0_full, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->k0_full[i], 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -535,27 +540,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kmap = [&](int i) { return i == 0 ? &mapK0 : &mapK12; };
       uint32_t un = 0;  // one-block units whose K and V were loaded
       // several key blocks per unit: whole K / V blocks into their stages.
-      // K_0 of a unit completes k0_full.  K_{j+1} and V_j instead complete
+      // K_0 of a unit completes k0_full of its stage.  K_{j+1} and V_j instead complete
       // phase j of tile A's p_full together with the softmax's P_A(j), so
       // that one wait of the MMA issuer covers PV_A(j) and S(j + 1).  Each
       // arrives (with its bytes) only once phase j - 1 is complete: K_{j+1}
       // waits for it here; V_j loads into a stage that PV_B(j - 1) released,
       // and PV_B(j - 1) was issued after that phase.  Phase j cannot complete
       // without these arrivals, so the parity waited on cannot alias.
-      uint32_t kq = 0, vq = 0;  // K and V blocks loaded (vq: p_full[0] phases joined)
-      uint32_t k0n = 0;         // phases of k0_full (units started)
+      uint32_t kq = 0, vq = 0;    // K and V blocks loaded (vq: p_full[0] phases joined)
+      uint32_t k0n[C::KST] = {};  // phases of k0_full[stage] (units whose K_0 went there)
       auto load_k = [&](const UnitInfo& ui, int kpos, bool first) -> bool {
         const uint32_t st = kq % C::KST, ph = (kq / C::KST) & 1u;
         if (!mbar_wait(&bars->kv_empty[st], ph ^ 1u, a.ctl, abort)) return false;
         if (!first && vq > 0 && !mbar_wait(&bars->p_full[0], (vq - 1) & 1u, a.ctl, abort))
           return false;
-        uint64_t* full = first ? &bars->k0_full : &bars->p_full[0];
+        uint64_t* full = first ? &bars->k0_full[st] : &bars->p_full[0];
         mbar_arrive_expect_tx(full, 3 * C::kSlot);
         for (int i = 0; i < 3; ++i)
           tma_load_3d(ring + (st * 3 + i) * C::kSlot, kmap(i), full, 64 * i, kv_c1(ui, kpos),
                       kv_c2(ui, kpos));
         ++kq;
-        if (first) ++k0n;
+        if (first) ++k0n[st];
         return true;
       };
       auto load_v = [&](const UnitInfo& ui, int vpos) -> bool {
@@ -653,7 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_drain(&bars->kv_full[1], (un - 1) & 1u, a.ctl);
         }
       } else {
-        if (k0n) mbar_wait_drain(&bars->k0_full, (k0n - 1) & 1u, a.ctl);
+        for (int st = 0; st < C::KST; ++st)
+          if (k0n[st]) mbar_wait_drain(&bars->k0_full[st], (k0n[st] - 1) & 1u, a.ctl);
         if (vq) mbar_wait_drain(&bars->p_full[0], (vq - 1) & 1u, a.ctl);
       }
     }
@@ -728,14 +734,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
       // K blocks in KST stages (the stage of the c-th K block is c % KST;
       // K stage s holds slots 3s .. 3s + 2), V blocks in one stage (slots
-      // 3 KST, 3 KST + 1).  This thread waits on K_0 of a unit (k0_full)
-      // and then, per key block j, only on P_A(j) -- whose barrier also
+      // 3 KST, 3 KST + 1).  This thread waits on K_0 of a unit (k0_full of
+      // its stage) and then, per key block j, only on P_A(j) -- whose barrier also
       // carries V_j and K_{j+1} -- and P_B(j); the softmax of tile B
       // releases each K stage once it has seen S_B of that block.  Every
       // wait and commit costs this thread hundreds of cycles while the
       // products stream operands out of shared memory, so it makes three
       // commits and two waits per block.
       uint32_t kc = 0;
+      uint32_t k0c[C::KST] = {};  // K_0 blocks taken from each K stage
       auto next_kslot = [&]() -> uint32_t {
         const uint32_t st = kc % C::KST;
         ++kc;
@@ -748,8 +755,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u < 0) break;
         UnitInfo ui;
         unit_info<G, BN, WIN>(u, a, cu, nut, ui);
-        if (!mbar_wait(&bars->k0_full, uc & 1u, a.ctl, abort)) break;
-        const uint32_t k0 = next_kslot();
+        const uint32_t k0 = next_kslot();  // slot of stage k0 / 3
+        if (!mbar_wait(&bars->k0_full[k0 / 3], k0c[k0 / 3] & 1u, a.ctl, abort)) break;
+        ++k0c[k0 / 3];
         for (int t = 0; t < 2 && ok; ++t) {
           if (!mbar_wait(&bars->q_ready[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
           tc_fence_after();

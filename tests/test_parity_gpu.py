@@ -102,6 +102,18 @@ def test_prefill_many_short_sequences(G):
     compare(out, lse, o_ref, l_ref, f"150 short sequences G={G}")
 
 
+@pytest.mark.parametrize("hkv,window,lens", [(96, 0, [130, 57]), (96, 128, [200]),
+                                              (520, 128, [70, 41])])
+def test_prefill_many_kv_heads(hkv, window, lens):
+    """G = 1 with many KV heads: the key-rotation pass packs whole tokens
+    into a block (96 heads: 5 tokens of 384 tasks; 520 heads: one token whose
+    2080 tasks take the block two rounds)."""
+    c = synth.prefill_case(lens, hkv, hkv, window=window, rope_base=1e4, seed=610 + hkv)
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"hkv {hkv} window {window}")
+
+
 @pytest.mark.parametrize("G,window", [(8, 128), (16, 128), (8, 64)])
 def test_prefill_window_max_jumps_late_in_band(G, window):
     """Each key is 0.8 x the query of its token's first head in the group, so
