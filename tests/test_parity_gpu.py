@@ -114,6 +114,21 @@ def test_prefill_many_kv_heads(hkv, window, lens):
     compare(out, lse, o_ref, l_ref, f"hkv {hkv} window {window}")
 
 
+@pytest.mark.parametrize("G,window", [(4, 64), (16, 0)])
+def test_prefill_many_units_per_cta(G, window):
+    """60 short sequences and 16 KV heads: every CTA runs a string of units
+    of one or two key blocks back to back (W = 64 at G = 4: 80-key blocks;
+    the global layer at G = 16), so the K_0 barriers of the K stages turn
+    over at every unit."""
+    rs = np.random.RandomState(1800 + G)
+    lens = [int(x) for x in rs.randint(1, 200, size=60)]
+    c = synth.prefill_case(lens, G * 16, 16, window=window, rope_base=1e4 if window else 5e6,
+                           seed=1800 + G)
+    out, lse = gpu_prefill(c)
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"many units per CTA G={G} W={window}")
+
+
 @pytest.mark.parametrize("G,window", [(8, 128), (16, 128), (8, 64)])
 def test_prefill_window_max_jumps_late_in_band(G, window):
     """Each key is 0.8 x the query of its token's first head in the group, so
@@ -236,6 +251,16 @@ def test_decode_ga_linear_multi_chunk(T, G):
     lens = [T, 64, 1023, 1024, 1025, 2048, 2049, 5000]  # 1 to 3 chunks of 2048
     d = synth.decode_case(lens, T, G * 2, 2, window=0, rope_base=5e6, seed=800 + T + G)
     _decode_compare(d, max(lens) + 3, False, f"ga T={T} G={G}")
+
+
+def test_decode_many_short_items():
+    """150 sequences of one to three 64-slot blocks, 16 KV heads: every CTA of
+    the split-KV kernel takes a run of short items back to back, so its K / V
+    stages and its per-item epilogue barrier turn over at every item."""
+    rs = np.random.RandomState(1700)
+    lens = [int(x) for x in rs.randint(2, 190, size=150)]
+    d = synth.decode_case(lens, 2, 4 * 16, 16, window=0, rope_base=5e6, seed=1700)
+    _decode_compare(d, 192, False, "many short items")
 
 
 @pytest.mark.parametrize("cap,window,T,lens", [
