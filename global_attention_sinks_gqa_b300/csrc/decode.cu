@@ -22,7 +22,9 @@
 // CTA roles (192 threads):
 //   warp 0      TMA producer: blocks of 64 cache slots (K: 3 boxes, V: 2 boxes
 //               of [64 slots][64 dims], 128-byte swizzle) into a 5-stage ring,
-//               running ahead across item boundaries.
+//               running ahead across item boundaries; a stage is released by a
+//               row thread once it has seen S of the block two later (that
+//               QK^T was issued after the block's PV).
 //   warp 1      TMEM allocator and single-thread MMA issuer:
 //                 S_j = Q K_j^T (M=128, N=64, K=192; Q from TMEM) into one of
 //                 two S buffers, O += P_j V_j (M=128, N=128, K=64, P from TMEM),
@@ -36,7 +38,8 @@
 //               bf16, lazy O rescaling, and the epilogue.  A single-chunk item
 //               finishes its rows (sink included); otherwise it writes
 //               (O / l, m + log2 l) and a merge kernel combines the chunks and
-//               the sink with one warp per output row.
+//               the sink with one warp per output row.  The epilogue waits on
+//               a barrier committed after the item's last PV (o_done).
 // TMEM: S_0 columns 0..63, S_1 64..127, O 128..255, Q buffers 256.. and 352..
 #include <math.h>
 

@@ -25,9 +25,12 @@
 //   warp 0      TMA producer: Q tiles (3 boxes of 64 dims each) and the key
 //               blocks, in slots of one [BN keys][64 dims] box (128-byte
 //               swizzle): a K block is 3 consecutive slots, a V block 2.
-//               Several blocks per unit: K in KST stages, V in one, each
-//               stage on one full / empty barrier pair, loaded K_0, K_1, V_0,
-//               K_2, V_1, ...  One block per unit: one K and one V stage whose
+//               Several blocks per unit: K in KST stages, V in one, loaded
+//               K_0, Q_A, Q_B, K_1, V_0, K_2, V_1, ...; K_0 lands on the K_0
+//               barrier of its stage, V_j and K_{j+1} on tile A's P barrier
+//               of block j (one wait of the MMA issuer covers both); the K
+//               stages are released by tile B's rows, the V stage by a
+//               commit.  One block per unit: one K and one V stage whose
 //               release (and that of the Q tiles) the producer reads from the
 //               phases of the S and PV completion barriers.
 //   warp 1      TMEM allocator and single-thread MMA issuer, per key block j:
@@ -36,7 +39,9 @@
 //               (S: M=128, N=BN, K=192 from shared memory; PV: P from TMEM,
 //               V from shared memory).  The tensor core runs them in issue
 //               order, so S_t may be rewritten right behind the PV reading P_t.
-//               (Two issuers, one per tile, measured slower.)
+//               (Two issuers, one per tile, measured slower: their products
+//               enter the pipe interleaved, both S complete together and the
+//               two softmaxes run while the pipe idles.)
 //   warps 2-3   idle (they complete warpgroup 0 for the register split)
 //   warps 4-7   tile A, one thread per query row (TMEM lane): RoPE of the Q
 //   warps 8-11  tile B  tile, masked online softmax in base 2 (running max
