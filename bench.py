@@ -387,7 +387,10 @@ def run_cuda(args, rank, world):
     # the step: inside the step every part runs under the SM clock the
     # power-capped global prefill leaves behind; alone, the short parts run
     # at their own clock.  The step's numbers above stay the reported ones.
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # twice the L2
+    # The flush (8 times the L2) also gives the host ~160 us to enqueue the
+    # part's calls before the GPU reaches the start event, so that the
+    # Python marshalling of short parts (five decode calls) is not timed.
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
 
     def alone(fn, reps):
         fn()
