@@ -224,6 +224,7 @@ hattn_status_t hattn_prefill(const void* q, const void* k, const void* v, const 
   if (launch_rope_keys_packed(k, workspace, cu_seqlens, batch, total_tokens, hkv, a.freqs, ctl, s,
                               a.unit_ctr) != cudaSuccess)
     return HATTN_ERR_CUDA;
+  a.after_pass = total_tokens > 0;  // the pass launched
   if (max_seqlen == 0) return HATTN_OK;
   if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;
   return HATTN_OK;
@@ -285,6 +286,7 @@ hattn_status_t hattn_prefill_shard(const void* q, const void* k, const void* v,
   if (launch_rope_keys_packed(k, workspace, nullptr, 1, total_k, hkv, a.freqs, ctl, s, a.unit_ctr,
                               a.rope_off) != cudaSuccess)
     return HATTN_ERR_CUDA;
+  a.after_pass = total_k > 0;  // the pass launched
   if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;
   return HATTN_OK;
 }
@@ -425,6 +427,7 @@ hattn_status_t hattn_prefill_cached(const void* q, const void* k_new, const void
   if (launch_kv_append_packed(k_new, v_new, cu_seqlens, prefix_lens, k_cache, v_cache, batch,
                               total_tokens, hkv, cap, a.freqs, ctl, a.unit_ctr, s) != cudaSuccess)
     return HATTN_ERR_CUDA;
+  a.after_pass = (total_tokens + batch) * long(hkv) > 0;  // the append launched
   if (max_seqlen == 0) return HATTN_OK;
   if (launch_prefill(a, s) != cudaSuccess) return HATTN_ERR_CUDA;
   return HATTN_OK;

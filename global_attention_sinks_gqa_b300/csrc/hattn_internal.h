@@ -100,6 +100,12 @@ struct PrefillArgs {
   long total_k = 0;  // 0: total
   int lead = 0;
   int rope_off = 0;
+  // The kernel just before on the stream is this call's key-rotation pass
+  // or append (itself launched in stream order), which writes only the
+  // rotated keys / caches, the work counter and the status word: the
+  // attention kernel may then start before it ends (programmatic dependent
+  // launch) and waits for it only before reading those.
+  bool after_pass = false;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 

@@ -554,7 +554,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // without these arrivals, so the parity waited on cannot alias.
       uint32_t kq = 0, vq = 0;    // K and V blocks loaded (vq: p_full[0] phases joined)
       uint32_t k0n[C::KST] = {};  // phases of k0_full[stage] (units whose K_0 went there)
+      // Launched as a dependent of the key-rotation (or append) kernel, this
+      // CTA may start before that kernel ends.  What it writes -- the rotated
+      // keys, the caches, the work counter -- is read only after the wait
+      // below, which this thread alone passes through; Q, the offsets and
+      // the sinks were complete before that kernel started.
+      bool dep = false;
+      auto dep_wait = [&]() {
+        if (!dep) {
+          grid_dep_wait();
+          dep = true;
+        }
+      };
       auto load_k = [&](const UnitInfo& ui, int kpos, bool first) -> bool {
+        dep_wait();
         const uint32_t st = kq % C::KST, ph = (kq / C::KST) & 1u;
         if (!mbar_wait(&bars->kv_empty[st], ph ^ 1u, a.ctl, abort)) return false;
         if (!first && vq > 0 && !mbar_wait(&bars->p_full[0], (vq - 1) & 1u, a.ctl, abort))
@@ -569,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto load_v = [&](const UnitInfo& ui, int vpos) -> bool {
+        dep_wait();
         if (!mbar_wait(&bars->kv_empty[C::KST], (vq & 1u) ^ 1u, a.ctl, abort)) return false;
         mbar_arrive_expect_tx(&bars->p_full[0], 2 * C::kSlot);
         for (int i = 0; i < 2; ++i)
@@ -584,10 +598,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pn >= uint32_t(kUnitQueue) &&
             !mbar_wait(&bars->unit_empty[q], ((pn / kUnitQueue) & 1u) ^ 1u, a.ctl, abort))
           break;
+        // The first unit of CTA i is unit i (its Q tiles load before the
+        // wait); the counter hands out the rest, from unit gridDim.x on.
         UnitInfo ui;
         int u;
+        bool fixed = pn == 0;
         do {
-          u = int(atomicAdd(a.unit_ctr, 1u));
+          if (fixed) {
+            u = int(blockIdx.x);
+            fixed = false;
+          } else {
+            dep_wait();
+            u = int(gridDim.x + atomicAdd(a.unit_ctr, 1u));
+          }
         } while (u < nunits && !unit_info<G, BN, WIN>(u, a, cu, nut, ui, true));
         if (u >= nunits) u = -1;
         bars->unit[q] = u;
@@ -600,7 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block: the Q tiles first -- a tile's buffer frees with its S MMA of
         // the previous unit and its RoPE heads the tile's next chain -- then
         // K_0, V_0.
-        if constexpr (!ONE) ok = load_k(ui, k0pos, true);
+        // (The CTA's first unit loads its Q tiles before K_0: they need no
+        // wait for the kernel before this one.)
+        const bool q_first = pn == 1;
+        if (!ONE && !q_first) ok = load_k(ui, k0pos, true);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -622,10 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ui.tok0 + ui.t0 + t * TQ);
           ++qf;
         }
+        if (!ONE && q_first && ok) ok = load_k(ui, k0pos, true);
         if constexpr (ONE) {
           // the unit's K block (slots 0-2) once the previous unit's S_B is
           // done, its V block (slots 3-4) once its PV_B is: the phases of
           // s_full[1] and pv_done[1] (products complete in issue order)
+          dep_wait();
           if (ok && un > 0)
             ok = mbar_wait(&bars->s_full[1], (un - 1) & 1u, a.ctl, abort);
           if (ok) {
@@ -879,20 +907,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       UnitInfo ui;
       unit_info<G, BN, WIN>(u, a, cu, nut, ui);
-      if (!warp_wait(&bars->q_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
       const int qmin = ui.P + ui.t0 + t * TQ;    // position of the tile's first token
       const int qpos = qmin + tl;
       const int qidx = qpos - ui.P;              // this row's index among the new tokens
       // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
       // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
       // The G lanes holding one token's heads each evaluate 32/G of the 32
-      // angles and exchange them by shuffles.
+      // angles (while the tile's Q is still loading) and exchange them by
+      // shuffles.
       {
         float2 cs_own[32 / G];
 #pragma unroll
         for (int k2 = 0; k2 < 32 / G; ++k2)
           cs_own[k2] = rope_cos_sin(qpos + a.rope_off, a.freqs.hi[hl + G * k2],
                                     a.freqs.lo[hl + G * k2]);
+        if (!warp_wait(&bars->q_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
         uint8_t* qrow = smem + C::kOffQ + t * C::kQBytes + r * 128;
         uint4 ch[8];
 #pragma unroll
@@ -1014,8 +1043,17 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   const long nunits = nut * a.batch * a.hkv;
   if (nunits == 0) return cudaSuccess;
   const int grid = int(nunits < num_sms() ? nunits : num_sms());
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk0, mk12, mv, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = a.after_pass ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk0, mk12, mv, a);
 }
 
 // Key blocks: a window unit whose band (W - 1 + 2*TQ keys) fits one block

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kPassThreads) rope_keys_packed_kernel(
     unsigned int* __restrict__ unit_ctr, int pos_off) {
   extern __shared__ float2 cs_tab[];  // [tokens of the block][32]
   __shared__ int pos_tab[kPassMaxTok];
+  grid_dep_launch();  // the attention kernel after this one may start its setup
   if (unit_ctr != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *unit_ctr = 0u;
   const int ntok = pass_tokens<TPT>(hkv);
   const long n0 = long(blockIdx.x) * ntok;
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(256) kv_append_packed_kernel(
     const int* __restrict__ cu_seqlens, const int* __restrict__ prefix,
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int batch, long total, int hkv,
     int cap, const RopeFreqs f, const DeviceCtl ctl, unsigned int* __restrict__ unit_ctr) {
+  grid_dep_launch();  // the attention kernel after this one may start its setup
   if (unit_ctr != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *unit_ctr = 0u;
   const int lane = threadIdx.x & 31;
   const long row = long(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);

@@ -118,12 +118,16 @@ def multi_block_prefill(units, seed, kst=2, shared_k0_barrier=False):
             kq += 1
 
         for n, nb in enumerate(units):
-            yield from load_k(n, 0, True)
+            # the CTA's first unit loads its Q tiles before K_0
+            if n > 0:
+                yield from load_k(n, 0, True)
             for t in range(2):
                 yield ("wait", q_empty[t], (qf[t] & 1) ^ 1)
                 q_full[t].arrive(tx=1, who="producer Q")
                 tma.append((("Q", t), ("Qraw", n, t), q_full[t]))
                 qf[t] += 1
+            if n == 0:
+                yield from load_k(n, 0, True)
             for j in range(nb):
                 if j + 1 < nb:
                     yield from load_k(n, j + 1, False)
