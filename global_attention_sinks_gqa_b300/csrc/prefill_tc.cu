@@ -141,6 +141,13 @@ struct Cfg {
   // K_{j+1} can then load as soon as K_{j+1-KST} is released and P_A(j - 1)
   // is done, about a key block ahead of its S product.
   static constexpr int KST = (NSLOT - 2) / 3;
+  // One block: the unit's band is TQ keys wider than either tile needs
+  // (W - 1 + TQ keys), so tile t multiplies only the NT keys from t * TOFF on
+  // when TQ is a whole number of 16-key steps; the band then starts at
+  // position t0 - W + 1 even where that is negative (those rows load as
+  // zeros and are masked), so that the offset stays TQ.
+  static constexpr int TOFF = (ONE && TQ % 16 == 0 && BN - TQ >= 16) ? TQ : 0;
+  static constexpr int NT = BN - TOFF;
   static_assert(ONE || KST >= 2, "two K stages");
   static_assert(KST <= 4, "one K_0 barrier per K stage");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
@@ -213,7 +220,7 @@ struct UnitInfo {
 // device-resident offsets (or prefix) are out of range; `report` records
 // the latter as HATTN_ERR_INVALID_ARG (the producer, which sees every unit
 // once, reports).
-template <int G, int BN, bool WIN>
+template <int G, int BN, bool WIN, bool UNCLAMPED = false>
 __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, const int* cu, int nut,
                                           UnitInfo& ui, bool report = false) {
   constexpr int UT = 256 / G;
@@ -232,7 +239,8 @@ __device__ __forceinline__ bool unit_info(int u, const PrefillArgs& a, const int
     return false;
   }
   const int qend = ui.P + min(ui.t0 + UT, ui.L);  // one past the last valid query position
-  ui.kstart = WIN ? max(0, ui.P + ui.t0 - a.window + 1) : 0;
+  ui.kstart = WIN ? (UNCLAMPED ? ui.P + ui.t0 - a.window + 1 : max(0, ui.P + ui.t0 - a.window + 1))
+                  : 0;
   ui.nblk = (qend - ui.kstart + BN - 1) / BN;
   return true;
 }
@@ -611,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dep_wait();
             u = int(gridDim.x + atomicAdd(a.unit_ctr, 1u));
           }
-        } while (u < nunits && !unit_info<G, BN, WIN>(u, a, cu, nut, ui, true));
+        } while (u < nunits && !unit_info<G, BN, WIN, (C::TOFF > 0)>(u, a, cu, nut, ui, true));
         if (u >= nunits) u = -1;
         bars->unit[q] = u;
         mbar_arrive(&bars->unit_full[q]);
@@ -699,8 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_rot = make_idesc_f16(128, BN, 0, 0);   // dims 0..63
-      constexpr uint32_t idesc_s = make_idesc_bf16(128, BN, 0, 0);    // dims 64..191
+      constexpr uint32_t idesc_rot = make_idesc_f16(128, C::NT, 0, 0);   // dims 0..63
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, C::NT, 0, 0);    // dims 64..191
       constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, 0, 1);
       const uint32_t qbase = smem_u32(smem + C::kOffQ);
       const uint32_t rbase = smem_u32(ring);
@@ -715,9 +723,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vdesc0 = make_sdesc_sw128(rbase, C::kSlot, 1024);
       // a K block sits in 3 consecutive slots from kslot, a V block in 2 from
       // vslot (dims 0..63 then 64..127: one N=128 MMA per k-step spans both)
+      // (tile t's keys start TOFF * t rows into the block: whole 8-row
+      // swizzle atoms, 16-key steps)
       auto issue_qk = [&](int t, uint32_t kslot) {
         const uint64_t qd = qdesc0 + uint64_t((t * C::kQBytes) >> 4);
-        const uint64_t kd = kdesc0 + uint64_t((kslot * C::kSlot) >> 4);
+        const uint64_t kd = kdesc0 + uint64_t((kslot * C::kSlot + t * C::TOFF * 128) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 12; ++kk)
           umma_ss(tmem + s_col<ONE>(t), qd + uint64_t(((kk >> 2) * C::kQBox + (kk & 3) * 32) >> 4),
@@ -728,8 +738,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t vd = vdesc0 + uint64_t((vslot * C::kSlot) >> 4);
         const uint32_t p_tmem = tmem + s_col<ONE>(t);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_ts(tmem + o_col<ONE>(t), p_tmem + kk * 8, vd + uint64_t((kk * 2048) >> 4), idesc_o,
+        for (int kk = 0; kk < C::NT / 16; ++kk)
+          umma_ts(tmem + o_col<ONE>(t), p_tmem + kk * 8,
+                  vd + uint64_t(((t * C::TOFF + 16 * kk) * 128) >> 4), idesc_o,
                   (acc || kk > 0) ? 1u : 0u);
       };
       if constexpr (ONE) {
@@ -787,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = read_unit(rn, false);
         if (u < 0) break;
         UnitInfo ui;
-        unit_info<G, BN, WIN>(u, a, cu, nut, ui);
+        unit_info<G, BN, WIN, (C::TOFF > 0)>(u, a, cu, nut, ui);
         const uint32_t k0 = next_kslot();  // slot of stage k0 / 3
         if (!mbar_wait(&bars->k0_full[k0 / 3], k0c[k0 / 3] & 1u, a.ctl, abort)) break;
         ++k0c[k0 / 3];
@@ -906,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       UnitInfo ui;
-      unit_info<G, BN, WIN>(u, a, cu, nut, ui);
+      unit_info<G, BN, WIN, (C::TOFF > 0)>(u, a, cu, nut, ui);
       const int qmin = ui.P + ui.t0 + t * TQ;    // position of the tile's first token
       const int qpos = qmin + tl;
       const int qidx = qpos - ui.P;              // this row's index among the new tokens
@@ -960,9 +971,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (ONE) {
         if (!warp_wait(&bars->s_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
         tc_fence_after();
-        const int kb = ui.kstart;  // position of column 0
-        softmax_one<BN>(t_s, a.scale_log2, qpos - a.window + 1 - kb, qpos - kb,
-                        qmax - a.window + 1 - kb, qmin - kb, m, l);
+        const int kb = ui.kstart + t * C::TOFF;  // position of column 0 (may be < 0)
+        // the window's far edge, and position 0 where the band starts before it
+        const int lo = max(qpos - a.window + 1, 0), lo_max = max(qmax - a.window + 1, 0);
+        softmax_one<C::NT>(t_s, a.scale_log2, lo - kb, qpos - kb, lo_max - kb, qmin - kb, m, l);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
