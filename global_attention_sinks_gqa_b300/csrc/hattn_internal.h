@@ -106,6 +106,7 @@ struct PrefillArgs {
   // attention kernel may then start before it ends (programmatic dependent
   // launch) and waits for it only before reading those.
   bool after_pass = false;
+  bool o_tma = false;  // set by the launcher: O may leave by TMA stores
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 

@@ -48,7 +48,12 @@
 //               exact after the first block, then moved only when it grows
 //               by more than 2^8, with O rescaled then), P written back to
 //               TMEM as bf16 over the consumed S columns, and the epilogue,
-//               which folds in the sink: O 2^m / (2^m l + 2^s).
+//               which folds in the sink: O 2^m / (2^m l + 2^s).  One-block
+//               units with all rows valid stage O in shared memory (64-byte
+//               swizzled quarters of the head dim: tile A's in the V stage
+//               once PV_B is done, tile B's in the spare slots) and one
+//               thread per tile stores it by TMA: a quarter of the L1
+//               transactions of row-per-thread stores.
 // TMEM: S_A 0.., S_B 128.., O_A 256..383, O_B 384..511 (several key blocks
 // per unit), or S_A 0.., O_A 128..255, S_B 256.., O_B 384..511 (one block).
 #include <cudaTypedefs.h>
@@ -84,6 +89,22 @@ bool make_map(CUtensorMap* m, const void* base, long rows, int heads, int dim, i
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map for TMA stores of O [rows, heads, 128] bf16 in quarters of the head
+// dim: a 32-element (64-byte) inner box of box_heads x box_rows, 64-byte
+// swizzle.
+static bool make_out_map(CUtensorMap* m, void* base, long rows, int heads, int box_heads,
+                         int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cuuint64_t(kDv), cuuint64_t(heads), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(kDv) * 2, cuuint64_t(kDv) * 2 * heads};
+  cuuint32_t box[3] = {32, cuuint32_t(box_heads), cuuint32_t(box_rows)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int num_sms() {
@@ -128,7 +149,26 @@ struct Cfg {
   static constexpr int kMaxSmem = 232448;
   static constexpr int NSLOT = (kMaxSmem - 1024 - kBarBytes - kOffRing) / kSlot;
   static constexpr int kOffBar = kOffRing + NSLOT * kSlot;
-  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  // One block: O leaves by TMA stores, staged in 8 KB quarters (128 rows x
+  // 32 dims, 64-byte swizzle).  Tile A's four go to the V stage (free once
+  // PV_B of the unit is done; the next V block waits for their reads), tile
+  // B's to the spare ring slots and the space past the barrier block -- as
+  // many as fit (kBAreas); the rest of its row is stored directly.
+  static constexpr int kOArea = 8192;
+  static constexpr int kVOff = kOffRing + 3 * kSlot;
+  static constexpr int kSpareOff = kOffRing + 5 * kSlot;
+  static constexpr int kSpareAreas = NSLOT > 5 ? (NSLOT - 5) * kSlot / kOArea : 0;
+  static constexpr int kFreeOff = kOffBar + kBarBytes;
+  static constexpr int kFreeAreas = (kMaxSmem - 1024 - kFreeOff) / kOArea;
+  static constexpr int kBAreas =
+      kSpareAreas + kFreeAreas < 4 ? kSpareAreas + kFreeAreas : 4;
+  static constexpr int kFreeUsed = kBAreas > kSpareAreas ? kBAreas - kSpareAreas : 0;
+  static constexpr int kSmemBytes =
+      (ONE ? kFreeOff + kFreeUsed * kOArea : kOffBar + kBarBytes) + 1024;  // + alignment slack
+  __host__ __device__ static constexpr int o_area(int t, int q) {
+    return t == 0 ? kVOff + q * kOArea
+                  : (q < kSpareAreas ? kSpareOff + q * kOArea : kFreeOff + (q - kSpareAreas) * kOArea);
+  }
   static constexpr uint32_t kTmemCols = 512;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= (ONE ? 256 : 128), "BN");
   static_assert(kSlot % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
@@ -151,6 +191,8 @@ struct Cfg {
   static_assert(ONE || KST >= 2, "two K stages");
   static_assert(KST <= 4, "one K_0 barrier per K stage");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory");
+  static_assert(!ONE || 2 * kSlot >= 4 * kOArea, "tile A's O quarters fit the V stage");
+  static_assert(kSlot % 1024 == 0 && kFreeOff % 1024 == 0, "staging areas 1 KB aligned");
 };
 
 // TMEM columns of tile t.  Blocks of <= 128 keys: S_A 0, S_B 128, O_A 256,
@@ -199,6 +241,9 @@ struct Bars {
   // (a unit of one block may start loading the next unit's K_0 before its
   // own K_0 has landed; per stage, the stage's previous K_0 was consumed)
   uint64_t k0_full[4];
+  // one block per unit: tile t's O quarters are staged (128 rows), and tile
+  // A's TMA stores have read theirs out of the V stage
+  uint64_t o_staged[2], o_read;
   uint64_t unit_full[kUnitQueue], unit_empty[kUnitQueue];
   uint64_t drain;
   uint32_t tmem_base;
@@ -450,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mapQ,
                    const __grid_constant__ CUtensorMap mapK0,
                    const __grid_constant__ CUtensorMap mapK12,
-                   const __grid_constant__ CUtensorMap mapV, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap mapV,
+                   const __grid_constant__ CUtensorMap mapO, const PrefillArgs a) {
   using C = Cfg<G, BN, ONE>;
   constexpr int TQ = C::TQ;
   constexpr int NSLOT = C::NSLOT;
@@ -487,6 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->unit_empty[i], kUnitReaders);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars->k0_full[i], 1);
+    for (int t = 0; t < 2; ++t) mbar_init(&bars->o_staged[t], 128);
+    mbar_init(&bars->o_read, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     mbar_fence_init();
@@ -496,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&mapK0);
     tma_prefetch_map(&mapK12);
     tma_prefetch_map(&mapV);
+    if (ONE && a.o_tma) tma_prefetch_map(&mapO);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
@@ -670,8 +719,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(ring + i * C::kSlot, kmap(i), &bars->kv_full[0], 64 * i,
                           kv_c1(ui, k0pos), kv_c2(ui, k0pos));
           }
+          // (and once tile A's TMA stores of the previous unit's O have read
+          // their staging out of the V stage)
           if (ok && un > 0)
-            ok = mbar_wait(&bars->pv_done[1], (un - 1) & 1u, a.ctl, abort);
+            ok = mbar_wait(&bars->pv_done[1], (un - 1) & 1u, a.ctl, abort) &&
+                 mbar_wait(&bars->o_read, (un - 1) & 1u, a.ctl, abort);
           if (ok) {
             mbar_arrive_expect_tx(&bars->kv_full[1], 2 * C::kSlot);
             for (int i = 0; i < 2; ++i)
@@ -858,6 +910,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float pm = 0.f, pl = 0.f, psink = 0.f;
     bool pvalid = false;
     long porow = 0;
+    // one block per unit: the tile's first token row and head, and whether
+    // all its rows are valid (then O leaves by TMA)
+    int ptok = 0, pgh = 0;
+    bool pfull = false;
+    uint32_t nstaged = 0;  // epilogues of this tile that staged O (phases of o_staged[t])
     uint32_t puc = 0;  // index of the unit the epilogue finishes
 
     const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
@@ -892,6 +949,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free[t]);
+      if constexpr (ONE) {
+        if (a.o_tma && pfull) {
+          // Tile A stages into the V stage, which PV_B of the unit must
+          // have finished reading.  16-byte chunk c of row r's quarter sits
+          // at c ^ (r / 2 % 4) (64-byte swizzle: conflict-free).
+          if (t == 0 && !warp_wait(&bars->pv_done[1], puc & 1u, a.ctl, abort)) return false;
+          const int nq = t == 0 ? 4 : C::kBAreas;
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            if (qd < nq) {
+              uint8_t* row = smem + C::o_area(t, qd) + r * 64;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(row + ((c ^ ((r >> 1) & 3)) << 4)) =
+                    make_uint4(pk[16 * qd + 4 * c], pk[16 * qd + 4 * c + 1],
+                               pk[16 * qd + 4 * c + 2], pk[16 * qd + 4 * c + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->o_staged[t]);
+          // the quarters that found no staging area: stored directly
+          uint8_t* dst = static_cast<uint8_t*>(a.out) + porow * 256;
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd)
+            if (qd >= nq) {
+              if (out32) {
+                st_global_v8(dst + 64 * qd, pk + 16 * qd);
+                st_global_v8(dst + 64 * qd + 32, pk + 16 * qd + 8);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  reinterpret_cast<uint4*>(dst + 64 * qd)[e] =
+                      make_uint4(pk[16 * qd + 4 * e], pk[16 * qd + 4 * e + 1],
+                                 pk[16 * qd + 4 * e + 2], pk[16 * qd + 4 * e + 3]);
+              }
+            }
+          // one thread of the tile stores the staged boxes once all 128
+          // rows are in, and (tile A) reports when they have been read
+          bool good = true;
+          if (r == 0) {
+            good = mbar_wait(&bars->o_staged[t], nstaged & 1u, a.ctl, abort);
+            if (good) {
+              for (int qd = 0; qd < nq; ++qd)
+                tma_store_3d(&mapO, smem + C::o_area(t, qd), 32 * qd, pgh, ptok);
+              bulk_commit();
+              bulk_wait_read();
+              if (t == 0) mbar_arrive(&bars->o_read);
+            }
+          }
+          ++nstaged;
+          if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+          if (a.lse != nullptr) a.lse[porow] = (msub + log2f(l_tot)) * kLn2;
+          return true;
+        }
+        if (t == 0 && r == 0) mbar_arrive(&bars->o_read);  // nothing staged
+      }
       if (pvalid) {
         uint8_t* dst = static_cast<uint8_t*>(a.out) + porow * 256;
         if (out32) {  // 32-byte stores: one full sector each
@@ -1009,10 +1122,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       psink = sink_l2;
       pvalid = qidx < ui.L;
       porow = long(ui.tok0 + qidx) * a.hq + h;
+      ptok = ui.tok0 + ui.t0 + t * TQ;
+      pgh = ui.g * G;
+      pfull = ui.t0 + (t + 1) * TQ <= ui.L;
       puc = uc;
       ++uc;
     }
     if (ok && have_prev) epilogue();
+    // the TMA stores of O complete before the CTA's shared memory goes
+    if (ONE && r == 0) bulk_wait_all();
   }
 
   __syncthreads();
@@ -1025,7 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int G, int BN, bool WIN, bool ONE>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   using C = Cfg<G, BN, ONE>;
-  CUtensorMap mq, mk0, mk12, mv;
+  CUtensorMap mq, mk0, mk12, mv, mo;
   const bool cached = a.prefix != nullptr;
   // packed: rotated dims [total_k, hkv, 64] and raw keys [total_k, hkv, 192];
   // cached: both from the cache [batch * hkv, cap, 192]
@@ -1038,6 +1156,10 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
       !(cached ? make_map(&mv, a.v, long(a.batch) * a.hkv, a.cap, kDv, BN, 1)
                : make_map(&mv, a.v, kr, a.hkv, kDv, 1, BN)))
     return cudaErrorInvalidValue;
+  PrefillArgs a2 = a;
+  // O by TMA stores where the output's layout allows a map (16-byte base)
+  a2.o_tma = ONE && make_out_map(&mo, a.out, a.total, a.hq, G, C::TQ);
+  if (!a2.o_tma) mo = mq;  // unused
   auto kern = prefill_kernel<G, BN, WIN, ONE>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1065,7 +1187,7 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = a.after_pass ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mq, mk0, mk12, mv, a);
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk0, mk12, mv, mo, a2);
 }
 
 // Key blocks: a window unit whose band (W - 1 + 2*TQ keys) fits one block

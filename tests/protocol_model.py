@@ -49,8 +49,9 @@ class Bar:
 
 
 def _schedule(rnd, actors, fifo, tma, on_mma, on_land, max_steps=200000):
-    """Run the role generators (each yields ("wait", bar, parity)) with the
-    tensor-core queue `fifo` and the in-flight copies `tma` until all end."""
+    """Run the role generators (each yields ("wait", bar, parity) or
+    ("step",)) with the tensor-core queue `fifo` and the in-flight copies
+    `tma` until all end."""
     waiting = {k: None for k in actors}
     alive = set(actors)
     steps = 0
@@ -70,7 +71,9 @@ def _schedule(rnd, actors, fifo, tma, on_mma, on_land, max_steps=200000):
         kind, a = rnd.choice(choices)
         if kind == "role":
             try:
-                waiting[a] = next(actors[a])
+                w = next(actors[a])
+                # ("step",): a point where other actors may run in between
+                waiting[a] = None if w[0] == "step" else w
             except StopIteration:
                 alive.discard(a)
                 waiting[a] = None
@@ -227,10 +230,13 @@ def multi_block_prefill(units, seed, kst=2, shared_k0_barrier=False):
               fifo, tma, on_mma, on_land)
 
 
-def one_block_prefill(nunits, seed):
+def one_block_prefill(nunits, seed, stage_a_after_own_pv=False, v_without_o_read=False):
     """Window units whose key band is one block: Q_t, K and V are released
     through the phases of S_t, S_B and PV_B; O_t sits over S_t's upper TMEM
-    columns, so the next S_t waits until the epilogue has read O_t."""
+    columns, so the next S_t waits until the epilogue has read O_t.  Tile A's
+    epilogue stages O in the V stage once PV_B of the unit is done, and the
+    next V block loads once that staging has been read (o_read).  Planted
+    mistakes: tile A staging after its own PV only; V loaded without o_read."""
     rnd = random.Random(seed)
     q_full = [Bar(f"q_full{t}", 1) for t in range(2)]
     q_ready = [Bar(f"q_ready{t}", 1) for t in range(2)]
@@ -239,7 +245,9 @@ def one_block_prefill(nunits, seed):
     pv_done = [Bar(f"pv_done{t}", 1) for t in range(2)]
     o_free = [Bar(f"o_free{t}", 1) for t in range(2)]
     kv_full = [Bar("kv_full0", 1), Bar("kv_full1", 1)]
+    o_read = Bar("o_read", 1)
     smem, tm, tma, fifo = {}, {}, [], []
+    pv_ran = {}  # (tile, unit) -> True once that PV has executed
 
     def producer():
         qf = [0, 0]
@@ -256,6 +264,8 @@ def one_block_prefill(nunits, seed):
             tma.append((("K",), ("K", n), kv_full[0]))
             if n > 0:
                 yield ("wait", pv_done[1], (n - 1) & 1)
+                if not v_without_o_read:
+                    yield ("wait", o_read, (n - 1) & 1)
             kv_full[1].arrive(tx=1)
             tma.append((("V",), ("V", n), kv_full[1]))
 
@@ -282,18 +292,31 @@ def one_block_prefill(nunits, seed):
             smem[("Q", t)] = ("Qrot", n)
             q_ready[t].arrive()
             if prev is not None:
-                yield ("wait", pv_done[t], prev & 1)
-                assert tm.get(("up", t)) == ("O", prev), f"epilogue read {tm.get(('up', t))}"
-                tm[("up", t)] = ("Oread", prev)
-                o_free[t].arrive()
+                yield from epilogue(t, prev)
             yield ("wait", s_full[t], n & 1)
             assert tm.get(("lo", t)) == ("S", n), f"softmax read {tm.get(('lo', t))}"
             tm[("lo", t)] = ("P", n)
             p_full[t].arrive()
             prev = n
         if prev is not None:
-            yield ("wait", pv_done[t], prev & 1)
-            assert tm.get(("up", t)) == ("O", prev)
+            yield from epilogue(t, prev)
+
+    def epilogue(t, n):
+        yield ("wait", pv_done[t], n & 1)
+        assert tm.get(("up", t)) == ("O", n), f"epilogue read {tm.get(('up', t))}"
+        tm[("up", t)] = ("Oread", n)
+        o_free[t].arrive()
+        if t == 0:
+            # stage into the V stage; the TMA stores read it out, then o_read
+            if not stage_a_after_own_pv:
+                yield ("wait", pv_done[1], n & 1)
+            if not pv_ran.get((1, n)):
+                raise RuntimeError(f"tile A stages O of unit {n} over V while PV_B still reads it")
+            smem[("V",)] = ("staged", n)
+            yield ("step",)
+            if smem.get(("V",)) != ("staged", n):
+                raise RuntimeError(f"V block landed over tile A's staged O of unit {n}")
+            o_read.arrive()
 
     def on_mma(op):
         _, t, n = op
@@ -308,6 +331,7 @@ def one_block_prefill(nunits, seed):
             if tm.get(("lo", t)) != ("P", n) or smem.get(("V",)) != ("V", n):
                 raise RuntimeError(f"PV_{t} of unit {n} reads P {tm.get(('lo', t))}, V {smem.get(('V',))}")
             tm[("up", t)] = ("O", n)
+            pv_ran[(t, n)] = True
 
     def on_land(copy):
         key, lab, b = copy

@@ -114,12 +114,13 @@ def test_prefill_many_kv_heads(hkv, window, lens):
     compare(out, lse, o_ref, l_ref, f"hkv {hkv} window {window}")
 
 
-@pytest.mark.parametrize("G,window", [(4, 64), (16, 0)])
+@pytest.mark.parametrize("G,window", [(4, 64), (16, 0), (8, 128), (16, 128)])
 def test_prefill_many_units_per_cta(G, window):
     """60 short sequences and 16 KV heads: every CTA runs a string of units
     of one or two key blocks back to back (W = 64 at G = 4: 80-key blocks;
     the global layer at G = 16), so the K_0 barriers of the K stages turn
-    over at every unit."""
+    over at every unit; at W = 128 (one-block units) full and ragged tiles
+    alternate, so O leaves by TMA stores and by direct stores in turn."""
     rs = np.random.RandomState(1800 + G)
     lens = [int(x) for x in rs.randint(1, 200, size=60)]
     c = synth.prefill_case(lens, G * 16, 16, window=window, rope_base=1e4 if window else 5e6,
@@ -127,6 +128,28 @@ def test_prefill_many_units_per_cta(G, window):
     out, lse = gpu_prefill(c)
     o_ref, l_ref = oracle_prefill(c)
     compare(out, lse, o_ref, l_ref, f"many units per CTA G={G} W={window}")
+
+
+@pytest.mark.parametrize("G", [8, 16])
+def test_prefill_output_at_16_byte_offset(G):
+    """out 16- but not 32-byte aligned, inside a NaN-filled buffer: the O
+    quarters stored by TMA and those stored directly (16-byte stores then)
+    land in place, and nothing outside out is written."""
+    c = synth.prefill_case([700, 333], 8 * G, 8, window=128, rope_base=1e4, seed=670 + G)
+    dev = torch.device("cuda")
+    n = c.q.shape[0] * c.q.shape[1] * 128
+    buf = torch.full((n + 8 + 64,), float("nan"), dtype=torch.bfloat16, device=dev)
+    out = buf[8:8 + n].view(c.q.shape[0], c.q.shape[1], 128)
+    assert out.data_ptr() % 32 == 16
+    lse = torch.empty(c.q.shape[0], c.q.shape[1], dtype=torch.float32, device=dev)
+    ha.prefill(c.q.to(dev), c.k.to(dev), c.v.to(dev), c.sink.to(dev), c.cu_seqlens.to(dev),
+               max_seqlen=c.max_seqlen, window=c.window, rope_base=c.rope_base,
+               softmax_scale=c.scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    ha.check_device_status()
+    assert torch.isnan(buf[:8]).all() and torch.isnan(buf[8 + n:]).all()
+    o_ref, l_ref = oracle_prefill(c)
+    compare(out, lse, o_ref, l_ref, f"out at a 16-byte offset G={G}")
 
 
 @pytest.mark.parametrize("G,window", [(8, 128), (16, 128), (8, 64)])

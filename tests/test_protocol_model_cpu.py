@@ -2,9 +2,10 @@
 
 Each protocol runs over a few hundred random interleavings of its roles, TMA
 copies and tensor-core products; none may take an arrival beyond a barrier's
-count, read a buffer's wrong contents or deadlock.  Two planted mistakes --
-protocols that an earlier version of the kernels had -- must be caught, which
-shows the models can fail.
+count, read a buffer's wrong contents or deadlock.  Planted mistakes --
+protocols that an earlier version of the kernels had, or that the staging of
+O would have without its waits -- must be caught, which shows the models can
+fail.
 """
 import random
 
@@ -44,6 +45,19 @@ def test_multi_block_prefill_catches_one_k0_barrier_for_all_units():
 def test_one_block_prefill_protocol(nunits):
     for seed in range(150):
         pm.one_block_prefill(nunits, seed)
+
+
+@pytest.mark.parametrize("mistake", ["stage_a_after_own_pv", "v_without_o_read"])
+def test_one_block_prefill_catches_staging_mistakes(mistake):
+    # tile A staging O into the V stage before PV_B has read it, or the next
+    # V block loaded before the staged O has been read out
+    failures = 0
+    for seed in range(200):
+        try:
+            pm.one_block_prefill(4, seed, **{mistake: True})
+        except (AssertionError, RuntimeError):
+            failures += 1
+    assert failures > 0
 
 
 def test_split_kv_decode_protocol():
