@@ -145,7 +145,7 @@ struct Cfg {
   static constexpr int kSlot = BN * 128;            // [BN keys][64 dims] bf16
   static constexpr int kOffQ = 0;
   static constexpr int kOffRing = 2 * kQBytes;
-  static constexpr int kBarBytes = 1024;
+  static constexpr int kBarBytes = 2048;
   static constexpr int kMaxSmem = 232448;
   static constexpr int NSLOT = (kMaxSmem - 1024 - kBarBytes - kOffRing) / kSlot;
   static constexpr int kOffBar = kOffRing + NSLOT * kSlot;
@@ -232,6 +232,13 @@ constexpr int kCuCache = 128;  // batches up to 127 sequences keep cu_seqlens in
 constexpr int kUnitQueue = 4;          // units the producer may publish ahead
 constexpr int kUnitReaders = 1 + 8;    // the MMA issuer and the eight softmax warps
 
+// t0: index of the unit's first query among its sequence's new tokens; P:
+// positions before them (the cached prefix; 0 for a plain prefill); key and
+// query positions (kstart, masks, RoPE) count from the sequence's start.
+struct UnitInfo {
+  int b, g, t0, L, tok0, kstart, nblk, P;
+};
+
 template <int NSLOT>
 struct Bars {
   uint64_t q_full[2], q_ready[2], q_empty[2];
@@ -248,15 +255,9 @@ struct Bars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int unit[kUnitQueue];  // published unit indices, -1: no more
+  int unit[kUnitQueue];         // published unit indices, -1: no more
+  UnitInfo uinfo[kUnitQueue];  // and what unit_info() gave for them
   int cu[kCuCache];
-};
-
-// t0: index of the unit's first query among its sequence's new tokens; P:
-// positions before them (the cached prefix; 0 for a plain prefill); key and
-// query positions (kstart, masks, RoPE) count from the sequence's start.
-struct UnitInfo {
-  int b, g, t0, L, tok0, kstart, nblk, P;
 };
 
 // Unit u of the persistent loop.  Global units run latest (longest) first so
@@ -308,6 +309,34 @@ __device__ __forceinline__ void mask_block(uint32_t (&s)[BN], bool lower, bool u
 #pragma unroll
     for (int c = 0; c < BN; ++c)
       if (c > c_hi) s[c] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Masks of a whole one-block band: columns c < c_lo or c > c_hi of this row
+// become -inf, checked only in the 16-column chunks that some row of the tile
+// loses a column in (lo_max: the largest c_lo of the tile, hi_min: the
+// smallest c_hi).  The chunk tests are the same for every row, so the warps
+// do not diverge; a window tile then checks about 32 of its columns.
+template <int N>
+__device__ __forceinline__ void mask_band(uint32_t (&s)[N], int c_lo, int c_hi, int lo_max,
+                                          int hi_min) {
+  static_assert(N % 16 == 0, "16-column chunks");
+#pragma unroll
+  for (int c0 = 0; c0 < N; c0 += 16) {
+    const bool lo = c0 < lo_max, hi = c0 + 15 > hi_min;
+    if (lo && hi) {
+#pragma unroll
+      for (int c = c0; c < c0 + 16; ++c)
+        if (c < c_lo || c > c_hi) s[c] = __float_as_uint(-INFINITY);
+    } else if (lo) {
+#pragma unroll
+      for (int c = c0; c < c0 + 16; ++c)
+        if (c < c_lo) s[c] = __float_as_uint(-INFINITY);
+    } else if (hi) {
+#pragma unroll
+      for (int c = c0; c < c0 + 16; ++c)
+        if (c > c_hi) s[c] = __float_as_uint(-INFINITY);
+    }
   }
 }
 
@@ -441,13 +470,11 @@ __device__ __forceinline__ void softmax_one(uint32_t t_s, float scale_log2, int 
                                             int lo_max, int hi_min, float& m, float& l) {
   constexpr int H1 = ((BN / 2 + 15) / 16) * 16;
   constexpr int H2 = BN - H1;
-  const bool lower1 = lo_max > 0, upper1 = hi_min < H1 - 1;
-  const bool lower2 = lo_max > H1, upper2 = hi_min < BN - 1;
   float l1;
   {
     uint32_t s1[H1];
     load_s_row<H1>(t_s, s1);
-    mask_block<H1>(s1, lower1, upper1, c_lo, c_hi);
+    mask_band<H1>(s1, c_lo, c_hi, lo_max, hi_min);
     m = row_max<H1>(s1) * scale_log2;
     l1 = exp_pack_store<H1>(s1, scale_log2, m == -INFINITY ? 0.f : m, t_s);
   }
@@ -456,7 +483,7 @@ __device__ __forceinline__ void softmax_one(uint32_t t_s, float scale_log2, int 
   {
     uint32_t s2[H2];
     load_s_row<H2>(t_s + H1, s2);
-    mask_block<H2>(s2, lower2, upper2, c_lo - H1, c_hi - H1);
+    mask_band<H2>(s2, c_lo - H1, c_hi - H1, lo_max - H1, hi_min - H1);
     const float m2 = fmaxf(m, row_max<H2>(s2) * scale_log2);
     redo = m2 > m + kRescaleThreshold;
     if (redo) {
@@ -568,14 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int* cu = cu_cached ? bars->cu : a.cu_seqlens;
   // Units are handed out by a counter in global memory, so SMs that run
   // faster take more of them; the producer draws each unit and publishes its
-  // index in a small queue that the MMA issuer and the softmax warps read in
-  // the same order (-1: no more units).  n: queue entries read so far.
-  auto read_unit = [&](uint32_t& n, bool whole_warp) -> int {
+  // index and its UnitInfo in a small queue that the MMA issuer and the
+  // softmax warps read in the same order (-1: no more units).  n: queue
+  // entries read so far; ui (when given): the unit's UnitInfo.
+  auto read_unit = [&](uint32_t& n, bool whole_warp, UnitInfo* ui = nullptr) -> int {
     const uint32_t q = n % kUnitQueue, ph = (n / kUnitQueue) & 1u;
     const bool ok = whole_warp ? warp_wait(&bars->unit_full[q], ph, a.ctl, abort)
                                : mbar_wait(&bars->unit_full[q], ph, a.ctl, abort);
     if (!ok) return -1;
     const int u = bars->unit[q];
+    if (ui != nullptr) *ui = bars->uinfo[q];
     if (whole_warp) __syncwarp();
     if (!whole_warp || lane == 0) mbar_arrive(&bars->unit_empty[q]);
     ++n;
@@ -649,15 +678,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       uint32_t pn = 0;  // queue entries published
-      while (ok) {
-        // draw the next unit that holds a query, publish it (or the end)
-        const uint32_t q = pn % kUnitQueue;
-        if (pn >= uint32_t(kUnitQueue) &&
-            !mbar_wait(&bars->unit_empty[q], ((pn / kUnitQueue) & 1u) ^ 1u, a.ctl, abort))
-          break;
-        // The first unit of CTA i is unit i (its Q tiles load before the
-        // wait); the counter hands out the rest, from unit gridDim.x on.
-        UnitInfo ui;
+      // The first unit of CTA i is unit i (its Q tiles load before the
+      // wait); the counter hands out the rest, from unit gridDim.x on.  One-
+      // block units draw the counter one unit ahead: its round trip (over a
+      // microsecond while HBM is busy) then overlaps a unit's loads.
+      int ahead = -1;  // a counter draw taken ahead, or -1
+      auto draw = [&](UnitInfo& ui) -> int {
         int u;
         bool fixed = pn == 0;
         do {
@@ -666,20 +692,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             fixed = false;
           } else {
             dep_wait();
-            u = int(gridDim.x + atomicAdd(a.unit_ctr, 1u));
+            if (ahead >= 0) {
+              u = ahead;
+              ahead = -1;
+            } else {
+              u = int(gridDim.x + atomicAdd(a.unit_ctr, 1u));
+            }
           }
         } while (u < nunits && !unit_info<G, BN, WIN, (C::TOFF > 0)>(u, a, cu, nut, ui, true));
-        if (u >= nunits) u = -1;
+        return u < nunits ? u : -1;
+      };
+      // publish a unit that holds a query (or the end, -1) in the queue
+      auto publish = [&](int u, const UnitInfo& ui) -> bool {
+        const uint32_t q = pn % kUnitQueue;
+        if (pn >= uint32_t(kUnitQueue) &&
+            !mbar_wait(&bars->unit_empty[q], ((pn / kUnitQueue) & 1u) ^ 1u, a.ctl, abort))
+          return false;
         bars->unit[q] = u;
+        bars->uinfo[q] = ui;
         mbar_arrive(&bars->unit_full[q]);
         ++pn;
-        if (u < 0) break;
+        return true;
+      };
+      UnitInfo ui;
+      int u = draw(ui);
+      ok = publish(u, ui);
+      while (ok && u >= 0) {
         const int k0pos = ui.kstart;
         // Several blocks: K_0 first (its stage frees while the previous
         // unit finishes), then the two Q tiles, then K_1, V_0, K_2, V_1, ...  One
         // block: the Q tiles first -- a tile's buffer frees with its S MMA of
         // the previous unit and its RoPE heads the tile's next chain -- then
-        // K_0, V_0.
+        // K_0, the next unit's queue entry (the softmax warps read it while
+        // this unit's S products run), V_0.
         // (The CTA's first unit loads its Q tiles before K_0: they need no
         // wait for the kernel before this one.)
         const bool q_first = pn == 1;
@@ -706,6 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++qf;
         }
         if (!ONE && q_first && ok) ok = load_k(ui, k0pos, true);
+        UnitInfo nui;
+        int nu = -1;
         if constexpr (ONE) {
           // the unit's K block (slots 0-2) once the previous unit's S_B is
           // done, its V block (slots 3-4) once its PV_B is: the phases of
@@ -718,6 +765,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 3; ++i)
               tma_load_3d(ring + i * C::kSlot, kmap(i), &bars->kv_full[0], 64 * i,
                           kv_c1(ui, k0pos), kv_c2(ui, k0pos));
+          }
+          if (ok) {
+            nu = draw(nui);
+            ok = publish(nu, nui);
+            if (nu >= 0) ahead = int(gridDim.x + atomicAdd(a.unit_ctr, 1u));
           }
           // (and once tile A's TMA stores of the previous unit's O have read
           // their staging out of the V stage)
@@ -740,7 +792,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j + 1 < ui.nblk) ok = load_k(ui, vpos + BN, false);
             if (ok) ok = load_v(ui, vpos);
           }
+          if (ok) {
+            nu = draw(nui);
+            ok = publish(nu, nui);
+          }
         }
+        u = nu;
+        ui = nui;
       }
       // never leave with copies in flight into this CTA's shared memory
       if (qfills0) mbar_wait_drain(&bars->q_full[0], (qfills0 - 1) & 1u, a.ctl);
@@ -1021,30 +1079,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
+    // RoPE angles of this row's token in unit x: the G lanes holding one
+    // token's heads each evaluate 32/G of the 32 and exchange them by
+    // shuffles when rotating.
+    auto angles = [&](const UnitInfo& x, float2 (&cs)[32 / G]) {
+      const int pos = x.P + x.t0 + t * TQ + tl + a.rope_off;
+#pragma unroll
+      for (int k2 = 0; k2 < 32 / G; ++k2)
+        cs[k2] = rope_cos_sin(pos, a.freqs.hi[hl + G * k2], a.freqs.lo[hl + G * k2]);
+    };
     bool ok = true;
     uint32_t rn = 0;
+    // One-block units take the next unit and its angles from the queue while
+    // their own S product runs (the epilogue's TMA stores leave that time
+    // free), so that the next Q tile's RoPE follows the softmax directly.
+    UnitInfo ui;
+    int u = ONE ? read_unit(rn, true, &ui) : 0;
+    float2 cs_own[32 / G];
+    if (ONE && u >= 0) angles(ui, cs_own);
     while (true) {
-      const int u = read_unit(rn, true);
+      if constexpr (!ONE) u = read_unit(rn, true);
       if (u < 0) {
         ok = !*abort;
         break;
       }
-      UnitInfo ui;
-      unit_info<G, BN, WIN, (C::TOFF > 0)>(u, a, cu, nut, ui);
+      if constexpr (!ONE) {
+        unit_info<G, BN, WIN, (C::TOFF > 0)>(u, a, cu, nut, ui);
+        angles(ui, cs_own);
+      }
       const int qmin = ui.P + ui.t0 + t * TQ;    // position of the tile's first token
       const int qpos = qmin + tl;
       const int qidx = qpos - ui.P;              // this row's index among the new tokens
       // RoPE of this row's dims 0..63 (box 0, 128-byte row, 16-byte chunks
       // swizzled by row % 8): pairs (i, i + 32) live in chunks c and c + 4.
-      // The G lanes holding one token's heads each evaluate 32/G of the 32
-      // angles (while the tile's Q is still loading) and exchange them by
-      // shuffles.
       {
-        float2 cs_own[32 / G];
-#pragma unroll
-        for (int k2 = 0; k2 < 32 / G; ++k2)
-          cs_own[k2] = rope_cos_sin(qpos + a.rope_off, a.freqs.hi[hl + G * k2],
-                                    a.freqs.lo[hl + G * k2]);
         if (!warp_wait(&bars->q_full[t], uc & 1u, a.ctl, abort)) { ok = false; break; }
         uint8_t* qrow = smem + C::kOffQ + t * C::kQBytes + r * 128;
         uint4 ch[8];
@@ -1081,7 +1149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY;  // running max (log2 units); the sink joins at the end
       float l = 0.f;
       const int qmax = qmin + TQ - 1;
+      UnitInfo nui;
+      int nu = -1;
+      float2 ncs[32 / G];
       if constexpr (ONE) {
+        nu = read_unit(rn, true, &nui);
+        if (nu >= 0) angles(nui, ncs);
         if (!warp_wait(&bars->s_full[t], blk & 1u, a.ctl, abort)) { ok = false; break; }
         tc_fence_after();
         const int kb = ui.kstart + t * C::TOFF;  // position of column 0 (may be < 0)
@@ -1127,6 +1200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       pfull = ui.t0 + (t + 1) * TQ <= ui.L;
       puc = uc;
       ++uc;
+      if constexpr (ONE) {
+        u = nu;
+        ui = nui;
+#pragma unroll
+        for (int k2 = 0; k2 < 32 / G; ++k2) cs_own[k2] = ncs[k2];
+      }
     }
     if (ok && have_prev) epilogue();
     // the TMA stores of O complete before the CTA's shared memory goes
