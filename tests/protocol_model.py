@@ -464,3 +464,40 @@ def split_kv_decode(items, seed, nst=5, epilogue_on_pv_done=False):
         b.complete_tx(1)
 
     _schedule(rnd, {"producer": producer(), "mma": mma(), "rows": rows()}, fifo, tma, on_mma, on_land)
+
+
+def unit_queue(entries, readers, seed, nq=4, skip_empty_wait=False):
+    """The prefill's unit queue: the producer publishes `entries` unit indices
+    (then the end, -1) into nq slots, each with a full barrier (count 1) and
+    an empty barrier (one arrival per reader); every reader takes the entries
+    in order at its own pace -- the MMA issuer one per unit, the softmax warps
+    of one-block units one entry ahead of the unit they work on.  Planted
+    mistake: a producer that reuses a slot without its empty barrier."""
+    rnd = random.Random(seed)
+    full = [Bar(f"unit_full{q}", 1) for q in range(nq)]
+    empty = [Bar(f"unit_empty{q}", readers) for q in range(nq)]
+    slot = {}
+    seq = list(range(entries)) + [-1]
+
+    def producer():
+        for pn, u in enumerate(seq):
+            q = pn % nq
+            if pn >= nq and not skip_empty_wait:
+                yield ("wait", empty[q], ((pn // nq) & 1) ^ 1)
+            slot[q] = u
+            full[q].arrive()
+            yield ("step",)
+
+    def reader(i):
+        for n, want in enumerate(seq):
+            q = n % nq
+            yield ("wait", full[q], (n // nq) & 1)
+            if slot.get(q) != want:
+                raise RuntimeError(f"reader {i} took {slot.get(q)} as entry {n}, not {want}")
+            empty[q].arrive()
+            for _ in range(rnd.randint(0, 3)):  # its own work between entries
+                yield ("step",)
+
+    actors = {"producer": producer()}
+    actors.update({f"reader{i}": reader(i) for i in range(readers)})
+    _schedule(rnd, actors, [], [], None, None)

@@ -77,3 +77,21 @@ def test_split_kv_decode_catches_epilogue_on_pv_done_parity():
         except (AssertionError, RuntimeError):
             failures += 1
     assert failures > 0
+
+
+@pytest.mark.parametrize("entries", [1, 3, 4, 9, 30])
+def test_unit_queue_protocol(entries):
+    # the MMA issuer and the eight softmax warps read every entry once, in
+    # order, whatever their lead or lag
+    for seed in range(40):
+        pm.unit_queue(entries, 9, seed)
+
+
+def test_unit_queue_catches_slot_reuse_before_all_read():
+    failures = 0
+    for seed in range(60):
+        try:
+            pm.unit_queue(12, 9, seed, skip_empty_wait=True)
+        except RuntimeError:
+            failures += 1
+    assert failures > 0
