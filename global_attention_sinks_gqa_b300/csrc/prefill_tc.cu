@@ -32,7 +32,10 @@
 //               stages are released by tile B's rows, the V stage by a
 //               commit.  One block per unit: one K and one V stage whose
 //               release (and that of the Q tiles) the producer reads from the
-//               phases of the S and PV completion barriers.
+//               phases of the S and PV completion barriers; between a unit's
+//               K and V blocks it publishes the next unit (the work counter
+//               drawn a unit ahead), which the softmax warps take, with its
+//               RoPE angles, while their S products run.
 //   warp 1      TMEM allocator and single-thread MMA issuer, per key block j:
 //                 O_A += P_A,j V_j ; S_A = Q_A K_{j+1}^T ;
 //                 O_B += P_B,j V_j ; S_B = Q_B K_{j+1}^T
