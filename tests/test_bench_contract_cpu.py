@@ -67,3 +67,20 @@ def test_accounting_matches_brute_force_and_the_stated_workload_figures():
     assert bench.decode_bytes(lens, 4, 64, 8, 128) == kv + 3 * 4 * 64 * (384 + 256 + 4) + 64 * 4
     # the backward's minimal products: S, dP, dV, dQ, dK
     assert bench.BWD_PAIR_FLOPS == 2 * (192 + 128 + 128 + 192 + 192)
+
+
+def test_recorded_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """roofline.traffic is reported only while the kernel's sources match
+    the digest stored with the capture; otherwise null with the reason."""
+    import json
+    rec = {"prefill_swa_32k": {"kind": "prefill", "sources": bench.sources_digest("prefill"),
+                               "dram_bytes": 123, "profile": "profiles/x.md"},
+           "prefill_ga_32k": {"kind": "prefill", "sources": "0" * 16, "dram_bytes": 456,
+                              "profile": "profiles/y.md"}}
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("prefill_swa_32k") == (123, "profiles/x.md")
+    assert bench.recorded_traffic("prefill_ga_32k") == (None, "kernel changed since the capture")
+    assert bench.recorded_traffic("decode_ga") == (None, "no capture recorded")
+
